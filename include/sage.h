@@ -1,0 +1,179 @@
+/* sage.h — C ABI of libsage: quantized (Sage-style) attention forward on
+ * GB300 (sm_103a).
+ *
+ * The operation (sources are the titles and sections of the pages this
+ * library restates):
+ *   - "[ROCm] Add aiter_sage_attn attention backend for gfx1201 (RDNA4)",
+ *     section "Changes": INT8 QK^T, FP8 PV, FP32 accumulation; BF16 Q/K/V,
+ *     head dim 128, non-causal, softmax_scale passed through; causal, masks,
+ *     dropout and packed multi-sequence inputs are rejected rather than
+ *     computed differently.
+ *   - "new MHA v4 entrypoint ...", "Technical Details": INT8 and MXFP4 E2M1
+ *     Q/K with FP8 V and BF16 output; Q/K/V preprocessing kept in separate
+ *     calls from the attention call; quantized tensors live in packed
+ *     layouts owned by the library. "Motivation": conditional softmax
+ *     rescaling, base-2 exponentials.
+ *   - "[None][feat] Add VisualGen FA4 autotuning ...", first paragraph and
+ *     "Validation": output plus float32 LSE, 1-CTA / 2-CTA tiles, split-KV,
+ *     self- and cross-attention with ragged key lengths.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers to caller-owned memory (e.g. PyTorch
+ *     allocations) unless stated otherwise; the library never allocates,
+ *     frees or keeps them.
+ *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ *     NULL = legacy default stream); no call synchronises the host except
+ *     sage_last_device_status().
+ *   - Arguments are validated on the host before any launch; an invalid call
+ *     returns a negative status and launches nothing.
+ *   - Errors that only the device can see (a k_lens entry out of range, a
+ *     bounded wait that ran out) are OR-ed into a per-device status word that
+ *     sage_last_device_status() reads and clears.
+ *   - BF16 inputs use element strides (sage_strides_t) over a logical
+ *     [B][N][H][D] tensor; the D stride must be 1, the base pointer 16-byte
+ *     aligned and the b/n/h strides multiples of 8 elements.
+ *   - Head dimension D must be 128. Only sm_103 devices are accepted.
+ */
+#ifndef SAGE_H
+#define SAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* sage_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  SAGE_OK = 0,
+  SAGE_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad size or stride */
+  SAGE_ERR_UNSUPPORTED = -2,    /* D != 128, causal != 0, unknown format */
+  SAGE_ERR_WORKSPACE = -3,      /* workspace missing or smaller than required */
+  SAGE_ERR_CUDA = -4,           /* a CUDA runtime call failed */
+  SAGE_ERR_DEVICE_TIMEOUT = -5, /* a bounded device wait ran out (device word) */
+  SAGE_ERR_ARCH = -6,           /* current device is not sm_103 */
+  SAGE_ERR_DEVICE_ARG = -7      /* device-side argument check failed (k_lens) */
+} sage_status_t;
+
+/* Operand formats ("new MHA v4 entrypoint", Technical Details / Test Result). */
+typedef enum {
+  SAGE_FMT_QK_INT8_V_FP8 = 0,  /* Q/K INT8 per-128-token-block scales, V FP8 E4M3 */
+  SAGE_FMT_QK_MXFP4_V_FP8 = 1  /* Q/K MXFP4 E2M1 + E8M0 per 32 channels, V FP8 E4M3 */
+} sage_format_t;
+
+typedef struct {
+  int64_t b, n, h; /* element strides of a [B][N][H][D] tensor; D stride is 1 */
+} sage_strides_t;
+
+/* ---------------------------------------------------------------------------
+ * Quantized layouts (Npad = ceil(N/128)*128; padding and tokens past the
+ * per-batch length are written as zero codes):
+ *
+ * SAGE_FMT_QK_INT8_V_FP8, Q or K:
+ *   data  : [B][H][Npad][D] INT8 codes in [-127, 127], each held as an IEEE
+ *           binary16 value (exact; 2 bytes per code). sm_103a tensor cores
+ *           have no 8-bit integer MMA, so the attention kernel multiplies the
+ *           codes on the FP16 pipe, where every product and every partial sum
+ *           (|S| <= 128*127*127 < 2^24) is exact: the INT32 result is
+ *           reproduced bit for bit.
+ *   scale : [B][H][Npad/128] float, absmax/127 of each 128-token block.
+ * SAGE_FMT_QK_MXFP4_V_FP8, Q or K:
+ *   data  : [B][H][Npad][D/2] bytes, two E2M1 codes per byte, element 2i in
+ *           the low nibble.
+ *   scale : [B][H][Npad][D/32] E8M0 bytes (2^(byte-127)).
+ * V (both formats):
+ *   data  : [B][H][D][Npad] FP8 E4M3 codes, token-contiguous (V transposed).
+ *   scale : [B][H][D] float, absmax/448 of each channel over valid tokens.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes needed for a quantized tensor. which: 0 = Q/K data, 1 = Q/K scale,
+ * 2 = V data, 3 = V scale. Returns 0 for invalid arguments. */
+size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, int64_t H,
+                            int64_t D);
+
+/* Workspace bytes. op: 0 = sage_quantize_qk (always 0), 1 = sage_quantize_v
+ * (per-channel partial maxima), 2 = sage_attn_fwd with `num_splits` KV
+ * splits (0 = the split count the library would choose). */
+size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int64_t Nq,
+                            int64_t Nk, int64_t D, int num_splits);
+
+/* Quantize Q or K ("new MHA v4 entrypoint": sage_quant_kernel /
+ * sage_quant_mxfp4 preprocessing; INT8 reading: one FP32 scale absmax/127 per
+ * 128-token block per (b,h), codes clamp(rne(x/s), -127, 127) with an IEEE
+ * FP32 division; MXFP4 reading: OCP Microscaling shared exponent
+ * floor(log2 amax) - 2 per 32 channels, E2M1 codes rounded to nearest even
+ * with saturation at 6).
+ *   x       : BF16 [B][N][H][D] with strides xs.
+ *   lens    : nullable int32 [B] device array of valid token counts
+ *             (0 <= lens[b] <= N); tokens >= lens[b] are excluded from the
+ *             maxima and written as zero codes. NULL = all N valid.
+ *   x_q     : output data (layout above), sage_quantized_bytes(fmt,0,...) bytes.
+ *   x_scale : output scales, sage_quantized_bytes(fmt,1,...) bytes. */
+sage_status_t sage_quantize_qk(sage_format_t fmt, const void* x, sage_strides_t xs, int64_t B,
+                               int64_t N, int64_t H, int64_t D, const int32_t* lens, void* x_q,
+                               void* x_scale, sage_stream_t stream);
+
+/* Quantize V to FP8 E4M3 ("new MHA v4 entrypoint": sage_quant_v_amax_partial,
+ * sage_quant_v_amax_finalize and sage_quant_v kernels; reading: one FP32
+ * scale absmax/448 per (b,h,channel) over valid tokens, codes E4M3 with round
+ * to nearest even and saturation, written token-contiguous).
+ * Two launches: partial maxima into `workspace`, then finalize + quantize.
+ *   workspace : device scratch of at least sage_workspace_bytes(1, ...) bytes,
+ *               16-byte aligned; contents on entry are ignored. */
+sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64_t N, int64_t H,
+                              int64_t D, const int32_t* lens, void* v_q, float* v_scale,
+                              void* workspace, size_t ws_bytes, sage_stream_t stream);
+
+typedef struct {
+  int32_t num_splits; /* KV splits: 0 = library choice, 1 = no split, >1 = forced */
+  int32_t cta_mode;   /* reserved: 0 = library choice */
+} sage_attn_options_t;
+
+/* Attention forward ("[ROCm] Add aiter_sage_attn ...", Changes; "new MHA v4
+ * entrypoint", Motivation; "[None][feat] Add VisualGen FA4 autotuning",
+ * first paragraph):
+ *   t_ij  = S_ij * s_q * s_k * softmax_scale * log2(e)   (S exact integer)
+ *   M_i   = ceil(max_j t_ij), raised tile by tile; O and l are rescaled by an
+ *           exact power of two only when it grows (conditional rescaling)
+ *   p_ij  = 2^(t_ij - M_i),  l_i = sum_j p_ij,  P8_ij = E4M3(p_ij * 2^8)
+ *   O_id  = sum_j dq(P8_ij) 2^-8 dq(V8_dj) s_v[d] / l_i          -> BF16
+ *   LSE_i = (M_i + log2 l_i) ln 2  (natural-log LSE of the logits)  -> FP32
+ *   q_q, q_scale, k_q, k_scale : quantized Q/K from sage_quantize_qk (fmt).
+ *   v_q, v_scale : quantized V from sage_quantize_v.
+ *   k_lens     : nullable int32 [B] device array of valid key counts
+ *                (0 <= k_lens[b] <= Nk; a 0 gives O = 0 and LSE = -inf);
+ *                an entry out of range sets SAGE_ERR_DEVICE_ARG in the
+ *                device status word and that batch's outputs are not written.
+ *   softmax_scale : <= 0 selects 1/sqrt(D).
+ *   causal     : must be 0.
+ *   o          : BF16 [B][Nq][H][D] output with strides os.
+ *   lse        : nullable float [B][H][Nq] contiguous output.
+ *   workspace  : split-KV scratch, sage_workspace_bytes(2, ...) bytes
+ *                (may be NULL when that is 0).
+ *   opts       : nullable; see sage_attn_options_t. */
+sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_scale,
+                            const void* k_q, const void* k_scale, const void* v_q,
+                            const float* v_scale, const int32_t* k_lens, int64_t B, int64_t H,
+                            int64_t Nq, int64_t Nk, int64_t D, float softmax_scale, int causal,
+                            void* o, sage_strides_t os, float* lse, void* workspace,
+                            size_t ws_bytes, const sage_attn_options_t* opts,
+                            sage_stream_t stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char* sage_status_string(sage_status_t st);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: SAGE_OK, SAGE_ERR_DEVICE_ARG or SAGE_ERR_DEVICE_TIMEOUT (the most
+ * severe seen since the last read), or SAGE_ERR_CUDA if the sync failed. */
+sage_status_t sage_last_device_status(sage_stream_t stream);
+
+/* Library version string. */
+const char* sage_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SAGE_H */

@@ -1,0 +1,220 @@
+"""CPU oracle for quantized (Sage-style) attention forward — TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package. It is a ctypes wrapper over ``sage_oracle.cpp`` (plain
+C++, FP64 arithmetic) and shares nothing with the CUDA library.
+
+Parity pins live in ``tests/test_oracle.py``; every function below is pinned
+there against brute force, closed forms, invariants or a library routine.
+
+Arrays: BF16 inputs are passed as ``numpy.uint16`` bit patterns with shape
+``[B, N, H, D]`` (any strides, unit stride along D).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sage_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+LOG2E = 1.4426950408889634
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with g++ (IEEE arithmetic, no contraction)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= max(os.path.getmtime(_SRC),
+                                              os.path.getmtime(os.path.join(_HERE, "sage_oracle.h")))):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+           "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [D]
+        lib.oracle_e4m3_decode.restype = D
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+        lib.oracle_e2m1_encode.argtypes = [D]
+        lib.oracle_e2m1_decode.restype = D
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_int8_quantize_value.restype = I32
+        lib.oracle_int8_quantize_value.argtypes = [ctypes.c_float, ctypes.c_float]
+        lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        lib.oracle_bf16_from_double.argtypes = [D]
+        q_args = [P, I64, I64, I64, I64, I64, I64, I64, P, P, P]
+        for name in ("oracle_quantize_int8", "oracle_quantize_v_fp8", "oracle_quantize_mxfp4"):
+            getattr(lib, name).restype = None
+            getattr(lib, name).argtypes = q_args
+        lib.oracle_attention.restype = None
+        lib.oracle_attention.argtypes = [I32, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, D,
+                                         P, I64, P, P, P, I32]
+        lib.oracle_attention_exact.restype = None
+        lib.oracle_attention_exact.argtypes = [P, I64, I64, I64, P, I64, I64, I64, P, I64, I64,
+                                               I64, P, I64, I64, I64, I64, I64, D, P, I64, P, P,
+                                               I32]
+        for name in ("oracle_p8_final",):
+            getattr(lib, name).restype = None
+            getattr(lib, name).argtypes = [P, I64, P]
+        lib.oracle_p8_online.restype = None
+        lib.oracle_p8_online.argtypes = [P, I64, I64, P]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _bnhd(x: np.ndarray):
+    assert x.dtype == np.uint16 and x.ndim == 4 and x.strides[3] == 2, "BF16 bits [B,N,H,D], unit D stride"
+    B, N, H, D = x.shape
+    sb, sn, sh = (s // 2 for s in x.strides[:3])
+    return B, N, H, D, sb, sn, sh
+
+
+def _lens(lens) -> Optional[np.ndarray]:
+    return None if lens is None else np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+
+
+def pad128(n: int) -> int:
+    return (n + 127) // 128 * 128
+
+
+# ------------------------------------------------------------------ scalars
+def e4m3_encode(x: float) -> int:
+    return int(_L().oracle_e4m3_encode(float(x)))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(_L().oracle_e4m3_decode(int(c)))
+
+
+def e2m1_encode(x: float) -> int:
+    return int(_L().oracle_e2m1_encode(float(x)))
+
+
+def e2m1_decode(c: int) -> float:
+    return float(_L().oracle_e2m1_decode(int(c)))
+
+
+def int8_quantize_value(x: float, s: float) -> int:
+    return int(_L().oracle_int8_quantize_value(float(x), float(s)))
+
+
+def bf16_from_double(x: float) -> int:
+    return int(_L().oracle_bf16_from_double(float(x)))
+
+
+# ------------------------------------------------------------------ quantize
+def quantize_int8(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
+    """INT8 codes [B,H,Npad,D] and FP32 block scales [B,H,Npad/128]."""
+    B, N, H, D, sb, sn, sh = _bnhd(x)
+    Np = pad128(N)
+    q = np.zeros((B, H, Np, D), np.int8)
+    s = np.zeros((B, H, Np // 128), np.float32)
+    ln = _lens(lens)
+    _L().oracle_quantize_int8(_ptr(x), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(q), _ptr(s))
+    return q, s
+
+
+def quantize_v_fp8(v: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
+    """E4M3 codes [B,H,D,Npad] (token-contiguous) and FP32 scales [B,H,D]."""
+    B, N, H, D, sb, sn, sh = _bnhd(v)
+    Np = pad128(N)
+    v8 = np.zeros((B, H, D, Np), np.uint8)
+    sv = np.zeros((B, H, D), np.float32)
+    ln = _lens(lens)
+    _L().oracle_quantize_v_fp8(_ptr(v), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(v8), _ptr(sv))
+    return v8, sv
+
+
+def quantize_mxfp4(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Packed E2M1 codes [B,H,Npad,D/2] and E8M0 scales [B,H,Npad,D/32]."""
+    B, N, H, D, sb, sn, sh = _bnhd(x)
+    Np = pad128(N)
+    c = np.zeros((B, H, Np, D // 2), np.uint8)
+    e = np.zeros((B, H, Np, D // 32), np.uint8)
+    ln = _lens(lens)
+    _L().oracle_quantize_mxfp4(_ptr(x), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(c), _ptr(e))
+    return c, e
+
+
+# ------------------------------------------------------------------ attention
+def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: int = 128,
+              softmax_scale: Optional[float] = None, k_lens=None, rows=None,
+              want_weights: bool = False, nthreads: int = 0):
+    """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K. V is E4M3.
+
+    Returns (o [B,H,nrows,D] float64, lse [B,H,nrows] float64, w or None).
+    """
+    B, H = q.shape[0], q.shape[1]
+    c = 1.0 / math.sqrt(D) if softmax_scale is None or softmax_scale <= 0 else float(softmax_scale)
+    arrs = [np.ascontiguousarray(a) for a in (q, q_scale, k, k_scale, v8, sv)]
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nr = Nq if r is None else len(r)
+    o = np.zeros((B, H, nr, D), np.float64)
+    lse = np.zeros((B, H, nr), np.float64)
+    w = np.zeros((B, H, nr, Nk), np.float64) if want_weights else None
+    ln = _lens(k_lens)
+    _L().oracle_attention(fmt, *(_ptr(a) for a in arrs), _ptr(ln), B, H, Nq, Nk, D, c, _ptr(r),
+                          nr, _ptr(o), _ptr(lse), _ptr(w), nthreads)
+    return o, lse, w
+
+
+def attention_exact(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, softmax_scale=None,
+                    k_lens=None, rows=None, nthreads: int = 0):
+    """Unquantized FP64 softmax attention of BF16 inputs [B,N,H,D]."""
+    B, Nq, H, D, qsb, qsn, qsh = _bnhd(q)
+    _, Nk, _, _, ksb, ksn, ksh = _bnhd(k)
+    _, _, _, _, vsb, vsn, vsh = _bnhd(v)
+    c = 1.0 / math.sqrt(D) if softmax_scale is None or softmax_scale <= 0 else float(softmax_scale)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nr = Nq if r is None else len(r)
+    o = np.zeros((B, H, nr, D), np.float64)
+    lse = np.zeros((B, H, nr), np.float64)
+    ln = _lens(k_lens)
+    _L().oracle_attention_exact(_ptr(q), qsb, qsn, qsh, _ptr(k), ksb, ksn, ksh, _ptr(v), vsb, vsn,
+                                vsh, _ptr(ln), B, H, Nq, Nk, D, c, _ptr(r), nr, _ptr(o), _ptr(lse),
+                                nthreads)
+    return o, lse
+
+
+def p8_final(t: np.ndarray) -> np.ndarray:
+    t = np.ascontiguousarray(t, dtype=np.float64)
+    out = np.zeros_like(t)
+    _L().oracle_p8_final(_ptr(t), len(t), _ptr(out))
+    return out
+
+
+def p8_online(t: np.ndarray, tile: int) -> np.ndarray:
+    t = np.ascontiguousarray(t, dtype=np.float64)
+    out = np.zeros_like(t)
+    _L().oracle_p8_online(_ptr(t), len(t), tile, _ptr(out))
+    return out
+
+
+def bf16_round(o: np.ndarray) -> np.ndarray:
+    """Round float64 values to BF16 (returned as uint16 bit patterns)."""
+    f = np.vectorize(bf16_from_double, otypes=[np.uint16])
+    return f(o)

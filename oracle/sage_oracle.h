@@ -1,0 +1,90 @@
+/* CPU oracle for quantized (Sage-style) attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. This is the plain, slow, obviously-correct
+ * restatement of what the GPU path computes; only the tests, the smoke check
+ * and the benchmark's CPU-baseline leg may load it. It shares no code, header,
+ * table or constant with the CUDA library.
+ *
+ * All arrays are host memory, C order, owned by the caller.
+ * BF16 values are passed as their raw 16-bit patterns (uint16_t).
+ * Element strides (sb, sn, sh) describe a [B][N][H][D] input with unit D
+ * stride.  `lens` (nullable) gives the number of valid tokens per batch.
+ * `nthreads` <= 0 means "all hardware threads".
+ */
+#ifndef SAGE_ORACLE_H
+#define SAGE_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- scalar format helpers (exposed so the tests can pin them) ---- */
+uint8_t oracle_e4m3_encode(double x);          /* RNE, saturate to +-448 */
+double oracle_e4m3_decode(uint8_t code);
+uint8_t oracle_e2m1_encode(double x);          /* RNE, saturate to +-6, 4-bit code */
+double oracle_e2m1_decode(uint8_t code);
+int oracle_int8_quantize_value(float x, float s); /* clamp(rne(x/s), -127, 127) */
+
+/* ---- quantization ---- */
+/* INT8 per-(b,h,128-token block) symmetric absmax.
+ * q: int8 [B][H][Npad][D], Npad = ceil(N/128)*128, padding rows 0.
+ * scale: float [B][H][Npad/128]. */
+void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+                          int64_t N, int64_t H, int64_t D, const int32_t* lens, int8_t* q,
+                          float* scale);
+/* FP8 E4M3 per-(b,h,channel) absmax over valid tokens, stored transposed:
+ * v8: uint8 [B][H][D][Npad] (token-contiguous), padding 0. sv: float [B][H][D]. */
+void oracle_quantize_v_fp8(const uint16_t* v, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+                           int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* v8,
+                           float* sv);
+/* MXFP4: per 32 consecutive channels of one token, shared E8M0 exponent and
+ * E2M1 elements. codes: uint8 [B][H][Npad][D/2] (element 2i in the low
+ * nibble), e8m0: uint8 [B][H][Npad][D/32]. Padding rows: codes 0, e8m0 0. */
+void oracle_quantize_mxfp4(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+                           int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* codes,
+                           uint8_t* e8m0);
+
+/* ---- attention ---- */
+/* fmt 0: q_data/k_data are int8 [B][H][Npad][D] with float block scales
+ *        [B][H][Npad/128];
+ * fmt 1: q_data/k_data are MXFP4 codes [B][H][Npad][D/2] with e8m0 scales
+ *        [B][H][Npad][D/32] (passed through q_scale/k_scale as bytes).
+ * V: fp8 [B][H][D][Nk_pad] + sv [B][H][D].
+ * rows (nullable): the query indices to evaluate (same set for every b,h);
+ * nrows = number of them (rows == NULL: all Nq).
+ * Outputs, for the evaluated rows only:
+ *   o: double [B][H][nrows][D] (before BF16 rounding), lse: double [B][H][nrows],
+ *   w (nullable): double [B][H][nrows][Nk] effective weights dq(P8)/256/l
+ *   (0 for masked keys). */
+void oracle_attention(int fmt, const void* q_data, const void* q_scale, const void* k_data,
+                      const void* k_scale, const uint8_t* v8, const float* sv,
+                      const int32_t* k_lens, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                      int64_t D, double softmax_scale, const int64_t* rows, int64_t nrows,
+                      double* o, double* lse, double* w, int nthreads);
+
+/* Unquantized FP64 softmax attention on the BF16 inputs ([B][N][H][D] with
+ * strides), for accuracy reporting and self-tests. Same output layout. */
+void oracle_attention_exact(const uint16_t* q, int64_t qsb, int64_t qsn, int64_t qsh,
+                            const uint16_t* k, int64_t ksb, int64_t ksn, int64_t ksh,
+                            const uint16_t* v, int64_t vsb, int64_t vsn, int64_t vsh,
+                            const int32_t* k_lens, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                            int64_t D, double softmax_scale, const int64_t* rows, int64_t nrows,
+                            double* o, double* lse, int nthreads);
+
+/* Tile-ordered online variant of the FP8 probability step for one row of
+ * log2-domain logits t[0..n): the running maximum is an integer and is raised
+ * tile by tile; each tile's probabilities are encoded against the running
+ * maximum. Returns, per element, dq(P8)*2^(m_run - M_final) / 256 so the
+ * result can be compared with the final-maximum encoding. */
+void oracle_p8_online(const double* t, int64_t n, int64_t tile, double* p_eff);
+/* Final-maximum encoding of the same row: dq(E4M3(2^(t-M)*256))/256. */
+void oracle_p8_final(const double* t, int64_t n, double* p_eff);
+
+/* BF16 round-to-nearest-even of a double (for the output conversion). */
+uint16_t oracle_bf16_from_double(double x);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,394 @@
+"""Pins for the CPU oracle: every oracle function is checked against something
+other than itself — brute force over the format tables, a library routine
+(torch's float8/bfloat16 conversions, SDPA, scipy's logsumexp/softmax),
+closed forms and invariants — so that a dropped term, a wrong sign, index or
+layout fails at least one test.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from precision_attention_diffusion_sage_gb300.inputs import WORKLOADS, Workload, bf16_bits, make_qkv
+
+L2E = 1.4426950408889634
+
+
+# ------------------------------------------------------------------ format tables
+def _e4m3_table():
+    """(code, value) for every finite E4M3 code, decoded by torch's float8_e4m3fn."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    return codes, vals
+
+
+def _nearest_even(x, codes, vals, max_mag):
+    """Brute force: the table value nearest to x; ties to the even code."""
+    a = min(abs(x), max_mag)
+    mags = np.abs(vals)
+    d = np.abs(mags - a)
+    best = d.min()
+    cand = [int(c) & 0x7F for c, v, dd in zip(codes, vals, d) if dd == best and v >= 0]
+    even = [c for c in cand if c % 2 == 0]
+    mag_code = even[0] if even else cand[0]
+    return mag_code
+
+
+def test_e4m3_decode_matches_torch():
+    codes, vals = _e4m3_table()
+    for c, v in zip(codes, vals):
+        assert oracle.e4m3_decode(int(c)) == v
+    assert math.isnan(oracle.e4m3_decode(0x7F))
+
+
+def test_e4m3_encode_bruteforce_and_torch():
+    codes, vals = _e4m3_table()
+    pos = sorted(set(float(v) for v in vals if v >= 0))
+    xs = list(pos)
+    xs += [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]        # exact ties
+    xs += [a * (1 + 1e-9) for a in pos[1:]] + [a * (1 - 1e-9) for a in pos[1:]]
+    rng = np.random.default_rng(0)
+    xs += list(np.exp2(rng.uniform(-12, 9.5, 2000)))
+    xs += [449.0, 463.9, 464.0, 500.0, 1e6, float("inf")]
+    for x in xs:
+        for s in (1.0, -1.0):
+            got = oracle.e4m3_encode(s * x)
+            want_mag = _nearest_even(x, codes, vals, 448.0)
+            want = want_mag | (0x80 if s < 0 else 0)
+            assert got == want, (s * x, got, want)
+            if x <= 448.0:  # torch's conversion is RNE without saturation
+                t = torch.tensor([s * x], dtype=torch.float64).to(torch.float8_e4m3fn)
+                assert int(t.view(torch.uint8)[0]) == got, (s * x,)
+
+
+def test_e4m3_hand_cases():
+    # OCP E4M3: 1.0 = 0.0111.000, 448 = 0.1111.110, 2^-9 = 0.0000.001, 2^-6 = 0.0001.000
+    assert oracle.e4m3_encode(1.0) == 0x38
+    assert oracle.e4m3_encode(448.0) == 0x7E
+    assert oracle.e4m3_encode(2.0 ** -9) == 0x01
+    assert oracle.e4m3_encode(2.0 ** -6) == 0x08
+    assert oracle.e4m3_encode(1.0625) == 0x38       # tie -> even mantissa (1.0)
+    assert oracle.e4m3_encode(1.1875) == 0x3A       # tie -> even mantissa (1.25)
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00   # subnormal tie -> 0
+    assert oracle.e4m3_encode(-(2.0 ** -10)) == 0x80
+    assert oracle.e4m3_encode(1e9) == 0x7E          # saturation
+    assert oracle.e4m3_encode(256.0) == 0x78
+
+
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_bruteforce():
+    codes = np.arange(16, dtype=np.uint8)
+    vals = np.array([E2M1[c & 7] * (-1 if c & 8 else 1) for c in codes])
+    for c in codes:
+        assert oracle.e2m1_decode(int(c)) == vals[c]
+    xs = list(E2M1) + [(a + b) / 2 for a, b in zip(E2M1[:-1], E2M1[1:])]
+    xs += list(np.random.default_rng(1).uniform(0, 8, 3000)) + [6.5, 7.0, 100.0]
+    for x in xs:
+        for s in (1.0, -1.0):
+            mag = _nearest_even(x, codes[:8], vals[:8], 6.0)
+            want = mag | (0x8 if s < 0 else 0)
+            assert oracle.e2m1_encode(s * x) == want, (s * x,)
+
+
+def test_e2m1_hand_cases():
+    # ties to even mantissa: 0.25->0, 0.75->1.0, 1.25->1.0, 1.75->2, 2.5->2, 3.5->4, 5->4
+    for x, c in [(0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6),
+                 (7.0, 7), (6.0, 7), (0.5, 1), (3.0, 5)]:
+        assert oracle.e2m1_encode(x) == c, x
+    assert oracle.e2m1_encode(-0.1) == 0x8
+
+
+def test_int8_value_hand_cases():
+    assert oracle.int8_quantize_value(2.5, 1.0) == 2      # ties to even
+    assert oracle.int8_quantize_value(3.5, 1.0) == 4
+    assert oracle.int8_quantize_value(-2.5, 1.0) == -2
+    assert oracle.int8_quantize_value(-200.0, 1.0) == -127  # symmetric clamp
+    s = np.float32(3.0) / np.float32(127.0)
+    assert oracle.int8_quantize_value(3.0, float(s)) == 127
+    assert oracle.int8_quantize_value(-3.0, float(s)) == -127
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(2)
+    xs = np.concatenate([rng.standard_normal(3000) * 10.0 ** rng.integers(-5, 5, 3000),
+                         [0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1e-40, 3e38]])
+    want = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_round(xs)
+    np.testing.assert_array_equal(got, want)
+
+
+# ------------------------------------------------------------------ quantization
+def _tiny(lens=None, seed=None, N=None):
+    w = WORKLOADS["tiny"]
+    if N is not None:
+        w = Workload("t", w.B, w.H, N, N, seed=w.seed, structure=w.structure)
+    q, k, v = make_qkv(w, seed=seed)
+    return w, q, k, v
+
+
+def _f32(x_bits):
+    return (x_bits.astype(np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("N,lens", [(256, None), (300, None), (300, [173])])
+def test_quantize_int8(N, lens):
+    w, q, k, v = _tiny(N=N)
+    x = bf16_bits(k)
+    codes, scale = oracle.quantize_int8(x, lens=lens)
+    xf = _f32(x)  # [B,N,H,D]
+    B, _, H, D = xf.shape
+    nv = lens[0] if lens else N
+    for b in range(B):
+        for h in range(H):
+            for blk in range(scale.shape[2]):
+                n0, n1 = blk * 128, min(blk * 128 + 128, nv)
+                blkx = xf[b, n0:n1, h, :]
+                amax = np.float32(np.abs(blkx).max()) if n1 > n0 else np.float32(0)
+                s = np.float32(amax / np.float32(127.0))
+                assert scale[b, h, blk] == s
+                c = codes[b, h, blk * 128:(blk + 1) * 128].astype(np.int32)
+                assert np.all(c[max(0, n1 - n0):] == 0)          # padding / past lens
+                if n1 > n0:
+                    cc = c[:n1 - n0]
+                    assert np.abs(cc).max() == 127                # the absmax maps to 127
+                    err = np.abs(blkx.astype(np.float64) - cc * np.float64(s))
+                    # half a step, plus the binary32 rounding of x/s (|x/s| <= 127, 2^-24 relative)
+                    assert err.max() <= s * (0.5 + 127 * 2.0 ** -24)
+                    ref = np.clip(np.rint(blkx / s), -127, 127)   # numpy binary32 division
+                    np.testing.assert_array_equal(cc, ref)
+
+
+@pytest.mark.parametrize("N,lens", [(256, None), (300, [211])])
+def test_quantize_v_fp8(N, lens):
+    w, q, k, v = _tiny(N=N)
+    x = bf16_bits(v)
+    v8, sv = oracle.quantize_v_fp8(x, lens=lens)
+    xf = _f32(x)
+    B, _, H, D = xf.shape
+    nv = lens[0] if lens else N
+    Np = oracle.pad128(N)
+    assert v8.shape == (B, H, D, Np)
+    for b in range(B):
+        for h in range(H):
+            amax = np.abs(xf[b, :nv, h, :]).max(axis=0)               # per channel
+            s = (amax / np.float32(448.0)).astype(np.float32)
+            np.testing.assert_array_equal(sv[b, h], s)
+            ratio = (xf[b, :nv, h, :] / s[None, :]).astype(np.float32)  # [n, d]
+            want = torch.from_numpy(ratio).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            np.testing.assert_array_equal(v8[b, h, :, :nv], want.T)   # token-contiguous
+            assert np.all(v8[b, h, :, nv:] == 0)
+            # every channel's absmax element encodes to +-448
+            top = np.abs(v8[b, h, np.arange(D), np.abs(xf[b, :nv, h, :]).argmax(axis=0)])
+            assert np.all((top & 0x7F) == 0x7E)
+
+
+@pytest.mark.parametrize("lens", [None, [100]])
+def test_quantize_mxfp4(lens):
+    w, q, k, v = _tiny()
+    x = bf16_bits(q)
+    codes, e8 = oracle.quantize_mxfp4(x, lens=lens)
+    xf = _f32(x).astype(np.float64)
+    B, N, H, D = xf.shape
+    nv = lens[0] if lens else N
+    codes_tab = np.arange(8, dtype=np.uint8)
+    vals_tab = np.array(E2M1)
+    for b in range(B):
+        for h in range(H):
+            for n in range(0, oracle.pad128(N), 7 if lens is None else 1):
+                if n >= nv:
+                    assert np.all(codes[b, h, n] == 0) and np.all(e8[b, h, n] == 0)
+                    continue
+                for g in range(D // 32):
+                    grp = xf[b, n, h, g * 32:(g + 1) * 32]
+                    amax = np.abs(grp).max()
+                    e = int(np.floor(np.log2(amax))) - 2
+                    assert e8[b, h, n, g] == e + 127
+                    X = 2.0 ** e
+                    for i in range(32):
+                        byte = codes[b, h, n, g * 16 + i // 2]
+                        c = (byte >> (4 * (i % 2))) & 0xF
+                        y = grp[i] / X
+                        mag = _nearest_even(y, codes_tab, vals_tab, 6.0)
+                        assert c == (mag | (0x8 if y < 0 or (y == 0 and math.copysign(1, y) < 0) else 0))
+
+
+def test_mxfp4_nibble_order_and_scale_closed_form():
+    x = np.zeros((1, 1, 1, 128), np.float32)
+    x[0, 0, 0, 0] = 6.0 * 2.0 ** 5     # element 0 -> +6 at scale 2^5
+    x[0, 0, 0, 1] = -1.0 * 2.0 ** 5    # element 1 -> -1
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    codes, e8 = oracle.quantize_mxfp4(bits)
+    assert e8[0, 0, 0, 0] == 127 + 5
+    assert codes[0, 0, 0, 0] == (0x7 | (0xA << 4))   # low nibble = element 0
+    assert e8[0, 0, 0, 1] == 0 and np.all(codes[0, 0, 0, 16:] == 0)  # all-zero group
+
+
+# ------------------------------------------------------------------ attention
+def _dequant_int8(codes, scale):
+    B, H, Np, D = codes.shape
+    return codes.astype(np.float64) * np.repeat(scale.astype(np.float64), 128, axis=2)[..., None]
+
+
+def _dequant_mxfp4(codes, e8):
+    lo = codes & 0xF
+    hi = codes >> 4
+    c = np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
+    mag = np.array(E2M1)[c & 7] * np.where(c & 8, -1.0, 1.0)
+    return mag * np.repeat(np.exp2(e8.astype(np.float64) - 127), 32, axis=-1)
+
+
+def _dequant_v(v8, sv):
+    tab = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    return tab[v8] * sv.astype(np.float64)[..., None]     # [B,H,D,Np]
+
+
+def _quantize_all(q, k, v, fmt, k_lens=None):
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    if fmt == 0:
+        qq, qs = oracle.quantize_int8(qb)
+        kq, ks = oracle.quantize_int8(kb, lens=k_lens)
+        qd, kd = _dequant_int8(qq, qs), _dequant_int8(kq, ks)
+    else:
+        qq, qs = oracle.quantize_mxfp4(qb)
+        kq, ks = oracle.quantize_mxfp4(kb, lens=k_lens)
+        qd, kd = _dequant_mxfp4(qq, qs), _dequant_mxfp4(kq, ks)
+    v8, sv = oracle.quantize_v_fp8(vb, lens=k_lens)
+    return (qq, qs, kq, ks, v8, sv), (qd, kd, _dequant_v(v8, sv))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_attention_lse_weights_and_output(fmt):
+    w, q, k, v = _tiny()
+    Nq, Nk, D = w.Nq, w.Nk, w.D
+    c = 1.0 / math.sqrt(D)
+    qz, (qd, kd, vd) = _quantize_all(q, k, v, fmt)
+    o, lse, wts = oracle.attention(fmt, *qz, Nq=Nq, Nk=Nk, want_weights=True)
+    z = c * np.einsum("bhid,bhjd->bhij", qd[:, :, :Nq], kd[:, :, :Nk])    # natural-log logits
+    # LSE is the logsumexp of the dequantized logits (no FP8 step involved)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(z, axis=-1), rtol=0, atol=1e-9)
+    # weights: FP8 rounding of the softmax, within half an E4M3 step (2^-4 relative)
+    sm = scipy.special.softmax(z, axis=-1)
+    assert np.all(np.abs(wts - sm) <= sm * 2.0 ** -4 + 2.0 ** -18)
+    np.testing.assert_allclose(wts.sum(-1), 1.0, atol=2.0 ** -4)
+    # each weight is exactly E4M3(p*256)/256/l with the integer maximum (brute force)
+    codes, vals = _e4m3_table()
+    t = z * L2E
+    M = np.ceil(t.max(-1, keepdims=True))
+    p = np.exp2(t - M)
+    l = p.sum(-1, keepdims=True)
+    for (b, h, i) in [(0, 0, 0), (0, 1, 77), (0, 0, 255)]:
+        for j in range(0, Nk, 5):
+            mag = _nearest_even(p[b, h, i, j] * 256.0, codes, vals, 448.0)
+            want = torch.tensor([mag], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
+            assert wts[b, h, i, j] == pytest.approx(want / 256.0 / l[b, h, i, 0], rel=1e-12)
+    # output is the weighted sum of the dequantized V rows
+    ref = np.einsum("bhij,bhdj->bhid", wts, vd[..., :Nk])
+    np.testing.assert_allclose(o, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_attention_special_cases():
+    w, q, k, v = _tiny()
+    Nq, Nk = w.Nq, w.Nk
+    # constant V: every output row is the dequantized constant (weights sum ~1 is not enough:
+    # O = sum w * v exactly, so O/v = sum w; check against sum of weights)
+    vc = torch.full_like(v, 0.75)
+    qz, (qd, kd, vd) = _quantize_all(q, k, vc, 0)
+    o, lse, wts = oracle.attention(0, *qz, Nq=Nq, Nk=Nk, want_weights=True)
+    np.testing.assert_allclose(o, wts.sum(-1, keepdims=True) * vd[:, :, :, :1].transpose(0, 1, 3, 2),
+                               rtol=1e-12)
+    assert np.all(np.abs(o - 0.75) <= 0.75 * 2.0 ** -4)
+    # softmax_scale -> 0: uniform weights, O = mean of dequantized V, LSE = ln Nk
+    qz, (qd, kd, vd) = _quantize_all(q, k, v, 0)
+    o, lse, wts = oracle.attention(0, *qz, Nq=Nq, Nk=Nk, softmax_scale=1e-30, want_weights=True)
+    np.testing.assert_allclose(wts, 1.0 / Nk, rtol=1e-12)
+    np.testing.assert_allclose(o, np.broadcast_to(vd[..., :Nk].mean(-1)[:, :, None, :], o.shape),
+                               rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(lse, math.log(Nk), rtol=1e-9)
+    # a single key: O is that key's value row up to the P8 rounding of p
+    o1, lse1, _ = oracle.attention(0, *qz, Nq=Nq, Nk=Nk, k_lens=[1])
+    assert np.all(np.abs(o1 - vd[:, :, None, :, 0]) <= np.abs(vd[:, :, None, :, 0]) * 2.0 ** -4 + 1e-12)
+    # zero valid keys: empty softmax
+    o0, lse0, _ = oracle.attention(0, *qz, Nq=Nq, Nk=Nk, k_lens=[0])
+    assert np.all(o0 == 0) and np.all(np.isneginf(lse0))
+
+
+def test_attention_block_permutation_invariance():
+    """Permuting whole 128-key blocks of K/V (their scales move with them)
+    leaves every output unchanged."""
+    w, q, k, v = _tiny()
+    qz, _ = _quantize_all(q, k, v, 0)
+    qq, qs, kq, ks, v8, sv = qz
+    o, lse, _ = oracle.attention(0, *qz, Nq=w.Nq, Nk=w.Nk)
+    perm = [1, 0]
+    kq2 = np.concatenate([kq[:, :, p * 128:(p + 1) * 128] for p in perm], axis=2)
+    ks2 = ks[:, :, perm]
+    v82 = np.concatenate([v8[..., p * 128:(p + 1) * 128] for p in perm], axis=3)
+    o2, lse2, _ = oracle.attention(0, qq, qs, kq2, ks2, v82, sv, Nq=w.Nq, Nk=w.Nk)
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13)
+
+
+def test_attention_ragged_equals_truncated():
+    w, q, k, v = _tiny()
+    L = 173
+    qz, _ = _quantize_all(q, k, v, 0, k_lens=[L])
+    o, lse, _ = oracle.attention(0, *qz, Nq=w.Nq, Nk=w.Nk, k_lens=[L])
+    qz2, _ = _quantize_all(q, k[:, :L], v[:, :L], 0)
+    o2, lse2, _ = oracle.attention(0, *qz2, Nq=w.Nq, Nk=L)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_attention_rows_subset():
+    w, q, k, v = _tiny()
+    qz, _ = _quantize_all(q, k, v, 0)
+    o, lse, _ = oracle.attention(0, *qz, Nq=w.Nq, Nk=w.Nk)
+    rows = [0, 5, 130, 255]
+    o2, lse2, _ = oracle.attention(0, *qz, Nq=w.Nq, Nk=w.Nk, rows=rows)
+    np.testing.assert_array_equal(o2, o[:, :, rows])
+    np.testing.assert_array_equal(lse2, lse[:, :, rows])
+
+
+def test_exact_attention_matches_torch_sdpa():
+    w, q, k, v = _tiny()
+    o, lse = oracle.attention_exact(bf16_bits(q), bf16_bits(k), bf16_bits(v))
+    qt, kt, vt = (t.double().permute(0, 2, 1, 3) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt).numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-10, atol=1e-12)
+    z = (qt @ kt.transpose(-1, -2)).numpy() / math.sqrt(w.D)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(z, axis=-1), rtol=1e-12)
+    # strided views (packed QKV) give the same answer
+    qkv = torch.stack([q, k, v], dim=2)  # [B,N,3,H,D]
+    o2, _ = oracle.attention_exact(bf16_bits(qkv[:, :, 0]), bf16_bits(qkv[:, :, 1]),
+                                   bf16_bits(qkv[:, :, 2]))
+    np.testing.assert_array_equal(o2, o)
+
+
+@pytest.mark.parametrize("fmt,min_cos", [(0, 0.999), (1, 0.95)])
+def test_quantized_close_to_exact(fmt, min_cos):
+    w, q, k, v = _tiny()
+    qz, _ = _quantize_all(q, k, v, fmt)
+    o, _, _ = oracle.attention(fmt, *qz, Nq=w.Nq, Nk=w.Nk)
+    oe, _ = oracle.attention_exact(bf16_bits(q), bf16_bits(k), bf16_bits(v))
+    cos = (o * oe).sum() / math.sqrt((o * o).sum() * (oe * oe).sum())
+    assert cos >= min_cos
+
+
+def test_p8_online_equals_final_encoding():
+    """The running-integer-maximum encoding equals the final-maximum encoding
+    wherever the probability is a normal E4M3 number after the 2^8 scale."""
+    rng = np.random.default_rng(3)
+    for trial in range(50):
+        n = int(rng.integers(1, 1000))
+        t = rng.standard_normal(n) * rng.uniform(0.1, 8) + np.linspace(0, rng.uniform(-5, 5), n)
+        a = oracle.p8_online(t, 128)
+        b = oracle.p8_final(t)
+        M = np.ceil(t.max())
+        normal = np.exp2(t - M) * 256.0 >= 2.0 ** -6
+        np.testing.assert_array_equal(a[normal], b[normal])
+        assert np.all(np.abs(a - b) <= 2.0 ** -17)
