@@ -1,0 +1,355 @@
+#!/usr/bin/env python
+"""Benchmark: effective attention TFLOPS on GB300 with quantization included.
+
+One step = the whole hot path on one batch of seeded synthetic input already
+resident in HBM: quantize Q (INT8), quantize K (INT8), quantize V (FP8 E4M3,
+two launches), attention forward (BF16 O + FP32 LSE). Effective TFLOPS =
+4*B*H*Nq*Nk*D / (summed step time). L2 is flushed between steps (a 256 MiB
+write outside the timed events). Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas: the path has no exchange step); value = units of all
+ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective attention TFLOPS at 1 GB300 (incl. quant) and % of dense INT8/FP8 peak"
+DEFAULT_WORKLOAD = "image_dit"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _roofline_peak(p16: float) -> float:
+    """Tensor roofline of the attention: half the flops (Q K^T) on the 16-bit
+    pipe, half (P V) on the FP8 pipe at twice that rate."""
+    p8 = 2.0 * p16
+    return 2.0 / (1.0 / p16 + 1.0 / p8)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sage_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", self.gpu_id], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 16):
+    """Time the CPU oracle (as it stands) on a bounded sample of workload w:
+    quantization of one head's Q/K/V plus attention for R query rows of that
+    head, R calibrated to take about `seconds`. Returns (flops, time_s, desc)."""
+    import numpy as np
+    import oracle
+    from precision_attention_diffusion_sage_gb300.inputs import bf16_bits, make_qkv
+
+    q, k, v = make_qkv(w)
+    qb, kb, vb = (bf16_bits(t[:, :, :1]) for t in (q, k, v))
+    lens = None if w.k_lens is None else w.k_lens
+
+    def run(rows):
+        t0 = time.perf_counter()
+        qz = oracle.quantize_int8(qb)
+        kz = oracle.quantize_int8(kb, lens=lens)
+        vz = oracle.quantize_v_fp8(vb, lens=lens)
+        oracle.attention(0, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows)
+        return time.perf_counter() - t0
+
+    def rows_of(n):
+        return np.linspace(0, w.Nq - 1, n).astype(np.int64)
+
+    t_cal = run(rows_of(seed_rows))
+    n = int(min(w.Nq, max(seed_rows, seed_rows * seconds / max(t_cal, 1e-3))))
+    dt = run(rows_of(n))
+    nk_sum = sum(w.k_lens) if w.k_lens else w.B * w.Nk
+    flops = 4.0 * n * (nk_sum / w.B) * w.D
+    desc = (f"oracle on head 0 of batch 0..{w.B - 1}: full Q/K/V quantization of that head "
+            f"+ attention for {n} of {w.Nq} query rows")
+    return flops, dt, desc, n
+
+
+def run_reference(args, w):
+    """The CPU oracle as the reference arm, on this run's workload and metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cores = os.cpu_count()
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    times, flops = [], 0.0
+    desc, n = "", 0
+    for i in range(args.warmup + args.steps):
+        f, dt, desc, n = _cpu_oracle_sample(w, budget)
+        if i >= args.warmup:
+            times.append(dt)
+            flops = f
+    tot = sum(times)
+    value = flops * len(times) / tot / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
+                       "k_lens": w.k_lens},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from precision_attention_diffusion_sage_gb300.inputs import WORKLOADS, make_qkv
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from precision_attention_diffusion_sage_gb300 import binding
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    q, k, v = make_qkv(w, device="cuda")
+    fmt = 0
+    B, Nq, H, D = q.shape
+    Nk = k.shape[1]
+    k_lens = None if w.k_lens is None else torch.tensor(w.k_lens, dtype=torch.int32, device=dev)
+    qq = torch.empty((B, H, binding.pad128(Nq), D), dtype=torch.float16, device=dev)
+    qs = torch.empty((B, H, binding.pad128(Nq) // 128), dtype=torch.float32, device=dev)
+    kq = torch.empty((B, H, binding.pad128(Nk), D), dtype=torch.float16, device=dev)
+    ks = torch.empty((B, H, binding.pad128(Nk) // 128), dtype=torch.float32, device=dev)
+    vq = torch.empty((B, H, D, binding.pad128(Nk)), dtype=torch.uint8, device=dev)
+    vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    vws = torch.empty(max(16, binding.sage_workspace_bytes(1, fmt, B, H, Nk, Nk)), dtype=torch.uint8,
+                      device=dev)
+    o = torch.empty((B, Nq, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    aws_n = binding.sage_workspace_bytes(2, fmt, B, H, Nq, Nk, D, args.splits)
+    aws = torch.empty(max(16, aws_n), dtype=torch.uint8, device=dev)
+    nsplit = binding.attn_splits(B, H, Nq, Nk, args.splits)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def quant():
+        binding.sage_quantize_qk(q, fmt, out=qq, scale=qs)
+        binding.sage_quantize_qk(k, fmt, lens=k_lens, out=kq, scale=ks)
+        binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
+
+    def attn():
+        binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens, out=o,
+                              lse=lse, num_splits=args.splits, workspace=aws)
+
+    for _ in range(args.warmup):
+        quant()
+        attn()
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record()
+        quant()
+        ev[i][1].record()
+        attn()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    assert binding.sage_last_device_status() == 0
+    t_quant = [e[0].elapsed_time(e[1]) for e in ev]
+    t_attn = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(t_quant) + sum(t_attn)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = w.flops
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    attn_ms = statistics.mean(t_attn)
+    hbm, p16, peak_kind = _peaks()
+    peak = _roofline_peak(p16)
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+
+    # end to end through the public call, host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        qd, kd, vd = (torch.empty_like(t) for t in (q, k, v))
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            oo, ll = binding.sage_attention(qd, kd, vd, k_lens=k_lens, num_splits=args.splits)
+            oh.copy_(oo, non_blocking=True)
+            lh.copy_(ll, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps):
+            flush.zero_()
+            ee[i][0].record()
+            e2e_step()
+            ee[i][1].record()
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = sum(a.elapsed_time(b) for a, b in ee)
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+        d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        e2e = {"value": world * flops * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, dt, desc, n = _cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": desc, "seconds": dt}
+
+    launches_per_step = 2 + 2 + 1 + (1 if nsplit > 1 else 0)
+    quant_bytes = (2 * (B * Nq * H * D * 2 + B * H * binding.pad128(Nq) * D * 2)
+                   if Nq == Nk else
+                   B * Nq * H * D * 4 + B * Nk * H * D * 2 + B * H * binding.pad128(Nk) * D * 2
+                   + B * H * binding.pad128(Nq) * D * 2)
+    quant_bytes += B * Nk * H * D * 4 + B * H * D * binding.pad128(Nk)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 QK^T (exact, fp16 tensor pipe) + fp8e4m3 PV", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
+                   "k_lens": w.k_lens, "format": "int8_qk_fp8_v", "splits": nsplit,
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "attn_only_tflops": achieved,
+        "quant_ms_per_step": statistics.mean(t_quant),
+        "attn_ms_per_step": attn_ms,
+        "quant_gbs": quant_bytes / (statistics.mean(t_quant) * 1e-3) / 1e9,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_basis": f"{peak_kind} bf16 {p16} TFLOP/s for Q K^T (fp16 pipe), "
+                                   f"x2 nominal fp8 ratio for P V, harmonic combination",
+                     "kernel": "attn_i8f8_kernel"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk, "wall_s": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

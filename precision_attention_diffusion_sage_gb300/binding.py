@@ -1,0 +1,220 @@
+"""Thin ctypes binding over ``libsage.so`` (the C ABI in ``include/sage.h``).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. Tensors are PyTorch CUDA tensors; outputs and scratch are allocated
+with torch when the caller does not pass them. Calls are enqueued on the
+current torch stream. A non-OK status raises ``SageError``. Importing this
+module raises if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsage.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "sage.h")
+
+FMT_INT8 = 0   # SAGE_FMT_QK_INT8_V_FP8
+FMT_MXFP4 = 1  # SAGE_FMT_QK_MXFP4_V_FP8
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libsage.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("n", ctypes.c_int64), ("h", ctypes.c_int64)]
+
+
+class AttnOptions(ctypes.Structure):
+    _fields_ = [("num_splits", ctypes.c_int32), ("cta_mode", ctypes.c_int32)]
+
+
+_P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+_lib.sage_quantized_bytes.restype = ctypes.c_size_t
+_lib.sage_quantized_bytes.argtypes = [_I32, _I32, _I64, _I64, _I64, _I64]
+_lib.sage_workspace_bytes.restype = ctypes.c_size_t
+_lib.sage_workspace_bytes.argtypes = [_I32, _I32, _I64, _I64, _I64, _I64, _I64, _I32]
+_lib.sage_quantize_qk.restype = _I32
+_lib.sage_quantize_qk.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P]
+_lib.sage_quantize_v.restype = _I32
+_lib.sage_quantize_v.argtypes = [_P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
+                                 ctypes.c_size_t, _P]
+_lib.sage_attn_fwd.restype = _I32
+_lib.sage_attn_fwd.argtypes = [_I32, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
+                               ctypes.c_float, _I32, _P, Strides, _P, _P, ctypes.c_size_t,
+                               ctypes.POINTER(AttnOptions), _P]
+_lib.sage_status_string.restype = ctypes.c_char_p
+_lib.sage_status_string.argtypes = [_I32]
+_lib.sage_last_device_status.restype = _I32
+_lib.sage_last_device_status.argtypes = [_P]
+_lib.sage_version.restype = ctypes.c_char_p
+_lib.sage_version.argtypes = []
+
+
+class SageError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_lib.sage_status_string(status).decode()} ({status})")
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise SageError(st, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _bnhd_strides(x: torch.Tensor) -> Strides:
+    if x.dim() != 4 or x.stride(3) != 1:
+        raise ValueError("expected a [B, N, H, D] tensor with unit stride along D")
+    return Strides(x.stride(0), x.stride(1), x.stride(2))
+
+
+def header_symbols() -> Sequence[str]:
+    """Function names declared in include/sage.h."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(sage_\w+)\s*\(", text, re.M)))
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def sage_version() -> str:
+    return _lib.sage_version().decode()
+
+
+def sage_quantized_bytes(fmt: int, which: int, B: int, N: int, H: int, D: int = 128) -> int:
+    return int(_lib.sage_quantized_bytes(fmt, which, B, N, H, D))
+
+
+def sage_workspace_bytes(op: int, fmt: int, B: int, H: int, Nq: int, Nk: int, D: int = 128,
+                         num_splits: int = 0) -> int:
+    return int(_lib.sage_workspace_bytes(op, fmt, B, H, Nq, Nk, D, num_splits))
+
+
+def attn_splits(B: int, H: int, Nq: int, Nk: int, num_splits: int = 0) -> int:
+    """KV split count sage_attn_fwd uses (derived from its workspace size)."""
+    ws = sage_workspace_bytes(2, FMT_INT8, B, H, Nq, Nk, 128, num_splits)
+    return 1 if ws == 0 else ws // (B * H * Nq * 129 * 4)
+
+
+def pad128(n: int) -> int:
+    return (n + 127) // 128 * 128
+
+
+def _lens_tensor(lens, device) -> Optional[torch.Tensor]:
+    if lens is None:
+        return None
+    if isinstance(lens, torch.Tensor):
+        return lens.to(device=device, dtype=torch.int32).contiguous()
+    return torch.tensor(list(lens), dtype=torch.int32, device=device)
+
+
+def sage_quantize_qk(x: torch.Tensor, fmt: int = FMT_INT8, lens=None,
+                     out: Optional[torch.Tensor] = None,
+                     scale: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Quantize BF16 Q or K ``[B, N, H, D]``.
+
+    INT8: returns (codes held as float16 ``[B, H, Npad, D]``, float32 scales
+    ``[B, H, Npad/128]``). MXFP4: (uint8 ``[B, H, Npad, D/2]``, uint8 E8M0
+    ``[B, H, Npad, D/32]``).
+    """
+    B, N, H, D = x.shape
+    Np = pad128(N)
+    if out is None:
+        out = (torch.empty((B, H, Np, D), dtype=torch.float16, device=x.device) if fmt == FMT_INT8
+               else torch.empty((B, H, Np, D // 2), dtype=torch.uint8, device=x.device))
+    if scale is None:
+        scale = (torch.empty((B, H, Np // 128), dtype=torch.float32, device=x.device)
+                 if fmt == FMT_INT8
+                 else torch.empty((B, H, Np, D // 32), dtype=torch.uint8, device=x.device))
+    ln = _lens_tensor(lens, x.device)
+    _check(_lib.sage_quantize_qk(fmt, _ptr(x), _bnhd_strides(x), B, N, H, D, _ptr(ln), _ptr(out),
+                                 _ptr(scale), _stream()), "sage_quantize_qk")
+    return out, scale
+
+
+def sage_quantize_v(v: torch.Tensor, lens=None, out: Optional[torch.Tensor] = None,
+                    scale: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Quantize BF16 V ``[B, N, H, D]`` to FP8 E4M3 ``[B, H, D, Npad]`` (uint8) + scales."""
+    B, N, H, D = v.shape
+    Np = pad128(N)
+    if out is None:
+        out = torch.empty((B, H, D, Np), dtype=torch.uint8, device=v.device)
+    if scale is None:
+        scale = torch.empty((B, H, D), dtype=torch.float32, device=v.device)
+    need = sage_workspace_bytes(1, FMT_INT8, B, H, N, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=v.device)
+    ln = _lens_tensor(lens, v.device)
+    _check(_lib.sage_quantize_v(_ptr(v), _bnhd_strides(v), B, N, H, D, _ptr(ln), _ptr(out),
+                                _ptr(scale), _ptr(workspace), workspace.numel(), _stream()),
+           "sage_quantize_v")
+    return out, scale
+
+
+def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int, Nk: int,
+                  k_lens=None, softmax_scale: Optional[float] = None, causal: int = 0,
+                  out: Optional[torch.Tensor] = None, return_lse: bool = True,
+                  lse: Optional[torch.Tensor] = None, num_splits: int = 0,
+                  workspace: Optional[torch.Tensor] = None):
+    """Attention forward on quantized operands. Returns (O ``[B, Nq, H, D]`` bf16, LSE or None)."""
+    B, H = q_q.shape[0], q_q.shape[1]
+    D = 128
+    dev = q_q.device
+    if out is None:
+        out = torch.empty((B, Nq, H, D), dtype=torch.bfloat16, device=dev)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    need = sage_workspace_bytes(2, fmt, B, H, Nq, Nk, D, num_splits)
+    if need > 0 and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ln = _lens_tensor(k_lens, dev)
+    opts = AttnOptions(num_splits, 0)
+    sc = -1.0 if softmax_scale is None else float(softmax_scale)
+    _check(_lib.sage_attn_fwd(fmt, _ptr(q_q), _ptr(q_scale), _ptr(k_q), _ptr(k_scale), _ptr(v_q),
+                              _ptr(v_scale), _ptr(ln), B, H, Nq, Nk, D, sc, causal, _ptr(out),
+                              _bnhd_strides(out), _ptr(lse if return_lse else None),
+                              _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                              ctypes.byref(opts), _stream()), "sage_attn_fwd")
+    return out, (lse if return_lse else None)
+
+
+def sage_last_device_status() -> int:
+    """Synchronise the current stream and read/clear the device status word."""
+    return int(_lib.sage_last_device_status(_stream()))
+
+
+def sage_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: int = FMT_INT8,
+                   k_lens=None, softmax_scale: Optional[float] = None, num_splits: int = 0,
+                   return_lse: bool = True):
+    """Quantize Q/K/V and attend: the four library calls in order."""
+    B, Nq, H, D = q.shape
+    Nk = k.shape[1]
+    qq, qs = sage_quantize_qk(q, fmt)
+    kq, ks = sage_quantize_qk(k, fmt, lens=k_lens)
+    vq, vs = sage_quantize_v(v, lens=k_lens)
+    return sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
+                         softmax_scale=softmax_scale, num_splits=num_splits,
+                         return_lse=return_lse)
+
+
+def int8_codes(x_q: torch.Tensor) -> torch.Tensor:
+    """INT8 codes from the FP16-held quantized Q/K layout."""
+    return x_q.to(torch.int8)

@@ -1,0 +1,622 @@
+// Fused quantized attention forward for sm_103a (INT8 Q/K, FP8 V).
+//
+// Restates the kernel described on "[ROCm] Add aiter_sage_attn attention
+// backend for gfx1201 (RDNA4)" ("Changes": INT8 QK^T, FP8 PV, FP32
+// accumulation, head dim 128, non-causal) and "new MHA v4 entrypoint ..."
+// ("Motivation": conditional softmax rescaling, base-2 exponentials,
+// pipelines that keep loads, vector ALUs and matrix units busy at once),
+// with the output plus float32 LSE and split-KV of "[None][feat] Add
+// VisualGen FA4 autotuning ..." (first paragraph).
+//
+// GB300 design, per CTA (NQT query tiles of 128 rows of one (b, h)):
+//   warps 0 .. 4*NQT-1 : one softmax warpgroup per query tile; thread r owns
+//                        row r (TMEM lane r) of its tile.
+//   warp 4*NQT         : TMA producer (Q once, then K/V tiles into a ring).
+//   warp 4*NQT+1       : tcgen05 MMA issuer; allocates/frees TMEM.
+// TMEM per tile: S (128 FP32 columns) and O (128 FP32 columns).
+// S = Q K^T runs as kind::f16 on the INT8 codes held as FP16 (sm_103a has no
+// 8-bit integer MMA): products and partial sums are integers below 2^24, so
+// the FP32 accumulator holds the INT32 dot product exactly.
+// Softmax: t = S * alpha, alpha = s_q s_k softmax_scale log2(e); the running
+// row maximum m is an integer (ceil), raised only when it grows; O and l are
+// then rescaled by the exact power of two 2^(m_old - m_new). P8 =
+// E4M3(2^(t - m + 8)) goes to shared memory (128-byte swizzled, K-major) and
+// O += P8 * V8^T runs as kind::f8f6f4. Epilogue: O * s_v / l -> BF16,
+// LSE = (m + log2 l - 8) ln 2 (l is kept in units of 2^-8).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "attention.cuh"
+#include "sm103_ptx.cuh"
+
+namespace sage {
+namespace {
+
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int NQT, int STAGES>
+struct SmemLayout {
+  static constexpr int kQ = 0;                          // NQT x 32 KB (FP16 128x128)
+  static constexpr int kK = kQ + NQT * 32768;           // STAGES x 32 KB
+  static constexpr int kV = kK + STAGES * 32768;        // STAGES x 16 KB (FP8 V^T 128x128)
+  static constexpr int kP = kV + STAGES * 16384;        // NQT x 16 KB (FP8 P 128x128)
+  static constexpr int kBar = kP + NQT * 16384;
+  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
+  //           s_full[T], s_free[T], p_full[T], o_done[T], mma_final
+  static constexpr int kNumBars = 1 + 4 * STAGES + 4 * NQT + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;     // tmem slot, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kDynamic = kBytes + 1024;        // + alignment slack
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two E4M3 codes: `lo` in bits 7..0, `hi` in bits 15..8.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 2^k for an integer-valued k <= 0 (0 below the normal range).
+__device__ __forceinline__ float exp2_neg_int(float k) {
+  const int ki = static_cast<int>(k);
+  return ki < -126 ? 0.0f : __uint_as_float(static_cast<uint32_t>(ki + 127) << 23);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int* status) {
+  if (mbar_wait(bar, parity, abort)) return true;
+  if (!*abort) {
+    *abort = 1;
+    atomicOr(status, kStatusTimeout);
+  }
+  return false;
+}
+
+// Warp-collective variant: every lane waits, the result is uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* status) {
+  const bool r = wait_or_abort(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, r);
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
+  const int zero = 0;
+  if (!mbar_wait(bar, parity, &zero)) atomicOr(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Threads per CTA: 6 warps for one query tile; 12 (three full warpgroups)
+// for two, so that registers can be moved to the softmax warpgroups with
+// setmaxnreg (each SM sub-partition holds one warp of every warpgroup).
+template <int NQT>
+constexpr int attn_threads() { return NQT == 1 ? 6 * 32 : 12 * 32; }
+
+template <int NQT, int STAGES>
+__global__ void __launch_bounds__(attn_threads<NQT>(), 1)
+    attn_i8f8_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using L = SmemLayout<NQT, STAGES>;
+  constexpr int kSoftmaxWarps = NQT * 4;
+  constexpr int kTmaWarp = kSoftmaxWarps;
+  constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  constexpr uint32_t kTmemCols = NQT == 1 ? 256 : 512;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sK = smem + L::kK;
+  uint8_t* sV = smem + L::kV;
+  uint8_t* sP = smem + L::kP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + STAGES;
+  uint64_t* v_full = k_empty + STAGES;
+  uint64_t* v_empty = v_full + STAGES;
+  uint64_t* s_full = v_empty + STAGES;
+  uint64_t* s_free = s_full + NQT;
+  uint64_t* p_full = s_free + NQT;
+  uint64_t* o_done = p_full + NQT;
+  uint64_t* mma_final = o_done + NQT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int64_t h = blockIdx.y;
+  const int64_t b = blockIdx.z / p.num_splits;
+  const int split = static_cast<int>(blockIdx.z % p.num_splits);
+  const int64_t bh = b * p.H + h;
+  const int64_t Nq_pad = p.nbq * 128, Nk_pad = p.nbk * 128;
+
+  // A CTA of an earlier launch already ran out of a bounded wait: do not
+  // pile further timeouts on top (the status word keeps the error).
+  if (*reinterpret_cast<volatile int*>(p.status) & kStatusTimeout) return;
+
+  // ---- per-batch key range (uniform over the CTA)
+  int64_t nk = p.Nk;
+  if (p.k_lens) {
+    nk = p.k_lens[b];
+    if (nk < 0 || nk > p.Nk) {
+      if (threadIdx.x == 0) atomicOr(p.status, kStatusDeviceArg);
+      return;
+    }
+  }
+  const int64_t nkv = (nk + 127) / 128;
+  const int64_t per_split = (nkv + p.num_splits - 1) / p.num_splits;
+  const int64_t j0 = static_cast<int64_t>(split) * per_split;
+  const int64_t j1 = j0 + per_split < nkv ? j0 + per_split : nkv;
+  const int64_t niter = j1 > j0 ? j1 - j0 : 0;
+
+  if (niter == 0) {
+    // No keys for this (batch, split): empty softmax, O = 0, LSE = -inf.
+    if (warp < kSoftmaxWarps) {
+      const int t = warp / 4, r = static_cast<int>(threadIdx.x & 127);
+      const int64_t row = (static_cast<int64_t>(blockIdx.x) * NQT + t) * 128 + r;
+      if (row < p.Nq) {
+        if (p.num_splits > 1) {
+          float* op = p.o_part + ((static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row) * 128;
+          for (int d = 0; d < 128; d += 4) *reinterpret_cast<float4*>(op + d) = make_float4(0, 0, 0, 0);
+          p.lse_part[(static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row] = -INFINITY;
+        } else {
+          __nv_bfloat16* orow = p.o + b * p.osb + row * p.osn + h * p.osh;
+          for (int d = 0; d < 128; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+          if (p.lse) p.lse[bh * p.Nq + row] = -INFINITY;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- setup
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 128);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(mma_final, 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  // With two query tiles, 384 threads launch with 168 registers each, a pool
+  // of 384 * 168 = 64512 that setmaxnreg redistributes: the two softmax
+  // warpgroups take 232 and the producer/MMA warpgroup keeps 40
+  // (128 * (232 + 232 + 40) = 64512). The host refuses to launch if the
+  // compiled register count would leave the pool smaller than that.
+  if (warp >= kSoftmaxWarps) {
+    if constexpr (NQT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
+  if (warp == kTmaWarp) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, NQT * 32768);
+      for (int t = 0; t < NQT; ++t) {
+        const int y = static_cast<int>(bh * Nq_pad + (static_cast<int64_t>(blockIdx.x) * NQT + t) * 128);
+        tma_load_2d(sQ + t * 32768, &tmQ, q_full, 0, y);
+        tma_load_2d(sQ + t * 32768 + 16384, &tmQ, q_full, 64, y);
+      }
+      int kfills[STAGES], vfills[STAGES];
+      for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
+      for (int64_t it = 0; it < niter; ++it) {
+        const int s = static_cast<int>(it % STAGES);
+        const uint32_t u = static_cast<uint32_t>(it / STAGES);
+        const int64_t j = j0 + it;
+        if (u > 0 && !wait_or_abort(&k_empty[s], (u - 1) & 1, abort, p.status)) break;
+        mbar_arrive_expect_tx(&k_full[s], 32768);
+        const int yk = static_cast<int>(bh * Nk_pad + j * 128);
+        tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
+        tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
+        ++kfills[s];
+        if (u > 0 && !wait_or_abort(&v_empty[s], (u - 1) & 1, abort, p.status)) break;
+        mbar_arrive_expect_tx(&v_full[s], 16384);
+        tma_load_2d(sV + s * 16384, &tmV, &v_full[s], static_cast<int>(j * 128),
+                    static_cast<int>(bh * 128));
+        ++vfills[s];
+      }
+      // Drain: no TMA write may still be in flight when the CTA exits.
+      drain_wait(q_full, 0, p.status);
+      for (int s = 0; s < STAGES; ++s) {
+        if (kfills[s] > 0) drain_wait(&k_full[s], static_cast<uint32_t>(kfills[s] - 1) & 1, p.status);
+        if (vfills[s] > 0) drain_wait(&v_full[s], static_cast<uint32_t>(vfills[s] - 1) & 1, p.status);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_f32acc(128, 128);  // f16 x f16 -> f32
+      constexpr uint32_t kIdescO = idesc_f32acc(128, 128);  // e4m3 x e4m3 -> f32
+      bool ok = wait_or_abort(q_full, 0, abort, p.status);
+      if (ok) ok = wait_or_abort(&k_full[0], 0, abort, p.status);
+      tc_fence_after();
+      auto issue_s = [&](int t, int stage) {
+        const uint32_t d = tbase + t * 256;
+        const uint32_t qa = smem_u32(sQ + t * 32768);
+        const uint32_t ka = smem_u32(sK + stage * 32768);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_f16_ss(d, sw128_kmajor_desc(qa + off), sw128_kmajor_desc(ka + off), kIdescS, k > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int stage, bool acc) {
+        const uint32_t d = tbase + t * 256 + 128;
+        const uint32_t pa = smem_u32(sP + t * 16384);
+        const uint32_t va = smem_u32(sV + stage * 16384);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f8_ss(d, sw128_kmajor_desc(pa + k * 32), sw128_kmajor_desc(va + k * 32), kIdescO,
+                    (acc || k > 0) ? 1u : 0u);
+      };
+      if (ok) {
+        for (int t = 0; t < NQT; ++t) {
+          issue_s(t, 0);
+          mma_commit(&s_full[t]);
+        }
+        mma_commit(&k_empty[0]);
+      }
+      for (int64_t it = 0; ok && it < niter; ++it) {
+        const int s = static_cast<int>(it % STAGES);
+        const uint32_t u = static_cast<uint32_t>(it / STAGES);
+        const bool has_next = it + 1 < niter;
+        const int sn = static_cast<int>((it + 1) % STAGES);
+        const uint32_t un = static_cast<uint32_t>((it + 1) / STAGES);
+        if (has_next && !(ok = wait_or_abort(&k_full[sn], un & 1, abort, p.status))) break;
+        if (!(ok = wait_or_abort(&v_full[s], u & 1, abort, p.status))) break;
+        tc_fence_after();
+        for (int t = 0; t < NQT && ok; ++t) {
+          if (has_next) {
+            if (!(ok = wait_or_abort(&s_free[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
+            tc_fence_after();
+            issue_s(t, sn);
+            mma_commit(&s_full[t]);
+          }
+          if (!(ok = wait_or_abort(&p_full[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
+          tc_fence_after();
+          issue_pv(t, s, it > 0);
+          mma_commit(&o_done[t]);
+        }
+        if (!ok) break;
+        if (has_next) mma_commit(&k_empty[sn]);
+        mma_commit(&v_empty[s]);
+      }
+      // All MMAs issued by this thread must finish before TMEM is freed.
+      mma_commit(mma_final);
+      drain_wait(mma_final, 0, p.status);
+    }
+  }
+  } else {
+      if constexpr (NQT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
+    // ================================================================ softmax
+    const int t = warp / 4;
+    const int r = static_cast<int>(threadIdx.x & 127);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_base + t * 256;
+    const uint32_t tO = tS + 128;
+    const int64_t qt = static_cast<int64_t>(blockIdx.x) * NQT + t;
+    const int64_t row = qt * 128 + r;
+    const float sq = qt < p.nbq ? __ldg(&p.q_scale[bh * p.nbq + qt]) : 0.0f;
+    const float alpha_q = sq * p.scale_log2;
+    const float* kscale = p.k_scale + bh * p.nbk;
+    float m = -INFINITY;  // running integer row maximum (log2 units)
+    float l = 0.0f;       // running row sum of 2^(t - m + 8)
+    bool ok = true;
+    const uint32_t p_row = smem_u32(sP + t * 16384) + r * 128;
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+
+    for (int64_t it = 0; it < niter; ++it) {
+      const int64_t j = j0 + it;
+      if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[t]);
+
+      const float alpha = alpha_q * __ldg(&kscale[j]);
+      const int nvalid = static_cast<int>(nk - j * 128 < 128 ? nk - j * 128 : 128);
+      float mx = -INFINITY;
+      if (nvalid == 128) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < nvalid) mx = fmaxf(mx, s[c]);
+      }
+      const float m_new = fmaxf(m, ceilf(mx * alpha));
+      const bool rescale = (it > 0) && (m_new > m);
+      bool o_ready = false;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // Conditional rescale: O_t holds PV up to the previous tile.
+        if (!(ok = warp_wait(&o_done[t], static_cast<uint32_t>(it - 1) & 1, abort, p.status))) break;
+        o_ready = true;
+        tc_fence_after();
+        const float f = rescale ? exp2_neg_int(m - m_new) : 1.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+          tmem_st32(tO + c * 32, v);
+        }
+        tc_fence_before();
+        l *= f;
+      }
+      m = m_new;
+      const float bias = 8.0f - m;
+
+      // P_t is free once PV_t of the previous tile has completed.
+      if (it > 0 && !o_ready) {
+        if (!(ok = warp_wait(&o_done[t], static_cast<uint32_t>(it - 1) & 1, abort, p.status))) break;
+      }
+      float lsum = 0.0f;
+      if (nvalid == 128) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = ch * 16 + q * 4;
+            const float e0 = ex2_approx(fmaf(s[c + 0], alpha, bias));
+            const float e1 = ex2_approx(fmaf(s[c + 1], alpha, bias));
+            const float e2 = ex2_approx(fmaf(s[c + 2], alpha, bias));
+            const float e3 = ex2_approx(fmaf(s[c + 3], alpha, bias));
+            lsum += (e0 + e1) + (e2 + e3);
+            pk[q] = e4m3x2(e0, e1) | (e4m3x2(e2, e3) << 16);
+          }
+          st_shared_v4(p_row + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+        }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = ch * 16 + q * 4;
+            const float e0 = c + 0 < nvalid ? ex2_approx(fmaf(s[c + 0], alpha, bias)) : 0.0f;
+            const float e1 = c + 1 < nvalid ? ex2_approx(fmaf(s[c + 1], alpha, bias)) : 0.0f;
+            const float e2 = c + 2 < nvalid ? ex2_approx(fmaf(s[c + 2], alpha, bias)) : 0.0f;
+            const float e3 = c + 3 < nvalid ? ex2_approx(fmaf(s[c + 3], alpha, bias)) : 0.0f;
+            lsum += (e0 + e1) + (e2 + e3);
+            pk[q] = e4m3x2(e0, e1) | (e4m3x2(e2, e3) << 16);
+          }
+          st_shared_v4(p_row + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      l += lsum;
+      fence_proxy_async_smem();
+      mbar_arrive(&p_full[t]);
+    }
+
+    // ---- epilogue
+    if (ok) ok = warp_wait(&o_done[t], static_cast<uint32_t>(niter - 1) & 1, abort, p.status);
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const float* sv = p.v_scale + bh * 128;
+      const float lse = (m + log2f(l) - 8.0f) * kLn2;
+      const bool store = row < p.Nq;
+      if (p.num_splits > 1) {
+        float* op = p.o_part + ((static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row) * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + c * 32, v);
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              float4 o4;
+              o4.x = __uint_as_float(v[i + 0]) * (__ldg(&sv[c * 32 + i + 0]) * inv_l);
+              o4.y = __uint_as_float(v[i + 1]) * (__ldg(&sv[c * 32 + i + 1]) * inv_l);
+              o4.z = __uint_as_float(v[i + 2]) * (__ldg(&sv[c * 32 + i + 2]) * inv_l);
+              o4.w = __uint_as_float(v[i + 3]) * (__ldg(&sv[c * 32 + i + 3]) * inv_l);
+              *reinterpret_cast<float4*>(op + c * 32 + i) = o4;
+            }
+          }
+        }
+        if (store) p.lse_part[(static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row] = lse;
+      } else {
+        __nv_bfloat16* orow = p.o + b * p.osb + row * p.osn + h * p.osh;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + c * 32, v);
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float a0 = __uint_as_float(v[i + 2 * k]) * (__ldg(&sv[c * 32 + i + 2 * k]) * inv_l);
+                const float a1 = __uint_as_float(v[i + 2 * k + 1]) * (__ldg(&sv[c * 32 + i + 2 * k + 1]) * inv_l);
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+                w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(orow + c * 32 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+        if (store && p.lse) p.lse[bh * p.Nq + row] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// Split-KV merge: one warp per output row, 4 channels per lane.
+__global__ void __launch_bounds__(256) merge_splits_kernel(const AttnParams p) {
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int64_t rows = p.B * p.H * p.Nq;
+  if (gw >= rows) return;
+  const int64_t bh = gw / p.Nq, row = gw % p.Nq;
+  const int64_t b = bh / p.H, h = bh % p.H;
+  const int64_t stride = p.B * p.H * p.Nq;
+  float mx = -INFINITY;
+  for (int s = 0; s < p.num_splits; ++s) mx = fmaxf(mx, p.lse_part[s * stride + gw]);
+  float4 acc = make_float4(0, 0, 0, 0);
+  float lse = -INFINITY;
+  if (mx != -INFINITY) {
+    float wsum = 0.0f;
+    for (int s = 0; s < p.num_splits; ++s) {
+      const float ls = p.lse_part[s * stride + gw];
+      const float w = ls == -INFINITY ? 0.0f : expf(ls - mx);
+      wsum += w;
+      const float4 o = *reinterpret_cast<const float4*>(p.o_part + (s * stride + gw) * 128 + lane * 4);
+      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+    }
+    const float inv = 1.0f / wsum;
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    lse = mx + logf(wsum);
+  }
+  __nv_bfloat16* orow = p.o + b * p.osb + row * p.osn + h * p.osh + lane * 4;
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x, acc.y);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&h0);
+  w.y = *reinterpret_cast<const uint32_t*>(&h1);
+  *reinterpret_cast<uint2*>(orow) = w;
+  if (lane == 0 && p.lse) p.lse[bh * p.Nq + row] = lse;
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, []() {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool make_map_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize,
+                 uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NQT, int STAGES>
+cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           const AttnParams& p, cudaStream_t stream) {
+  using L = SmemLayout<NQT, STAGES>;
+  static_assert(L::kDynamic <= 232448, "shared memory budget");
+  auto kern = attn_i8f8_kernel<NQT, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
+  if (e != cudaSuccess) return e;
+  if constexpr (NQT == 2) {
+    // setmaxnreg can only hand out the registers the CTA was launched with.
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if (static_cast<long>(fa.numRegs) * attn_threads<NQT>() < 128L * (232 + 232 + 40))
+      return cudaErrorInvalidConfiguration;
+  }
+  dim3 grid(static_cast<unsigned>((p.nbq + NQT - 1) / NQT), static_cast<unsigned>(p.H),
+            static_cast<unsigned>(p.B * p.num_splits));
+  kern<<<grid, attn_threads<NQT>(), L::kDynamic, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_q_tiles_per_cta(int64_t nbq) { return nbq >= 2 ? 2 : 1; }
+
+int attn_auto_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
+  const int64_t nbq = pad128(Nq) / 128, nkv = pad128(Nk) / 128;
+  const int nqt = attn_q_tiles_per_cta(nbq);
+  const int64_t ctas = (nbq + nqt - 1) / nqt * B * H;
+  if (ctas >= 152 || nkv < 4) return 1;
+  int64_t s = (2 * 152 + ctas - 1) / ctas;
+  if (s > nkv / 2) s = nkv / 2;
+  if (s > 16) s = 16;
+  if (s * B > 65535) s = 65535 / B;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+cudaError_t launch_attention_i8f8(const AttnLaunch& a, cudaStream_t stream) {
+  if (!get_encode()) return cudaErrorNotSupported;
+  const int64_t Nq_pad = pad128(a.p.Nq), Nk_pad = pad128(a.p.Nk);
+  CUtensorMap mq, mk, mv;
+  if (!make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128,
+                   static_cast<uint64_t>(a.p.B * a.p.H * Nq_pad), 64, 128) ||
+      !make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128,
+                   static_cast<uint64_t>(a.p.B * a.p.H * Nk_pad), 64, 128) ||
+      !make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(Nk_pad),
+                   static_cast<uint64_t>(a.p.B * a.p.H * 128), 128, 128))
+    return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (attn_q_tiles_per_cta(a.p.nbq) == 2)
+    e = launch_variant<2, 2>(mq, mk, mv, a.p, stream);
+  else
+    e = launch_variant<1, 3>(mq, mk, mv, a.p, stream);
+  if (e != cudaSuccess || a.p.num_splits <= 1) return e;
+  const int64_t rows = a.p.B * a.p.H * a.p.Nq;
+  const int64_t blocks = (rows * 32 + 255) / 256;
+  merge_splits_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.p);
+  return cudaGetLastError();
+}
+
+}  // namespace sage

@@ -1,0 +1,44 @@
+// Shared definitions between the kernels and the host layer of libsage.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace sage {
+
+// Bits OR-ed into the per-device status word by kernels.
+constexpr int kStatusDeviceArg = 1;  // a k_lens / lens entry was out of range
+constexpr int kStatusTimeout = 2;    // a bounded wait ran out
+
+constexpr int kHeadDim = 128;
+constexpr int kTile = 128;  // tokens per quantization block and per MMA tile
+
+__host__ __device__ constexpr int64_t pad128(int64_t n) { return (n + 127) / 128 * 128; }
+
+// ---- launchers (defined in quantize.cu / attention.cu, called from sage_api.cu)
+struct QuantQKArgs {
+  const uint16_t* x;  // bf16 bits
+  int64_t sb, sn, sh;
+  int64_t B, N, H;
+  const int32_t* lens;
+  void* out;      // fp16 codes or packed e2m1
+  void* scale;    // float scales or e8m0 bytes
+  int* status;
+};
+cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s);
+cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s);
+
+struct QuantVArgs {
+  const uint16_t* v;
+  int64_t sb, sn, sh;
+  int64_t B, N, H;
+  const int32_t* lens;
+  uint8_t* out;   // [B][H][D][Npad]
+  float* scale;   // [B][H][D]
+  float* partial; // [B][H][nchunks][D]
+  int* status;
+};
+constexpr int kVChunk = 512;  // tokens per partial-maximum chunk
+__host__ __device__ inline int64_t v_partial_chunks(int64_t N) { return (N + kVChunk - 1) / kVChunk; }
+cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s);
+
+}  // namespace sage

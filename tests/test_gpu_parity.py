@@ -1,0 +1,217 @@
+"""CUDA path vs the CPU oracle, through the C ABI (via the ctypes binding).
+
+Quantized tensors and scales must be bit-exact; O within max-abs 1e-2 and
+cosine >= 0.9999 of the oracle; LSE within 1e-3 absolute. Small cases run the
+oracle on every row; the full-size workloads compare every quantized tensor
+and a deterministic sample of query rows (every row of the sample is exact to
+compute on its own, so sampled parity is parity for those rows).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_attention_diffusion_sage_gb300.inputs import WORKLOADS, Workload, bf16_bits, make_qkv
+
+from _helpers import (assert_attention_close, assert_qk_equal, assert_v_equal, gpu_codes,
+                      oracle_quantize)
+
+pytestmark = pytest.mark.gpu
+
+binding = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global binding
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from precision_attention_diffusion_sage_gb300 import build as sage_build
+    sage_build.build()
+    from precision_attention_diffusion_sage_gb300 import binding as b
+    binding = b
+    yield
+
+
+def _small(B, H, Nq, Nk, seed, structure="plain"):
+    w = Workload("case", B, H, Nq, Nk, seed=seed, structure=structure)
+    q, k, v = make_qkv(w)
+    return w, q.cuda(), k.cuda(), v.cuda()
+
+
+def _run_gpu(fmt, q, k, v, k_lens=None, num_splits=0, softmax_scale=None):
+    Nq, Nk = q.shape[1], k.shape[1]
+    qq, qs = binding.sage_quantize_qk(q, fmt)
+    kq, ks = binding.sage_quantize_qk(k, fmt, lens=k_lens)
+    vq, vs = binding.sage_quantize_v(v, lens=k_lens)
+    o, lse = binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
+                                   num_splits=num_splits, softmax_scale=softmax_scale)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    return (qq, qs), (kq, ks), (vq, vs), o, lse
+
+
+def _oracle_attention(fmt, qz, kz, vz, Nq, Nk, k_lens=None, rows=None, softmax_scale=None):
+    o, lse, _ = oracle.attention(fmt, qz[0], qz[1], kz[0], kz[1], vz[0], vz[1], Nq=Nq, Nk=Nk,
+                                 k_lens=k_lens, rows=rows, softmax_scale=softmax_scale)
+    return o, lse
+
+
+# ------------------------------------------------------------------ quantization
+@pytest.mark.parametrize("N,lens", [(256, None), (1, None), (127, None), (129, None),
+                                    (300, None), (300, [173])])
+def test_quantize_int8_bitexact(N, lens):
+    w, q, k, v = _small(1, 2, N, N, seed=10 + N, structure="k_offset_std2")
+    xq, xs = binding.sage_quantize_qk(k, 0, lens=lens)
+    rq, rs = oracle.quantize_int8(bf16_bits(k), lens=lens)
+    assert_qk_equal(0, xq, xs, rq, rs)
+
+
+@pytest.mark.parametrize("N,lens", [(256, None), (1, None), (300, None), (700, [611])])
+def test_quantize_v_bitexact(N, lens):
+    w, q, k, v = _small(1, 3, N, N, seed=20 + N)
+    vq, vs = binding.sage_quantize_v(v, lens=lens)
+    rq, rs = oracle.quantize_v_fp8(bf16_bits(v), lens=lens)
+    assert_v_equal(vq, vs, rq, rs)
+
+
+@pytest.mark.parametrize("N,lens", [(256, None), (129, None), (300, [100])])
+def test_quantize_mxfp4_bitexact(N, lens):
+    w, q, k, v = _small(1, 2, N, N, seed=30 + N)
+    xq, xs = binding.sage_quantize_qk(q, 1, lens=lens)
+    rq, rs = oracle.quantize_mxfp4(bf16_bits(q), lens=lens)
+    assert_qk_equal(1, xq, xs, rq, rs)
+
+
+def test_quantize_strided_packed_qkv():
+    """A packed [B, N, 3, H, D] QKV buffer quantizes like contiguous tensors."""
+    w, q, k, v = _small(1, 2, 300, 300, seed=5)
+    qkv = torch.stack([q, k, v], dim=2)
+    a = binding.sage_quantize_qk(qkv[:, :, 1], 0)
+    b = binding.sage_quantize_qk(k.contiguous(), 0)
+    torch.testing.assert_close(a[0], b[0], rtol=0, atol=0)
+    torch.testing.assert_close(a[1], b[1], rtol=0, atol=0)
+    va = binding.sage_quantize_v(qkv[:, :, 2])
+    vb = binding.sage_quantize_v(v.contiguous())
+    assert torch.equal(va[0], vb[0]) and torch.equal(va[1], vb[1])
+
+
+# ------------------------------------------------------------------ attention
+def test_attention_tiny_workload():
+    w = WORKLOADS["tiny"]
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(0, q, k, v)
+    qz, kz, vz = oracle_quantize(0, q, k, v)
+    assert_qk_equal(0, qq, qs, *qz)
+    assert_qk_equal(0, kq, ks, *kz)
+    assert_v_equal(vq, vs, *vz)
+    ro, rl = _oracle_attention(0, qz, kz, vz, w.Nq, w.Nk)
+    assert_attention_close(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (127, 127), (129, 129), (300, 300), (128, 1000),
+                                   (513, 77), (256, 384)])
+def test_attention_ragged_tails(Nq, Nk):
+    w, q, k, v = _small(1, 2, Nq, Nk, seed=Nq * 7 + Nk)
+    _, _, _, o, lse = _run_gpu(0, q, k, v)
+    qz, kz, vz = oracle_quantize(0, q, k, v)
+    ro, rl = _oracle_attention(0, qz, kz, vz, Nq, Nk)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_cross_ragged_k_lens():
+    w, q, k, v = _small(2, 2, 300, 512, seed=41)
+    lens = [512, 300]
+    _, _, _, o, lse = _run_gpu(0, q, k, v, k_lens=lens)
+    qz, kz, vz = oracle_quantize(0, q, k, v, k_lens=lens)
+    ro, rl = _oracle_attention(0, qz, kz, vz, 300, 512, k_lens=lens)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_zero_length_batch():
+    w, q, k, v = _small(2, 2, 200, 256, seed=42)
+    lens = [0, 256]
+    _, _, _, o, lse = _run_gpu(0, q, k, v, k_lens=lens)
+    assert torch.all(o[0] == 0)
+    assert torch.all(torch.isneginf(lse[0]))
+    qz, kz, vz = oracle_quantize(0, q, k, v, k_lens=lens)
+    ro, rl = _oracle_attention(0, qz, kz, vz, 200, 256, k_lens=lens)
+    assert_attention_close(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_attention_split_kv(splits):
+    w, q, k, v = _small(1, 2, 256, 1000, seed=43)
+    _, _, _, o, lse = _run_gpu(0, q, k, v, num_splits=splits)
+    qz, kz, vz = oracle_quantize(0, q, k, v)
+    ro, rl = _oracle_attention(0, qz, kz, vz, 256, 1000)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_softmax_scale():
+    w, q, k, v = _small(1, 2, 256, 256, seed=44)
+    _, _, _, o, lse = _run_gpu(0, q, k, v, softmax_scale=0.3)
+    qz, kz, vz = oracle_quantize(0, q, k, v)
+    ro, rl = _oracle_attention(0, qz, kz, vz, 256, 256, softmax_scale=0.3)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_kv_block_reversal_invariance():
+    """Reversing the order of whole 128-key blocks (Nk a multiple of 128) maps
+    quantization blocks onto quantization blocks: same codes, same output up
+    to FP32 summation order."""
+    w, q, k, v = _small(1, 2, 256, 512, seed=45)
+    _, _, _, o1, l1 = _run_gpu(0, q, k, v)
+    idx = torch.cat([torch.arange(b * 128, (b + 1) * 128) for b in reversed(range(4))]).cuda()
+    _, _, _, o2, l2 = _run_gpu(0, q, k[:, idx], v[:, idx])
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-4
+
+
+def test_attention_output_strides():
+    """O written through caller strides ([B, H, N, D] memory viewed as [B, N, H, D])."""
+    w, q, k, v = _small(1, 2, 200, 256, seed=46)
+    qq, qs = binding.sage_quantize_qk(q, 0)
+    kq, ks = binding.sage_quantize_qk(k, 0)
+    vq, vs = binding.sage_quantize_v(v)
+    base = torch.zeros((1, 2, 200, 128), dtype=torch.bfloat16, device="cuda")
+    out = base.permute(0, 2, 1, 3)
+    o, lse = binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=200, Nk=256, out=out)
+    o_ref, _ = binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=200, Nk=256)
+    assert torch.equal(out, o_ref)
+
+
+def test_device_status_reports_bad_k_lens():
+    w, q, k, v = _small(1, 1, 128, 128, seed=47)
+    qq, qs = binding.sage_quantize_qk(q, 0)
+    kq, ks = binding.sage_quantize_qk(k, 0)
+    vq, vs = binding.sage_quantize_v(v)
+    binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=128, Nk=128, k_lens=[129])
+    assert binding.sage_last_device_status() == -7  # SAGE_ERR_DEVICE_ARG
+    assert binding.sage_last_device_status() == 0   # read-and-clear
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _sample_rows(Nq):
+    rows = sorted(set([0, 1, 127, 128, Nq // 3, Nq // 2 + 5, Nq - 129, Nq - 2, Nq - 1]))
+    return [r for r in rows if 0 <= r < Nq]
+
+
+@pytest.mark.parametrize("name,heads", [("image_dit", None), ("video_dit", [0, 17, 39]),
+                                        ("long_video", [0, 39]), ("cross", None),
+                                        ("cross_ragged", None)])
+def test_full_size_workload(name, heads):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(0, q, k, v, k_lens=w.k_lens)
+    hs = list(range(w.H)) if heads is None else heads
+    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
+    qz, kz, vz = oracle_quantize(0, sub(q), sub(k), sub(v), k_lens=w.k_lens)
+    assert_qk_equal(0, qq[:, hs], qs[:, hs], *qz)
+    assert_qk_equal(0, kq[:, hs], ks[:, hs], *kz)
+    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
+    rows = _sample_rows(w.Nq)
+    ro, rl = _oracle_attention(0, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
+    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)

@@ -1,0 +1,88 @@
+"""Host-only checks of the C-ABI library: it builds, loads without a GPU,
+exports every entry point the header declares, sizes buffers as documented
+and rejects invalid calls before any launch."""
+import ctypes
+import re
+
+import pytest
+
+from precision_attention_diffusion_sage_gb300 import build as sage_build
+
+sage_build.build()
+from precision_attention_diffusion_sage_gb300 import binding  # noqa: E402
+
+
+def test_exports_every_header_symbol():
+    names = binding.header_symbols()
+    assert {"sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd"} <= set(names)
+    lib = binding.library()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_header_has_no_torch_types():
+    text = open(binding.HEADER_PATH).read()
+    for token in ("at::", "torch::", "Tensor", "#include <torch", "c10::"):
+        assert token not in text, token
+    assert 'extern "C"' in text
+
+
+def test_quantized_bytes():
+    B, N, H, D = 2, 300, 3, 128
+    Np = 384
+    assert binding.sage_quantized_bytes(0, 0, B, N, H, D) == B * H * Np * D * 2
+    assert binding.sage_quantized_bytes(0, 1, B, N, H, D) == B * H * 3 * 4
+    assert binding.sage_quantized_bytes(1, 0, B, N, H, D) == B * H * Np * 64
+    assert binding.sage_quantized_bytes(1, 1, B, N, H, D) == B * H * Np * 4
+    assert binding.sage_quantized_bytes(0, 2, B, N, H, D) == B * H * D * Np
+    assert binding.sage_quantized_bytes(0, 3, B, N, H, D) == B * H * D * 4
+    assert binding.sage_quantized_bytes(0, 0, B, N, H, 64) == 0      # D must be 128
+    assert binding.sage_quantized_bytes(7, 0, B, N, H, D) == 0       # unknown format
+
+
+def test_workspace_bytes():
+    assert binding.sage_workspace_bytes(0, 0, 1, 2, 256, 256) == 0
+    assert binding.sage_workspace_bytes(1, 0, 1, 2, 1000, 1000) == 1 * 2 * 2 * 128 * 4
+    # forced splits: [splits][B][H][Nq][D] partial O + [splits][B][H][Nq] LSE, FP32
+    assert binding.sage_workspace_bytes(2, 0, 1, 2, 256, 1024, 128, 3) == 3 * 2 * 256 * 129 * 4
+    assert binding.sage_workspace_bytes(2, 0, 1, 2, 256, 1024, 128, 1) == 0
+    # large grids need no split
+    assert binding.sage_workspace_bytes(2, 0, 1, 40, 14040, 14040) == 0
+
+
+def _status(name):
+    return {"SAGE_OK": 0, "SAGE_ERR_INVALID_ARG": -1, "SAGE_ERR_UNSUPPORTED": -2,
+            "SAGE_ERR_WORKSPACE": -3}[name]
+
+
+def test_host_validation_rejects_before_launch():
+    lib = binding.library()
+    S = binding.Strides(0, 0, 0)
+    fake = ctypes.c_void_p(1 << 20)
+    # D != 128 and causal are unsupported
+    assert lib.sage_quantize_qk(0, fake, S, 1, 128, 1, 64, None, fake, fake, None) == -2
+    assert lib.sage_attn_fwd(0, fake, fake, fake, fake, fake, fake, None, 1, 1, 128, 128, 128,
+                             -1.0, 1, fake, S, None, None, 0, None, None) == -2
+    # unknown format
+    assert lib.sage_quantize_qk(9, fake, S, 1, 128, 1, 128, None, fake, fake, None) == -2
+    # null / misaligned pointers and bad strides
+    assert lib.sage_quantize_qk(0, None, S, 1, 128, 1, 128, None, fake, fake, None) == -1
+    assert lib.sage_quantize_qk(0, ctypes.c_void_p((1 << 20) + 2), S, 1, 128, 1, 128, None, fake,
+                                fake, None) == -1
+    assert lib.sage_quantize_qk(0, fake, binding.Strides(0, 130, 0), 1, 128, 1, 128, None, fake,
+                                fake, None) == -1
+    # empty inputs
+    assert lib.sage_quantize_qk(0, fake, S, 1, 0, 1, 128, None, fake, fake, None) == -1
+    # V quantization needs its workspace
+    assert lib.sage_quantize_v(fake, S, 1, 1000, 1, 128, None, fake, fake, None, 0, None) == -3
+    # attention with a forced split and no workspace
+    opts = binding.AttnOptions(4, 0)
+    assert lib.sage_attn_fwd(0, fake, fake, fake, fake, fake, fake, None, 1, 1, 128, 1024, 128,
+                             -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None) == -3
+
+
+def test_status_strings():
+    lib = binding.library()
+    for code in range(-7, 1):
+        assert lib.sage_status_string(code).decode().startswith("SAGE_")
+    assert binding.sage_version().startswith("libsage")
