@@ -127,6 +127,29 @@ sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64
                               int64_t D, const int32_t* lens, void* v_q, float* v_scale,
                               void* workspace, size_t ws_bytes, sage_stream_t stream);
 
+/* The pages this library restates have no counterpart to this entry point.
+ * sage_quantize_v for callers that cannot allocate device memory (a plugin
+ * inside a framework that owns all device memory through its own allocator,
+ * a service whose memory plan is fixed at start-up, a process out of
+ * allocation budget): same arguments, results and layouts as
+ * sage_quantize_v, but the partial-maximum scratch lives in an 8 MiB array
+ * compiled into the library, so the call allocates nothing and takes no
+ * workspace. The array is held by every device that loads the library until
+ * the process exits.
+ *   - Limit: B * H * ceil(N / 512) * 128 * 4 bytes must not exceed 8 MiB
+ *     (for example 40 heads, B*H = 40, up to N = 209,408 tokens); larger calls
+ *     return SAGE_ERR_WORKSPACE and launch nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents (nothing in it needs to start at zero: each call writes
+ *     every partial maximum it reads). Calls that overlap on the GPU (other
+ *     streams, other threads) race on it: serialise them. */
+sage_status_t sage_quantize_v_noalloc(const void* v, sage_strides_t vs, int64_t B, int64_t N,
+                                      int64_t H, int64_t D, const int32_t* lens, void* v_q,
+                                      float* v_scale, sage_stream_t stream);
+
 typedef struct {
   int32_t num_splits; /* KV splits: 0 = library choice, 1 = no split, >1 = forced */
   int32_t cta_mode;   /* reserved: 0 = library choice */
