@@ -99,19 +99,20 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 16):
+def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64):
     """Time the CPU oracle (as it stands) on a bounded sample of workload w:
-    quantization of one head's Q/K/V plus attention for R query rows of that
-    head, R calibrated to take about `seconds`. Returns (flops, time_s, desc)."""
+    quantization of the first `nh` heads' Q/K/V plus attention for `n` query
+    rows of those heads, sized from a short calibration run to take about
+    `seconds`. Returns (flops, time_s, description, rows)."""
     import numpy as np
     import oracle
     from precision_attention_diffusion_sage_gb300.inputs import bf16_bits, make_qkv
 
     q, k, v = make_qkv(w)
-    qb, kb, vb = (bf16_bits(t[:, :, :1]) for t in (q, k, v))
     lens = None if w.k_lens is None else w.k_lens
 
-    def run(rows):
+    def run(nh, rows):
+        qb, kb, vb = (bf16_bits(t[:, :, :nh]) for t in (q, k, v))
         t0 = time.perf_counter()
         qz = oracle.quantize_int8(qb)
         kz = oracle.quantize_int8(kb, lens=lens)
@@ -122,13 +123,17 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 16):
     def rows_of(n):
         return np.linspace(0, w.Nq - 1, n).astype(np.int64)
 
-    t_cal = run(rows_of(seed_rows))
-    n = int(min(w.Nq, max(seed_rows, seed_rows * seconds / max(t_cal, 1e-3))))
-    dt = run(rows_of(n))
+    t_cal = run(1, rows_of(min(seed_rows, w.Nq)))
+    units = min(seed_rows, w.Nq) * seconds / max(t_cal, 1e-3)   # (head, row) pairs
+    if units <= w.Nq:
+        nh, n = 1, int(max(min(seed_rows, w.Nq), units))
+    else:
+        nh, n = int(min(w.H, math.ceil(units / w.Nq))), w.Nq
+    dt = run(nh, rows_of(n))
     nk_sum = sum(w.k_lens) if w.k_lens else w.B * w.Nk
-    flops = 4.0 * n * (nk_sum / w.B) * w.D
-    desc = (f"oracle on head 0 of batch 0..{w.B - 1}: full Q/K/V quantization of that head "
-            f"+ attention for {n} of {w.Nq} query rows")
+    flops = 4.0 * nh * n * nk_sum * w.D
+    desc = (f"oracle on heads 0..{nh - 1} of every batch: full Q/K/V quantization of those heads "
+            f"+ attention for {n} of {w.Nq} query rows each")
     return flops, dt, desc, n
 
 

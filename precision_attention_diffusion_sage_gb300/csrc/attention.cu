@@ -11,18 +11,21 @@
 // GB300 design, per CTA (NQT query tiles of 128 rows of one (b, h)):
 //   warps 0 .. 4*NQT-1 : one softmax warpgroup per query tile; thread r owns
 //                        row r (TMEM lane r) of its tile.
-//   warp 4*NQT         : TMA producer (Q once, then K/V tiles into a ring).
+//   warp 4*NQT         : TMA producer of Q (once) and the K ring.
 //   warp 4*NQT+1       : tcgen05 MMA issuer; allocates/frees TMEM.
+//   warp 4*NQT+2       : TMA producer of the V ring (separate so that a K
+//                        load never waits for a V slot to free up).
 // TMEM per tile: S (128 FP32 columns) and O (128 FP32 columns).
 // S = Q K^T runs as kind::f16 on the INT8 codes held as FP16 (sm_103a has no
 // 8-bit integer MMA): products and partial sums are integers below 2^24, so
 // the FP32 accumulator holds the INT32 dot product exactly.
 // Softmax: t = S * alpha, alpha = s_q s_k softmax_scale log2(e); the running
-// row maximum m is an integer (ceil), raised only when it grows; O and l are
-// then rescaled by the exact power of two 2^(m_old - m_new). P8 =
-// E4M3(2^(t - m + 8)) goes to shared memory (128-byte swizzled, K-major) and
+// row reference m is an integer (ceil of the maximum), raised only when a tile
+// exceeds it by more than kHeadroom; O and l are then rescaled by the exact
+// power of two 2^(m_old - m_new). P8 = E4M3(2^(t - m + 8 - kHeadroom)) goes to
+// a double-buffered 128-byte-swizzled K-major tile in shared memory and
 // O += P8 * V8^T runs as kind::f8f6f4. Epilogue: O * s_v / l -> BF16,
-// LSE = (m + log2 l - 8) ln 2 (l is kept in units of 2^-8).
+// LSE = (m + log2 l - 8 + kHeadroom) ln 2 (l is kept in P8 units).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -38,17 +41,25 @@ namespace sage {
 namespace {
 
 constexpr float kLn2 = 0.693147180559945309f;
+// Headroom of the running integer maximum (log2 units). The reference m is
+// raised (and O, l rescaled by 2^(m_old - m_new)) only when a tile's ceil(max t)
+// exceeds m + kHeadroom; otherwise p8 = 2^(t - m + 8 - kHeadroom) <= 2^8 still
+// fits E4M3. Every p8 differs from the final-maximum encoding by an exact power
+// of two, so the two agree wherever both are normal E4M3 numbers (the band of
+// differing subnormals widens by at most kHeadroom binades, below 2^-12 of the
+// row maximum).
+constexpr float kHeadroom = 2.0f;
 
 template <int NQT, int STAGES>
 struct SmemLayout {
   static constexpr int kQ = 0;                          // NQT x 32 KB (FP16 128x128)
   static constexpr int kK = kQ + NQT * 32768;           // STAGES x 32 KB
   static constexpr int kV = kK + STAGES * 32768;        // STAGES x 16 KB (FP8 V^T 128x128)
-  static constexpr int kP = kV + STAGES * 16384;        // NQT x 16 KB (FP8 P 128x128)
-  static constexpr int kBar = kP + NQT * 16384;
+  static constexpr int kP = kV + STAGES * 16384;        // NQT x 2 x 16 KB (FP8 P, double buffer)
+  static constexpr int kBar = kP + NQT * 2 * 16384;
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
-  //           s_full[T], s_free[T], p_full[T], o_done[T], mma_final
-  static constexpr int kNumBars = 1 + 4 * STAGES + 4 * NQT + 1;
+  //           s_full[T], s_free[T], p_full[T][2], o_done[T][2], mma_final
+  static constexpr int kNumBars = 1 + 4 * STAGES + 6 * NQT + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem slot, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynamic = kBytes + 1024;        // + alignment slack
@@ -65,6 +76,38 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Four E4M3 codes packed in a word, element i in bits 8i+7 .. 8i.
+__device__ __forceinline__ uint32_t e4m3x4(float e0, float e1, float e2, float e3) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      " mov.b32 %0, {lo, hi};\n}\n"
+      : "=r"(r)
+      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
+  return r;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 128 values: eight independent 3-input-max chains, then a tree.
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = max3f(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+  for (int base = 24; base < 120; base += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = max3f(m[k], s[base + k], s[base + 8 + k]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], s[120 + k]);
+  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 // 2^k for an integer-valued k <= 0 (0 below the normal range).
@@ -103,11 +146,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// Threads per CTA: 6 warps for one query tile; 12 (three full warpgroups)
+// Threads per CTA: 7 warps for one query tile; 12 (three full warpgroups)
 // for two, so that registers can be moved to the softmax warpgroups with
 // setmaxnreg (each SM sub-partition holds one warp of every warpgroup).
 template <int NQT>
-constexpr int attn_threads() { return NQT == 1 ? 6 * 32 : 12 * 32; }
+constexpr int attn_threads() { return NQT == 1 ? 7 * 32 : 12 * 32; }
 
 template <int NQT, int STAGES>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
@@ -116,8 +159,9 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using L = SmemLayout<NQT, STAGES>;
   constexpr int kSoftmaxWarps = NQT * 4;
-  constexpr int kTmaWarp = kSoftmaxWarps;
+  constexpr int kTmaWarp = kSoftmaxWarps;       // Q and K loads
   constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  constexpr int kTmaVWarp = kSoftmaxWarps + 2;  // V loads
   constexpr uint32_t kTmemCols = NQT == 1 ? 256 : 512;
 
   extern __shared__ uint8_t smem_raw[];
@@ -136,8 +180,11 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   uint64_t* s_full = v_empty + STAGES;
   uint64_t* s_free = s_full + NQT;
   uint64_t* p_full = s_free + NQT;
-  uint64_t* o_done = p_full + NQT;
-  uint64_t* mma_final = o_done + NQT;
+  // p_full[t * 2 + buffer]: all 128 rows of that P buffer written. One per
+  // buffer: a fast warp may finish tile j+1 before a slow warp of its
+  // warpgroup has arrived for tile j, so the two must not share a barrier.
+  uint64_t* o_done = p_full + 2 * NQT;  // [t * 2 + buffer]: P V of that P buffer done
+  uint64_t* mma_final = o_done + 2 * NQT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -200,8 +247,10 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     for (int t = 0; t < NQT; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&s_free[t], 128);
-      mbar_init(&p_full[t], 128);
-      mbar_init(&o_done[t], 1);
+      mbar_init(&p_full[2 * t], 128);
+      mbar_init(&p_full[2 * t + 1], 128);
+      mbar_init(&o_done[2 * t], 1);
+      mbar_init(&o_done[2 * t + 1], 1);
     }
     mbar_init(mma_final, 1);
     *abort = 0;
@@ -222,106 +271,142 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   // compiled register count would leave the pool smaller than that.
   if (warp >= kSoftmaxWarps) {
     if constexpr (NQT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
+  // The producer and MMA warps run their loops warp-converged (every lane
+  // waits; values stay warp-uniform, so the TMA coordinates and the MMA
+  // descriptors live in uniform registers) and one elected lane issues.
   if (warp == kTmaWarp) {
-    // ================================================================ TMA producer
-    if (lane == 0) {
+    // ================================================================ TMA producer (Q, K)
+    if (elect_one()) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(q_full, NQT * 32768);
       for (int t = 0; t < NQT; ++t) {
         const int y = static_cast<int>(bh * Nq_pad + (static_cast<int64_t>(blockIdx.x) * NQT + t) * 128);
         tma_load_2d(sQ + t * 32768, &tmQ, q_full, 0, y);
         tma_load_2d(sQ + t * 32768 + 16384, &tmQ, q_full, 64, y);
       }
-      int kfills[STAGES], vfills[STAGES];
-      for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
-      for (int64_t it = 0; it < niter; ++it) {
-        const int s = static_cast<int>(it % STAGES);
-        const uint32_t u = static_cast<uint32_t>(it / STAGES);
-        const int64_t j = j0 + it;
-        if (u > 0 && !wait_or_abort(&k_empty[s], (u - 1) & 1, abort, p.status)) break;
+    }
+    __syncwarp();
+    int kfills[STAGES];
+    for (int s = 0; s < STAGES; ++s) kfills[s] = 0;
+    for (int64_t it = 0; it < niter; ++it) {
+      const int s = static_cast<int>(it % STAGES);
+      const uint32_t u = static_cast<uint32_t>(it / STAGES);
+      if (u > 0 && !warp_wait(&k_empty[s], (u - 1) & 1, abort, p.status)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], 32768);
-        const int yk = static_cast<int>(bh * Nk_pad + j * 128);
+        const int yk = static_cast<int>(bh * Nk_pad + (j0 + it) * 128);
         tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
         tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
-        ++kfills[s];
-        if (u > 0 && !wait_or_abort(&v_empty[s], (u - 1) & 1, abort, p.status)) break;
-        mbar_arrive_expect_tx(&v_full[s], 16384);
-        tma_load_2d(sV + s * 16384, &tmV, &v_full[s], static_cast<int>(j * 128),
-                    static_cast<int>(bh * 128));
-        ++vfills[s];
       }
-      // Drain: no TMA write may still be in flight when the CTA exits.
-      drain_wait(q_full, 0, p.status);
-      for (int s = 0; s < STAGES; ++s) {
-        if (kfills[s] > 0) drain_wait(&k_full[s], static_cast<uint32_t>(kfills[s] - 1) & 1, p.status);
-        if (vfills[s] > 0) drain_wait(&v_full[s], static_cast<uint32_t>(vfills[s] - 1) & 1, p.status);
-      }
+      __syncwarp();
+      ++kfills[s];
     }
+    // Drain: no TMA write may still be in flight when the CTA exits.
+    drain_wait(q_full, 0, p.status);
+    for (int s = 0; s < STAGES; ++s)
+      if (kfills[s] > 0) drain_wait(&k_full[s], static_cast<uint32_t>(kfills[s] - 1) & 1, p.status);
+  } else if (warp == kTmaVWarp) {
+    // ================================================================ TMA producer (V)
+    if (elect_one()) tma_prefetch_desc(&tmV);
+    __syncwarp();
+    int vfills[STAGES];
+    for (int s = 0; s < STAGES; ++s) vfills[s] = 0;
+    for (int64_t it = 0; it < niter; ++it) {
+      const int s = static_cast<int>(it % STAGES);
+      const uint32_t u = static_cast<uint32_t>(it / STAGES);
+      if (u > 0 && !warp_wait(&v_empty[s], (u - 1) & 1, abort, p.status)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&v_full[s], 16384);
+        tma_load_2d(sV + s * 16384, &tmV, &v_full[s], static_cast<int>((j0 + it) * 128),
+                    static_cast<int>(bh * 128));
+      }
+      __syncwarp();
+      ++vfills[s];
+    }
+    for (int s = 0; s < STAGES; ++s)
+      if (vfills[s] > 0) drain_wait(&v_full[s], static_cast<uint32_t>(vfills[s] - 1) & 1, p.status);
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_f32acc(128, 128);  // f16 x f16 -> f32
-      constexpr uint32_t kIdescO = idesc_f32acc(128, 128);  // e4m3 x e4m3 -> f32
-      bool ok = wait_or_abort(q_full, 0, abort, p.status);
-      if (ok) ok = wait_or_abort(&k_full[0], 0, abort, p.status);
-      tc_fence_after();
-      auto issue_s = [&](int t, int stage) {
-        const uint32_t d = tbase + t * 256;
-        const uint32_t qa = smem_u32(sQ + t * 32768);
-        const uint32_t ka = smem_u32(sK + stage * 32768);
+    constexpr uint32_t kIdescS = idesc_f32acc(128, 128);  // f16 x f16 -> f32
+    constexpr uint32_t kIdescO = idesc_f32acc(128, 128);  // e4m3 x e4m3 -> f32
+    // Descriptor low words of every operand buffer (k slices add a constant).
+    const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ));    // + t * 2048 per Q tile
+    const uint32_t k_lo = sw128_desc_lo(smem_u32(sK));    // + stage * 2048
+    const uint32_t p_lo = sw128_desc_lo(smem_u32(sP));    // + (2t + buffer) * 1024
+    const uint32_t v_lo = sw128_desc_lo(smem_u32(sV));    // + stage * 1024
+    // The elected lane is the same (lowest) lane every time, so the commits
+    // track the MMAs that lane issued.
+    auto issue_s = [&](int t, int stage) {
+      const uint32_t d = tbase + t * 256;
+      const uint32_t qa = q_lo + t * 2048, ka = k_lo + stage * 2048;
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss(d, sw128_kmajor_desc(qa + off), sw128_kmajor_desc(ka + off), kIdescS, k > 0);
+          const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+          mma_f16_ss_lo(d, qa + off, ka + off, kIdescS, k > 0);
         }
-      };
-      auto issue_pv = [&](int t, int stage, bool acc) {
-        const uint32_t d = tbase + t * 256 + 128;
-        const uint32_t pa = smem_u32(sP + t * 16384);
-        const uint32_t va = smem_u32(sV + stage * 16384);
+        mma_commit(&s_full[t]);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int t, int pbuf, int stage, bool acc) {
+      const uint32_t d = tbase + t * 256 + 128;
+      const uint32_t pa = p_lo + (t * 2 + pbuf) * 1024, va = v_lo + stage * 1024;
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_f8_ss(d, sw128_kmajor_desc(pa + k * 32), sw128_kmajor_desc(va + k * 32), kIdescO,
-                    (acc || k > 0) ? 1u : 0u);
-      };
-      if (ok) {
-        for (int t = 0; t < NQT; ++t) {
-          issue_s(t, 0);
-          mma_commit(&s_full[t]);
-        }
-        mma_commit(&k_empty[0]);
+          mma_f8_ss_lo(d, pa + k * 2, va + k * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+        mma_commit(&o_done[2 * t + pbuf]);
       }
-      for (int64_t it = 0; ok && it < niter; ++it) {
-        const int s = static_cast<int>(it % STAGES);
-        const uint32_t u = static_cast<uint32_t>(it / STAGES);
-        const bool has_next = it + 1 < niter;
-        const int sn = static_cast<int>((it + 1) % STAGES);
-        const uint32_t un = static_cast<uint32_t>((it + 1) / STAGES);
-        if (has_next && !(ok = wait_or_abort(&k_full[sn], un & 1, abort, p.status))) break;
-        if (!(ok = wait_or_abort(&v_full[s], u & 1, abort, p.status))) break;
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) mma_commit(bar);
+      __syncwarp();
+    };
+    bool ok = warp_wait(q_full, 0, abort, p.status);
+    if (ok) ok = warp_wait(&k_full[0], 0, abort, p.status);
+    tc_fence_after();
+    if (ok) {
+      for (int t = 0; t < NQT; ++t) issue_s(t, 0);
+      commit(&k_empty[0]);
+    }
+    for (int64_t it = 0; ok && it < niter; ++it) {
+      const int s = static_cast<int>(it % STAGES);
+      const uint32_t u = static_cast<uint32_t>(it / STAGES);
+      const bool has_next = it + 1 < niter;
+      const int sn = static_cast<int>((it + 1) % STAGES);
+      const uint32_t un = static_cast<uint32_t>((it + 1) / STAGES);
+      // Next S tiles first (each needs only its softmax warpgroup to have
+      // read the previous S), then this tile's P V products. V is waited
+      // for only right before the P V MMAs.
+      if (has_next) {
+        if (!(ok = warp_wait(&k_full[sn], un & 1, abort, p.status))) break;
         tc_fence_after();
         for (int t = 0; t < NQT && ok; ++t) {
-          if (has_next) {
-            if (!(ok = wait_or_abort(&s_free[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
-            tc_fence_after();
-            issue_s(t, sn);
-            mma_commit(&s_full[t]);
-          }
-          if (!(ok = wait_or_abort(&p_full[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
+          if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
           tc_fence_after();
-          issue_pv(t, s, it > 0);
-          mma_commit(&o_done[t]);
+          issue_s(t, sn);
         }
         if (!ok) break;
-        if (has_next) mma_commit(&k_empty[sn]);
-        mma_commit(&v_empty[s]);
+        commit(&k_empty[sn]);
       }
-      // All MMAs issued by this thread must finish before TMEM is freed.
-      mma_commit(mma_final);
-      drain_wait(mma_final, 0, p.status);
+      if (!(ok = warp_wait(&v_full[s], u & 1, abort, p.status))) break;
+      tc_fence_after();
+      for (int t = 0; t < NQT && ok; ++t) {
+        if (!(ok = warp_wait(&p_full[2 * t + (it & 1)], static_cast<uint32_t>(it >> 1) & 1, abort,
+                             p.status)))
+          break;
+        tc_fence_after();
+        issue_pv(t, static_cast<int>(it & 1), s, it > 0);
+      }
+      if (!ok) break;
+      commit(&v_empty[s]);
     }
+    // All MMAs issued by the elected lane must finish before TMEM is freed.
+    commit(mma_final);
+    drain_wait(mma_final, 0, p.status);
   }
   } else {
       if constexpr (NQT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
@@ -339,42 +424,46 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     float m = -INFINITY;  // running integer row maximum (log2 units)
     float l = 0.0f;       // running row sum of 2^(t - m + 8)
     bool ok = true;
-    const uint32_t p_row = smem_u32(sP + t * 16384) + r * 128;
+    const uint32_t p_row0 = smem_u32(sP + (t * 2) * 16384) + r * 128;  // P buffer 0; buffer 1 at +16 KB
     const uint32_t swz = static_cast<uint32_t>(r & 7);
 
+    float sk_next = __ldg(&kscale[j0]);  // K block scale, loaded one tile ahead
     for (int64_t it = 0; it < niter; ++it) {
       const int64_t j = j0 + it;
+      const float sk = sk_next;
+      if (it + 1 < niter) sk_next = __ldg(&kscale[j + 1]);
       if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
       tc_fence_after();
       float s[128];
+      {
+        uint32_t v[128];
+        tmem_ld128(tS, v);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(v[i]);
       }
       tc_fence_before();
       mbar_arrive(&s_free[t]);
 
-      const float alpha = alpha_q * __ldg(&kscale[j]);
+      const float alpha = alpha_q * sk;
       const int nvalid = static_cast<int>(nk - j * 128 < 128 ? nk - j * 128 : 128);
-      float mx = -INFINITY;
-      if (nvalid == 128) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      } else {
+      if (nvalid < 128) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c < nvalid) mx = fmaxf(mx, s[c]);
+          if (c >= nvalid) s[c] = -INFINITY;
       }
-      const float m_new = fmaxf(m, ceilf(mx * alpha));
+      const float mx = row_max128(s);
+      const float cand = ceilf(mx * alpha);
+      // First tile: set the reference. Later: raise it only past the headroom.
+      const float m_new = (it == 0) ? cand : (cand > m + kHeadroom ? cand : m);
       const bool rescale = (it > 0) && (m_new > m);
-      bool o_ready = false;
+      bool o_prev_done = false;  // P V of the previous tile known complete
       if (__any_sync(0xffffffffu, rescale)) {
-        // Conditional rescale: O_t holds PV up to the previous tile.
-        if (!(ok = warp_wait(&o_done[t], static_cast<uint32_t>(it - 1) & 1, abort, p.status))) break;
-        o_ready = true;
+        // Conditional rescale: O_t must hold P V up to the previous tile.
+        const int pb = static_cast<int>((it - 1) & 1);
+        if (!(ok = warp_wait(&o_done[2 * t + pb], static_cast<uint32_t>((it - 1) >> 1) & 1, abort,
+                             p.status)))
+          break;
+        o_prev_done = true;
         tc_fence_after();
         const float f = rescale ? exp2_neg_int(m - m_new) : 1.0f;
 #pragma unroll
@@ -389,58 +478,56 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         l *= f;
       }
       m = m_new;
-      const float bias = 8.0f - m;
+      const float bias = 8.0f - kHeadroom - m;
+      const uint32_t p_row = p_row0 + static_cast<uint32_t>(it & 1) * 16384;
 
-      // P_t is free once PV_t of the previous tile has completed.
-      if (it > 0 && !o_ready) {
-        if (!(ok = warp_wait(&o_done[t], static_cast<uint32_t>(it - 1) & 1, abort, p.status))) break;
+      // P buffer it%2 is free once P V of tile it-2 (same buffer) is complete.
+      if (it >= 2 && !o_prev_done) {
+        const int pb = static_cast<int>(it & 1);
+        if (!(ok = warp_wait(&o_done[2 * t + pb], static_cast<uint32_t>((it - 2) >> 1) & 1, abort,
+                             p.status)))
+          break;
       }
-      float lsum = 0.0f;
-      if (nvalid == 128) {
+      // x = S * alpha + (8 - m) two at a time (packed FP32x2 FMA), p8 = 2^x,
+      // four partial row sums (packed FP32x2 adds).
+      const float2 alpha2 = make_float2(alpha, alpha), bias2 = make_float2(bias, bias);
+      float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t pk[4];
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t pk[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = ch * 16 + q * 4;
-            const float e0 = ex2_approx(fmaf(s[c + 0], alpha, bias));
-            const float e1 = ex2_approx(fmaf(s[c + 1], alpha, bias));
-            const float e2 = ex2_approx(fmaf(s[c + 2], alpha, bias));
-            const float e3 = ex2_approx(fmaf(s[c + 3], alpha, bias));
-            lsum += (e0 + e1) + (e2 + e3);
-            pk[q] = e4m3x2(e0, e1) | (e4m3x2(e2, e3) << 16);
+        for (int q = 0; q < 4; ++q) {
+          const int c = ch * 16 + q * 4;
+          float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), alpha2, bias2);
+          float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), alpha2, bias2);
+          if (nvalid < 128) {  // masked keys contribute exactly 0
+            x01.x = c + 0 < nvalid ? x01.x : -INFINITY;
+            x01.y = c + 1 < nvalid ? x01.y : -INFINITY;
+            x23.x = c + 2 < nvalid ? x23.x : -INFINITY;
+            x23.y = c + 3 < nvalid ? x23.y : -INFINITY;
           }
-          st_shared_v4(p_row + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+          const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+          const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+          acc0 = __fadd2_rn(acc0, e01);
+          acc1 = __fadd2_rn(acc1, e23);
+          pk[q] = e4m3x4(e01.x, e01.y, e23.x, e23.y);
         }
-      } else {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = ch * 16 + q * 4;
-            const float e0 = c + 0 < nvalid ? ex2_approx(fmaf(s[c + 0], alpha, bias)) : 0.0f;
-            const float e1 = c + 1 < nvalid ? ex2_approx(fmaf(s[c + 1], alpha, bias)) : 0.0f;
-            const float e2 = c + 2 < nvalid ? ex2_approx(fmaf(s[c + 2], alpha, bias)) : 0.0f;
-            const float e3 = c + 3 < nvalid ? ex2_approx(fmaf(s[c + 3], alpha, bias)) : 0.0f;
-            lsum += (e0 + e1) + (e2 + e3);
-            pk[q] = e4m3x2(e0, e1) | (e4m3x2(e2, e3) << 16);
-          }
-          st_shared_v4(p_row + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
-        }
+        st_shared_v4(p_row + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
       }
-      l += lsum;
+      l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       fence_proxy_async_smem();
-      mbar_arrive(&p_full[t]);
+      mbar_arrive(&p_full[2 * t + (it & 1)]);
     }
 
     // ---- epilogue
-    if (ok) ok = warp_wait(&o_done[t], static_cast<uint32_t>(niter - 1) & 1, abort, p.status);
+    if (ok)
+      ok = warp_wait(&o_done[2 * t + static_cast<int>((niter - 1) & 1)],
+                     static_cast<uint32_t>((niter - 1) >> 1) & 1, abort, p.status);
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const float* sv = p.v_scale + bh * 128;
-      const float lse = (m + log2f(l) - 8.0f) * kLn2;
+      const float lse = (m + log2f(l) - 8.0f + kHeadroom) * kLn2;
       const bool store = row < p.Nq;
       if (p.num_splits > 1) {
         float* op = p.o_part + ((static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row) * 128;
