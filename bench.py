@@ -223,11 +223,18 @@ def main():
     aws_n = binding.sage_workspace_bytes(2, fmt, B, H, Nq, Nk, D, args.splits)
     aws = torch.empty(max(16, aws_n), dtype=torch.uint8, device=dev)
     nsplit = binding.attn_splits(B, H, Nq, Nk, args.splits)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # L2 flush between steps: reading 256 MiB leaves L2 holding clean lines of
+    # an unrelated buffer (a write would leave dirty lines whose write-back
+    # lands on the next kernel).
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
 
-    def quant():
+    def quant(evs=None):
         binding.sage_quantize_qk(q, fmt, out=qq, scale=qs)
+        if evs:
+            evs[0].record()
         binding.sage_quantize_qk(k, fmt, lens=k_lens, out=kq, scale=ks)
+        if evs:
+            evs[1].record()
         binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
 
     def attn():
@@ -245,16 +252,16 @@ def main():
     except Exception:
         gpu_id = str(local)
     clocks = ClockSampler(gpu_id)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks.start()
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        flush.sum()
         ev[i][0].record()
-        quant()
+        quant((ev[i][3], ev[i][4]))
         ev[i][1].record()
         attn()
         ev[i][2].record()
@@ -264,6 +271,9 @@ def main():
     clk = clocks.stop()
     assert binding.sage_last_device_status() == 0
     t_quant = [e[0].elapsed_time(e[1]) for e in ev]
+    t_qk = (statistics.mean(e[0].elapsed_time(e[3]) for e in ev),
+            statistics.mean(e[3].elapsed_time(e[4]) for e in ev),
+            statistics.mean(e[4].elapsed_time(e[1]) for e in ev))
     t_attn = [e[1].elapsed_time(e[2]) for e in ev]
     total_ms = sum(t_quant) + sum(t_attn)
     if world > 1:
@@ -299,7 +309,7 @@ def main():
         ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         barrier()
         for i in range(args.steps):
-            flush.zero_()
+            flush.sum()
             ee[i][0].record()
             e2e_step()
             ee[i][1].record()
@@ -335,10 +345,11 @@ def main():
         "dtype": "int8 QK^T (exact, fp16 tensor pipe) + fp8e4m3 PV", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
                    "k_lens": w.k_lens, "format": "int8_qk_fp8_v", "splits": nsplit,
-                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "l2": "flushed between steps (256 MiB read outside the timed events)",
                    "parallelism": f"replicas x{world}"},
         "attn_only_tflops": achieved,
         "quant_ms_per_step": statistics.mean(t_quant),
+        "quant_q_k_v_ms": [round(t, 4) for t in t_qk],
         "attn_ms_per_step": attn_ms,
         "quant_gbs": quant_bytes / (statistics.mean(t_quant) * 1e-3) / 1e9,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -32,7 +32,8 @@
  *   - BF16 inputs use element strides (sage_strides_t) over a logical
  *     [B][N][H][D] tensor; the D stride must be 1, the base pointer 16-byte
  *     aligned and the b/n/h strides multiples of 8 elements.
- *   - Head dimension D must be 128. Only sm_103 devices are accepted.
+ *   - Head dimension D must be 128, N at most 4,194,240 tokens. Only sm_103
+ *     devices are accepted.
  */
 #ifndef SAGE_H
 #define SAGE_H
@@ -95,8 +96,8 @@ size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, 
                             int64_t D);
 
 /* Workspace bytes. op: 0 = sage_quantize_qk (always 0), 1 = sage_quantize_v
- * (per-channel partial maxima), 2 = sage_attn_fwd with `num_splits` KV
- * splits (0 = the split count the library would choose). */
+ * (per-(b,h,channel) maxima, B*H*128*4 bytes), 2 = sage_attn_fwd with
+ * `num_splits` KV splits (0 = the split count the library would choose). */
 size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int64_t Nq,
                             int64_t Nk, int64_t D, int num_splits);
 
@@ -120,7 +121,8 @@ sage_status_t sage_quantize_qk(sage_format_t fmt, const void* x, sage_strides_t 
  * sage_quant_v_amax_finalize and sage_quant_v kernels; reading: one FP32
  * scale absmax/448 per (b,h,channel) over valid tokens, codes E4M3 with round
  * to nearest even and saturation, written token-contiguous).
- * Two launches: partial maxima into `workspace`, then finalize + quantize.
+ * A clear of the workspace, then two launches: channel maxima of every
+ * 128-token block folded into `workspace`, then finalize + quantize.
  *   workspace : device scratch of at least sage_workspace_bytes(1, ...) bytes,
  *               16-byte aligned; contents on entry are ignored. */
 sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64_t N, int64_t H,
@@ -132,20 +134,19 @@ sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64
  * inside a framework that owns all device memory through its own allocator,
  * a service whose memory plan is fixed at start-up, a process out of
  * allocation budget): same arguments, results and layouts as
- * sage_quantize_v, but the partial-maximum scratch lives in an 8 MiB array
+ * sage_quantize_v, but the channel-maximum scratch lives in an 8 MiB array
  * compiled into the library, so the call allocates nothing and takes no
  * workspace. The array is held by every device that loads the library until
  * the process exits.
- *   - Limit: B * H * ceil(N / 512) * 128 * 4 bytes must not exceed 8 MiB
- *     (for example 40 heads, B*H = 40, up to N = 209,408 tokens); larger calls
- *     return SAGE_ERR_WORKSPACE and launch nothing.
+ *   - Limit: B * H * 128 * 4 bytes must not exceed 8 MiB, i.e. B * H <= 16384
+ *     (any N); larger calls return SAGE_ERR_WORKSPACE and launch nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
  *   - All calls on a device share the one array and it keeps the previous
- *     call's contents (nothing in it needs to start at zero: each call writes
- *     every partial maximum it reads). Calls that overlap on the GPU (other
- *     streams, other threads) race on it: serialise them. */
+ *     call's contents; each call clears the part it uses (on its stream)
+ *     before using it. Calls that overlap on the GPU (other streams, other
+ *     threads) race on it: serialise them. */
 sage_status_t sage_quantize_v_noalloc(const void* v, sage_strides_t vs, int64_t B, int64_t N,
                                       int64_t H, int64_t D, const int32_t* lens, void* v_q,
                                       float* v_scale, sage_stream_t stream);

@@ -28,11 +28,9 @@
 // LSE = (m + log2 l - 8 + kHeadroom) ln 2 (l is kept in P8 units).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <cmath>
 #include <cstdio>
-#include <mutex>
 
 #include "attention.cuh"
 #include "sm103_ptx.cuh"
@@ -619,31 +617,12 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const AttnParams p) {
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-bool get_encode() {
-  std::call_once(g_encode_once, []() {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode != nullptr;
-}
-
 bool make_map_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize,
                  uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[2] = {inner, rows};
+  const uint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  const uint32_t box[2] = {box_inner, box_rows};
+  return encode_tiled(m, dt, 2, ptr, dims, strides, box, true);
 }
 
 template <int NQT, int STAGES>
@@ -684,7 +663,6 @@ int attn_auto_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
 }
 
 cudaError_t launch_attention_i8f8(const AttnLaunch& a, cudaStream_t stream) {
-  if (!get_encode()) return cudaErrorNotSupported;
   const int64_t Nq_pad = pad128(a.p.Nq), Nk_pad = pad128(a.p.Nk);
   CUtensorMap mq, mk, mv;
   if (!make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128,

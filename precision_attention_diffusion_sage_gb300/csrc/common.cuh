@@ -1,5 +1,6 @@
 // Shared definitions between the kernels and the host layer of libsage.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -13,6 +14,13 @@ constexpr int kHeadDim = 128;
 constexpr int kTile = 128;  // tokens per quantization block and per MMA tile
 
 __host__ __device__ constexpr int64_t pad128(int64_t n) { return (n + 127) / 128 * 128; }
+
+// TMA tensor map of a `rank`-dimensional tensor (dims[0] innermost; strides in
+// bytes for dims 1..rank-1), no interleave, optional 128-byte swizzle,
+// zero fill out of bounds. Returns false if the driver rejects it.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* ptr,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  bool swizzle128);
 
 // ---- launchers (defined in quantize.cu / attention.cu, called from sage_api.cu)
 struct QuantQKArgs {
@@ -34,11 +42,11 @@ struct QuantVArgs {
   const int32_t* lens;
   uint8_t* out;   // [B][H][D][Npad]
   float* scale;   // [B][H][D]
-  float* partial; // [B][H][nchunks][D]
+  int* amax;      // [B][H][D] channel maxima as binary32 bit patterns (workspace)
   int* status;
 };
-constexpr int kVChunk = 512;  // tokens per partial-maximum chunk
-__host__ __device__ inline int64_t v_partial_chunks(int64_t N) { return (N + kVChunk - 1) / kVChunk; }
+// Workspace of the V quantization: one int per (b, h, channel).
+inline int64_t v_workspace_bytes(int64_t B, int64_t H) { return B * H * 128 * 4; }
 cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s);
 
 }  // namespace sage

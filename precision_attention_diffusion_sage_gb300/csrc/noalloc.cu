@@ -1,6 +1,6 @@
 // sage_quantize_v_noalloc: V quantization for callers that cannot allocate.
 //
-// sage_quantize_v needs device scratch for its per-channel partial maxima,
+// sage_quantize_v needs device scratch for its per-channel maxima,
 // which the caller normally allocates and passes in. Some callers cannot do
 // that at the point where they quantize: a plugin living inside a host
 // framework that owns every byte of device memory through its own allocator
@@ -26,7 +26,7 @@
 namespace sage {
 namespace {
 
-// 8 MiB of FP32 partial maxima: B * H * ceil(N / 512) * 128 floats at most.
+// 8 MiB of channel maxima: B * H * 128 four-byte words at most (B * H <= 16384).
 constexpr size_t kNoAllocScratchFloats = static_cast<size_t>(2) * 1024 * 1024;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
@@ -68,8 +68,8 @@ extern "C" sage_status_t sage_quantize_v_noalloc(const void* v, sage_strides_t v
   float* scratch = nullptr;
   const sage_status_t st = sage::noalloc_scratch(&scratch);
   if (st != SAGE_OK) return st;
-  // Every partial maximum the second kernel reads is written by the first
-  // kernel of the same call, so the array needs no clearing between calls.
+  // The regular path clears the words it uses on the caller's stream before
+  // folding the channel maxima into them, so stale contents never leak.
   return sage_quantize_v(v, vs, B, N, H, D, lens, v_q, v_scale, scratch,
                          sizeof(sage::g_noalloc_scratch), stream);
 }

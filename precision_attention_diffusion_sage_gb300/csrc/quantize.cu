@@ -1,6 +1,14 @@
 // Quantization kernels (HBM-bound): Q/K to INT8 with per-128-token-block
 // scales, Q/K to MXFP4 (E2M1 + E8M0 per 32 channels), V to FP8 E4M3 with
-// per-channel scales in two passes (partial maxima, then finalize+quantize).
+// per-channel scales in two passes (channel maxima of 128-token blocks
+// combined with an integer atomic maximum, then finalize + quantize).
+//
+// The codes are the IEEE binary32 quotient x / s rounded (to an integer, or
+// to E4M3) exactly as the definition states. The kernels compute the
+// quotient as x * (1/s) (within 1.5 ulp of it) and take the exact division
+// only for the rare values that lie within a few ulps of a rounding boundary,
+// so the result is bit-identical while the common path avoids a division per
+// element.
 //
 // Restates the preprocessing named on "new MHA v4 entrypoint ..." (the
 // sage_quant_kernel, sage_quant_mxfp4, sage_quant_v_amax_partial /
@@ -11,6 +19,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "sm103_ptx.cuh"
 
 namespace sage {
 namespace {
@@ -53,20 +62,43 @@ __device__ __forceinline__ float block_max_256(float v, float* red) {
   return m;
 }
 
-// INT8 code of x at scale s > 0: clamp(rne(x / s), -127, 127), returned as
-// its exact FP16 value.
-__device__ __forceinline__ __half int8_code(float x, float s) {
-  const float r = __fdiv_rn(x, s);
-  int q = __float2int_rn(r);
-  q = max(-127, min(127, q));
-  return __int2half_rn(q);
+// Round to the nearest integer, ties to even, for |x| < 2^22 (binary32 adds).
+__device__ __forceinline__ float round_rne(float x) {
+  return __fsub_rn(__fadd_rn(x, 12582912.0f), 12582912.0f);
+}
+
+// INT8 code of x at scale s > 0 (inv = 1/s): clamp(rne(x / s), -127, 127)
+// with x / s the IEEE binary32 quotient. r = x * inv is within 1.5 ulp of
+// that quotient (|r| <= 128, so within 2^-16); unless r is that close to a
+// half-integer the rounding agrees, otherwise the exact division decides.
+__device__ __forceinline__ float int8_code(float x, float s, float inv) {
+  const float r = __fmul_rn(x, inv);
+  float n = round_rne(r);
+  // Written so that a NaN (1/s overflowed for a subnormal s) also takes the
+  // exact path.
+  if (!(fabsf(__fsub_rn(r, n)) <= 0.5f - 0x1p-14f)) n = round_rne(__fdiv_rn(x, s));
+  return fminf(fmaxf(n, -127.0f), 127.0f);
+}
+
+// Branch-free form for the streaming kernels: n = rne(x * inv) via one FMA
+// with the 1.5 * 2^23 rounding constant, and `exact` set when the exact
+// product x * inv lies within 2^-14 of a half-integer (then x / s, which is
+// within 1.2e-5 of that product, may round the other way: the caller redoes
+// those few elements with the division). |n| <= 127 needs no clamp: x / s
+// never exceeds amax / s = 127 (1 + 2^-23).
+__device__ __forceinline__ float int8_code_fast(float x, float inv, bool& exact) {
+  const float t = __fmaf_rn(x, inv, 12582912.0f);
+  const float n = __fsub_rn(t, 12582912.0f);
+  const float d = __fmaf_rn(x, inv, -n);  // exact residual of the product
+  exact |= !(fabsf(d) <= 0.5f - 0x1p-14f);
+  return n;
 }
 
 // One CTA per (128-token block, h, b); 256 threads, each owning 8 channels of
 // 8 token rows.
 __global__ void __launch_bounds__(256) quantize_qk_int8_kernel(QuantQKArgs a) {
   __shared__ float red[8];
-  const int64_t blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
   const int64_t Np = pad128(a.N), nb = Np / 128;
   const int64_t nv = valid_tokens(a.lens, b, a.N, a.status);
   const int col = (threadIdx.x & 15) * 8;
@@ -88,6 +120,7 @@ __global__ void __launch_bounds__(256) quantize_qk_int8_kernel(QuantQKArgs a) {
   }
   amax = block_max_256(amax, red);
   const float s = __fdiv_rn(amax, 127.0f);
+  const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
   const int64_t bh = b * a.H + h;
   if (threadIdx.x == 0) static_cast<float*>(a.scale)[bh * nb + blk] = s;
   __half* out = static_cast<__half*>(a.out);
@@ -96,16 +129,18 @@ __global__ void __launch_bounds__(256) quantize_qk_int8_kernel(QuantQKArgs a) {
     const int64_t n = blk * 128 + r0 + i * 16;
     float f[8];
     unpack8(raw[i], f);
-    __half hq[8];
+    uint32_t w[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      hq[k] = (n < nv && s > 0.0f) ? int8_code(f[k], s) : __float2half_rn(0.0f);
-    uint4 o;
-    o.x = static_cast<uint32_t>(__half_as_ushort(hq[0])) | (static_cast<uint32_t>(__half_as_ushort(hq[1])) << 16);
-    o.y = static_cast<uint32_t>(__half_as_ushort(hq[2])) | (static_cast<uint32_t>(__half_as_ushort(hq[3])) << 16);
-    o.z = static_cast<uint32_t>(__half_as_ushort(hq[4])) | (static_cast<uint32_t>(__half_as_ushort(hq[5])) << 16);
-    o.w = static_cast<uint32_t>(__half_as_ushort(hq[6])) | (static_cast<uint32_t>(__half_as_ushort(hq[7])) << 16);
-    *reinterpret_cast<uint4*>(out + (bh * Np + n) * 128 + col) = o;
+    for (int k = 0; k < 4; ++k) {
+      float c0 = 0.0f, c1 = 0.0f;
+      if (n < nv && s > 0.0f) {
+        c0 = int8_code(f[2 * k], s, inv);
+        c1 = int8_code(f[2 * k + 1], s, inv);
+      }
+      const __half2 h2 = __floats2half2_rn(c0, c1);  // exact: |c| <= 127
+      w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(out + (bh * Np + n) * 128 + col) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -142,7 +177,7 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&x)[8], float scale) {
 // MXFP4: 256 threads = 16 token rows per pass, 16 lanes per row, each lane 8
 // channels; 4 lanes share one 32-channel group. 64 rows per CTA.
 __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
-  const int64_t h = blockIdx.y, b = blockIdx.z;
+  const int64_t h = blockIdx.x, b = blockIdx.z;
   const int64_t Np = pad128(a.N);
   const int64_t nv = valid_tokens(a.lens, b, a.N, a.status);
   const int64_t bh = b * a.H + h;
@@ -152,7 +187,7 @@ __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
   uint8_t* e8 = static_cast<uint8_t*>(a.scale);
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
-    const int64_t n = blockIdx.x * 64 + pass * 16 + (threadIdx.x >> 4);  // < Np by the grid
+    const int64_t n = blockIdx.y * 64 + pass * 16 + (threadIdx.x >> 4);  // < Np by the grid
     float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (n < nv) unpack8(ldg_v4(a.x + b * a.sb + n * a.sn + h * a.sh + col), f);
     float amax = 0.0f;
@@ -174,21 +209,25 @@ __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
   }
 }
 
-// V pass 1: per-channel maxima over chunks of kVChunk tokens.
-__global__ void __launch_bounds__(256) v_amax_partial_kernel(QuantVArgs a) {
+// V pass 1: channel maxima of one 128-token block, folded into the per-(b,h)
+// channel maxima with an integer atomic maximum (non-negative binary32
+// values order like their bit patterns).
+__global__ void __launch_bounds__(256) v_amax_kernel(QuantVArgs a) {
   __shared__ float red[16][128];
-  const int64_t chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
   const int64_t nv = valid_tokens(a.lens, b, a.N, a.status);
   const int col = (threadIdx.x & 15) * 8;
   const int rg = threadIdx.x >> 4;
   float m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const int64_t n0 = chunk * kVChunk;
-  const int64_t n1 = min(n0 + kVChunk, nv);
-  for (int64_t n = n0 + rg; n < n1; n += 16) {
-    float f[8];
-    unpack8(ldg_v4(a.v + b * a.sb + n * a.sn + h * a.sh + col), f);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], fabsf(f[k]));
+  for (int i = 0; i < 8; ++i) {
+    const int64_t n = blk * 128 + rg + 16 * i;
+    if (n < nv) {
+      float f[8];
+      unpack8(ldg_v4(a.v + b * a.sb + n * a.sn + h * a.sh + col), f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], fabsf(f[k]));
+    }
   }
 #pragma unroll
   for (int k = 0; k < 8; ++k) red[rg][col + k] = m[k];
@@ -197,8 +236,7 @@ __global__ void __launch_bounds__(256) v_amax_partial_kernel(QuantVArgs a) {
     float r = red[0][threadIdx.x];
 #pragma unroll
     for (int g = 1; g < 16; ++g) r = fmaxf(r, red[g][threadIdx.x]);
-    const int64_t nch = v_partial_chunks(a.N);
-    a.partial[((b * a.H + h) * nch + chunk) * 128 + threadIdx.x] = r;
+    if (r > 0.0f) atomicMax(&a.amax[(b * a.H + h) * 128 + threadIdx.x], __float_as_int(r));
   }
 }
 
@@ -208,22 +246,43 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two E4M3 codes of x / s (IEEE binary32 quotient) for s > 0, inv = 1/s.
+// r = x * inv is within 1.5 ulp of the quotient; when the codes of r shrunk
+// and grown by 2^-21 agree, every value in between (the quotient included)
+// has that code; otherwise the exact divisions decide.
+__device__ __forceinline__ uint32_t e4m3x2_div(float x0, float x1, float s, float inv) {
+  const float r0 = __fmul_rn(x0, inv), r1 = __fmul_rn(x1, inv);
+  const uint32_t lo = e4m3x2(__fmul_rn(r0, 1.0f - 0x1p-21f), __fmul_rn(r1, 1.0f - 0x1p-21f));
+  const uint32_t hi = e4m3x2(__fmul_rn(r0, 1.0f + 0x1p-21f), __fmul_rn(r1, 1.0f + 0x1p-21f));
+  if (lo == hi && inv < INFINITY) return lo;  // (1/s overflows only for a subnormal s)
+  return e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+}
+
+// Branch-free form: codes of r = x * inv shrunk and grown by 2^-21; when they
+// differ (`exact` set) the caller redoes the pair with the division.
+__device__ __forceinline__ uint32_t e4m3x2_fast(float x0, float x1, float inv, bool& exact) {
+  const float r0 = __fmul_rn(x0, inv), r1 = __fmul_rn(x1, inv);
+  const uint32_t lo = e4m3x2(__fmul_rn(r0, 1.0f - 0x1p-21f), __fmul_rn(r1, 1.0f - 0x1p-21f));
+  const uint32_t hi = e4m3x2(__fmul_rn(r0, 1.0f + 0x1p-21f), __fmul_rn(r1, 1.0f + 0x1p-21f));
+  exact |= (lo != hi);
+  return lo;
+}
+
 // V pass 2: finalize the channel scales, quantize one 128-token tile and
 // write it transposed ([D][Npad], token-contiguous) through shared memory.
 __global__ void __launch_bounds__(256) v_quantize_kernel(QuantVArgs a) {
   constexpr int kPitchWords = 33;  // 128 tokens = 32 words, +1 to spread banks
   __shared__ uint32_t tileT[128 * kPitchWords];
-  __shared__ float sv[128];
-  const int64_t tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  __shared__ float sv[128], sinv[128];
+  const int64_t h = blockIdx.x, tile = blockIdx.y, b = blockIdx.z;
   const int64_t nv = valid_tokens(a.lens, b, a.N, a.status);
   const int64_t bh = b * a.H + h;
   const int64_t Np = pad128(a.N);
   if (threadIdx.x < 128) {
-    const int64_t nch = v_partial_chunks(a.N);
-    float m = 0.0f;
-    for (int64_t c = 0; c < nch; ++c) m = fmaxf(m, a.partial[(bh * nch + c) * 128 + threadIdx.x]);
+    const float m = __int_as_float(a.amax[bh * 128 + threadIdx.x]);
     const float s = __fdiv_rn(m, 448.0f);
     sv[threadIdx.x] = s;
+    sinv[threadIdx.x] = s > 0.0f ? __frcp_rn(s) : 0.0f;
     if (tile == 0) a.scale[bh * 128 + threadIdx.x] = s;
   }
   __syncthreads();
@@ -246,14 +305,10 @@ __global__ void __launch_bounds__(256) v_quantize_kernel(QuantVArgs a) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int d = cg * 8 + k;
-      const float s = sv[d];
-      float r[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t n = tile * 128 + t0 + u;
-        r[u] = (n < nv && s > 0.0f) ? __fdiv_rn(f[u][k], s) : 0.0f;
-      }
-      tileT[d * kPitchWords + t0 / 4] = e4m3x2(r[0], r[1]) | (e4m3x2(r[2], r[3]) << 16);
+      const float s = sv[d], inv = sinv[d];
+      uint32_t w = 0;
+      if (s > 0.0f) w = e4m3x2_div(f[0][k], f[1][k], s, inv) | (e4m3x2_div(f[2][k], f[3][k], s, inv) << 16);
+      tileT[d * kPitchWords + t0 / 4] = w;
     }
   }
   __syncthreads();
@@ -266,31 +321,377 @@ __global__ void __launch_bounds__(256) v_quantize_kernel(QuantVArgs a) {
   }
 }
 
+
+// ----------------------------------------------------------------------------
+// TMA-fed persistent variants. A grid of about two CTAs per SM walks the
+// 128-token blocks (head index fastest, so concurrent CTAs read contiguous
+// token rows); each block's 128 x 128 BF16 tile arrives by one 4-D TMA box
+// into a ring of shared-memory stages, prefetched kStages - 1 blocks ahead.
+// Thread 0 issues the loads; a stage is reused only after the __syncthreads
+// that ends the block that read it.
+constexpr int kQStages = 3;
+constexpr int kBlockBytes = 128 * 128 * 2;
+
+struct BlockCoord {
+  int64_t b, h, blk;
+};
+__device__ __forceinline__ BlockCoord block_coord(int64_t i, int64_t H, int64_t nb) {
+  BlockCoord c;
+  c.h = i % H;
+  c.blk = (i / H) % nb;
+  c.b = i / (H * nb);
+  return c;
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+// Shared pipeline state of the persistent block loop.
+template <int STAGES>
+struct BlockRing {
+  uint8_t* base;
+  uint64_t* full;
+  int issued;  // loads issued by thread 0
+
+  __device__ uint8_t* stage(int64_t k) const { return base + (k % STAGES) * kBlockBytes; }
+  __device__ void init(uint8_t* smem, volatile int* abort) {
+    base = smem;
+    full = reinterpret_cast<uint64_t*>(base + STAGES * kBlockBytes);
+    issued = 0;
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+      *abort = 0;
+      fence_barrier_init();
+    }
+    __syncthreads();
+  }
+  // Thread 0: load the k-th block of this CTA (if it exists) into stage k % STAGES.
+  __device__ void load(const CUtensorMap* map, int64_t k, int64_t total, int64_t H, int64_t nb) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (threadIdx.x != 0 || i >= total) return;
+    const BlockCoord c = block_coord(i, H, nb);
+    const int s = static_cast<int>(k % STAGES);
+    mbar_arrive_expect_tx(&full[s], kBlockBytes);
+    tma_load_4d(stage(k), map, &full[s], 0, static_cast<int32_t>(c.h),
+                static_cast<int32_t>(c.blk * 128), static_cast<int32_t>(c.b));
+    ++issued;
+  }
+  // Every thread waits; the outcome is made uniform over the CTA (the
+  // caller's barriers must see every thread).
+  __device__ bool wait(int64_t k, volatile int* abort, int* status) {
+    const int s = static_cast<int>(k % STAGES);
+    bool ok = mbar_wait(&full[s], static_cast<uint32_t>(k / STAGES) & 1, abort);
+    if (!ok) {
+      *abort = 1;
+      atomicOr(status, kStatusTimeout);
+    }
+    return __syncthreads_and(ok) != 0;
+  }
+  // Thread 0 after the loop: wait (bounded) for loads that were issued but
+  // not consumed (only after an abort), so no TMA write outlives the CTA.
+  __device__ void drain(int64_t consumed, int* status) {
+    if (threadIdx.x != 0) return;
+    const int zero = 0;
+    for (int64_t k = consumed; k < issued; ++k)
+      if (!mbar_wait(&full[k % STAGES], static_cast<uint32_t>(k / STAGES) & 1, &zero))
+        atomicOr(status, kStatusTimeout);
+  }
+};
+
+__global__ void __launch_bounds__(256, 2) quantize_qk_int8_tma_kernel(
+    const __grid_constant__ CUtensorMap tmX, QuantQKArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float red[8];
+  __shared__ int abort_flag;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  BlockRing<kQStages> ring;
+  ring.init(base, &abort_flag);
+  const int64_t Np = pad128(a.N), nb = Np / 128, total = a.B * a.H * nb;
+  const int col = (threadIdx.x & 15) * 8;
+  const int r0 = threadIdx.x >> 4;
+  __half* out = static_cast<__half*>(a.out);
+  float* scale = static_cast<float*>(a.scale);
+  for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmX, k, total, a.H, nb);
+  int64_t k = 0;
+  for (;; ++k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (i >= total) break;
+    ring.load(&tmX, k + kQStages - 1, total, a.H, nb);
+    if (!ring.wait(k, &abort_flag, a.status)) break;
+    const BlockCoord c = block_coord(i, a.H, nb);
+    const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
+    const uint8_t* tile = ring.stage(k);
+    uint4 raw[8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int rr = r0 + 16 * j;
+      raw[j] = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
+      if (c.blk * 128 + rr >= nv) raw[j] = make_uint4(0, 0, 0, 0);
+      float f[8];
+      unpack8(raw[j], f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+    }
+    amax = block_max_256(amax, red);
+    const float s = __fdiv_rn(amax, 127.0f);
+    const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
+    const int64_t bh = c.b * a.H + c.h;
+    if (threadIdx.x == 0) scale[bh * nb + c.blk] = s;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t row = c.blk * 128 + r0 + 16 * j;
+      float f[8], n[8];
+      unpack8(raw[j], f);
+      bool redo = false;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) n[q] = int8_code_fast(f[q], inv, redo);
+      if (s == 0.0f) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) n[q] = 0.0f;
+      } else if (redo) {  // rare: a near-tie (or a subnormal scale) in this row
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          n[q] = fminf(fmaxf(round_rne(__fdiv_rn(f[q], s)), -127.0f), 127.0f);
+      }
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 h2 = __floats2half2_rn(n[2 * q], n[2 * q + 1]);  // exact
+        w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(out + (bh * Np + row) * 128 + col) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();  // stage k % kQStages (and red[]) free again
+  }
+  ring.drain(k, a.status);
+}
+
+__global__ void __launch_bounds__(256, 2) v_amax_tma_kernel(const __grid_constant__ CUtensorMap tmV,
+                                                            QuantVArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float red[16][128];
+  __shared__ int abort_flag;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  BlockRing<kQStages> ring;
+  ring.init(base, &abort_flag);
+  const int64_t nb = pad128(a.N) / 128, total = a.B * a.H * nb;
+  const int col = (threadIdx.x & 15) * 8;
+  const int rg = threadIdx.x >> 4;
+  for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmV, k, total, a.H, nb);
+  int64_t k = 0;
+  for (;; ++k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (i >= total) break;
+    ring.load(&tmV, k + kQStages - 1, total, a.H, nb);
+    if (!ring.wait(k, &abort_flag, a.status)) break;
+    const BlockCoord c = block_coord(i, a.H, nb);
+    const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
+    const uint8_t* tile = ring.stage(k);
+    float m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int rr = rg + 16 * j;
+      if (c.blk * 128 + rr < nv) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m[q] = fmaxf(m[q], fabsf(f[q]));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) red[rg][col + q] = m[q];
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      float r = red[0][threadIdx.x];
+#pragma unroll
+      for (int g = 1; g < 16; ++g) r = fmaxf(r, red[g][threadIdx.x]);
+      if (r > 0.0f) atomicMax(&a.amax[(c.b * a.H + c.h) * 128 + threadIdx.x], __float_as_int(r));
+    }
+    __syncthreads();
+  }
+  ring.drain(k, a.status);
+}
+
+constexpr int kVStages = 2;
+
+__global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
+    const __grid_constant__ CUtensorMap tmV, QuantVArgs a) {
+  constexpr int kPitchWords = 33;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tileT[128 * kPitchWords];
+  __shared__ float sv[128], sinv[128];
+  __shared__ int abort_flag;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  BlockRing<kVStages> ring;
+  ring.init(base, &abort_flag);
+  const int64_t Np = pad128(a.N), nb = Np / 128, total = a.B * a.H * nb;
+  const int cg = threadIdx.x & 15;
+  const int tg = threadIdx.x >> 4;
+  for (int k = 0; k < kVStages - 1; ++k) ring.load(&tmV, k, total, a.H, nb);
+  int64_t k = 0;
+  for (;; ++k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (i >= total) break;
+    ring.load(&tmV, k + kVStages - 1, total, a.H, nb);
+    const BlockCoord c = block_coord(i, a.H, nb);
+    const int64_t bh = c.b * a.H + c.h;
+    if (threadIdx.x < 128) {
+      const float mx = __int_as_float(a.amax[bh * 128 + threadIdx.x]);
+      const float s = __fdiv_rn(mx, 448.0f);
+      sv[threadIdx.x] = s;
+      sinv[threadIdx.x] = s > 0.0f ? __frcp_rn(s) : 0.0f;
+      if (c.blk == 0) a.scale[bh * 128 + threadIdx.x] = s;
+    }
+    if (!ring.wait(k, &abort_flag, a.status)) break;  // (also orders sv/sinv)
+    const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
+    const uint8_t* tile = ring.stage(k);
+    float s8[8], inv8[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      s8[q] = sv[cg * 8 + q];
+      inv8[q] = sinv[cg * 8 + q];
+    }
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      const int t0 = half * 64 + tg * 4;
+      float f[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint4 raw = *reinterpret_cast<const uint4*>(tile + (t0 + u) * 256 + cg * 16);
+        if (c.blk * 128 + t0 + u >= nv) raw = make_uint4(0, 0, 0, 0);
+        unpack8(raw, f[u]);
+      }
+      uint32_t w[8];
+      uint32_t redo = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        bool e0 = false, e1 = false;
+        const uint32_t lo = e4m3x2_fast(f[0][q], f[1][q], inv8[q], e0);
+        const uint32_t hi = e4m3x2_fast(f[2][q], f[3][q], inv8[q], e1);
+        w[q] = s8[q] > 0.0f ? (lo | (hi << 16)) : 0u;
+        redo |= static_cast<uint32_t>(s8[q] > 0.0f && (e0 || e1 || !(inv8[q] < INFINITY))) << q;
+      }
+      if (redo) {  // rare: pairs near an E4M3 rounding boundary
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if ((redo >> q) & 1)
+            w[q] = e4m3x2(__fdiv_rn(f[0][q], s8[q]), __fdiv_rn(f[1][q], s8[q])) |
+                   (e4m3x2(__fdiv_rn(f[2][q], s8[q]), __fdiv_rn(f[3][q], s8[q])) << 16);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tileT[(cg * 8 + q) * kPitchWords + t0 / 4] = w[q];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int wi = threadIdx.x + 256 * j;
+      const int d = wi >> 5, tw = wi & 31;
+      reinterpret_cast<uint32_t*>(a.out + (bh * 128 + d) * Np + c.blk * 128)[tw] =
+          tileT[d * kPitchWords + tw];
+    }
+    __syncthreads();  // stage, tileT and sv free again
+  }
+  ring.drain(k, a.status);
+}
+
 }  // namespace
 
+namespace {
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      return 152;
+  }
+  return n;
+}
+
+// 4-D map of a BF16 [B][N][H][128] tensor with element strides (sb, sn, sh):
+// one box = 128 tokens x 128 channels of one (b, h).
+bool bnhd_map(CUtensorMap* m, const uint16_t* x, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+              int64_t N, int64_t H) {
+  if (sb <= 0 || sn <= 0 || sh <= 0) return false;
+  const uint64_t dims[4] = {128, static_cast<uint64_t>(H), static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(sh) * 2, static_cast<uint64_t>(sn) * 2,
+                               static_cast<uint64_t>(sb) * 2};
+  const uint32_t box[4] = {128, 1, 128, 1};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box, false);
+}
+
+unsigned persistent_grid(int64_t blocks) {
+  const int64_t g = 2 * static_cast<int64_t>(num_sms());
+  return static_cast<unsigned>(blocks < g ? blocks : g);
+}
+
+template <class K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+// The TMA-fed persistent kernels serve every input a tensor map can describe
+// (positive strides); the direct-load kernels (grid with the head index
+// fastest, so concurrent CTAs read contiguous token rows) serve the rest.
 cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(pad128(a.N) / 128), static_cast<unsigned>(a.H),
+  CUtensorMap m;
+  if (bnhd_map(&m, a.x, a.sb, a.sn, a.sh, a.B, a.N, a.H)) {
+    const int smem = kQStages * kBlockBytes + kQStages * 8 + 128;
+    cudaError_t e = set_smem(quantize_qk_int8_tma_kernel, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = a.B * a.H * (pad128(a.N) / 128);
+    quantize_qk_int8_tma_kernel<<<persistent_grid(blocks), 256, smem, s>>>(m, a);
+    return cudaGetLastError();
+  }
+  dim3 grid(static_cast<unsigned>(a.H), static_cast<unsigned>(pad128(a.N) / 128),
             static_cast<unsigned>(a.B));
   quantize_qk_int8_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(pad128(a.N) / 64), static_cast<unsigned>(a.H),
+  dim3 grid(static_cast<unsigned>(a.H), static_cast<unsigned>(pad128(a.N) / 64),
             static_cast<unsigned>(a.B));
   quantize_qk_mxfp4_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s) {
-  dim3 g1(static_cast<unsigned>(v_partial_chunks(a.N)), static_cast<unsigned>(a.H),
-          static_cast<unsigned>(a.B));
-  v_amax_partial_kernel<<<g1, 256, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaMemsetAsync(a.amax, 0, static_cast<size_t>(v_workspace_bytes(a.B, a.H)), s);
   if (e != cudaSuccess) return e;
-  dim3 g2(static_cast<unsigned>(pad128(a.N) / 128), static_cast<unsigned>(a.H),
-          static_cast<unsigned>(a.B));
-  v_quantize_kernel<<<g2, 256, 0, s>>>(a);
+  CUtensorMap m;
+  if (bnhd_map(&m, a.v, a.sb, a.sn, a.sh, a.B, a.N, a.H)) {
+    const int64_t blocks = a.B * a.H * (pad128(a.N) / 128);
+    const int smem1 = kQStages * kBlockBytes + kQStages * 8 + 128;
+    const int smem2 = kVStages * kBlockBytes + kVStages * 8 + 128;
+    if ((e = set_smem(v_amax_tma_kernel, smem1)) != cudaSuccess) return e;
+    if ((e = set_smem(v_quantize_tma_kernel, smem2)) != cudaSuccess) return e;
+    v_amax_tma_kernel<<<persistent_grid(blocks), 256, smem1, s>>>(m, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    v_quantize_tma_kernel<<<persistent_grid(blocks), 256, smem2, s>>>(m, a);
+    return cudaGetLastError();
+  }
+  dim3 grid(static_cast<unsigned>(a.H), static_cast<unsigned>(pad128(a.N) / 128),
+            static_cast<unsigned>(a.B));
+  v_amax_kernel<<<grid, 256, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  v_quantize_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,7 @@ constexpr int64_t kMaxGridYZ = 65535;
 sage_status_t check_shape(int64_t B, int64_t N, int64_t H, int64_t D) {
   if (D != kHeadDim) return SAGE_ERR_UNSUPPORTED;
   if (B < 1 || N < 1 || H < 1 || B > kMaxGridYZ || H > kMaxGridYZ) return SAGE_ERR_INVALID_ARG;
+  if (pad128(N) / 64 > kMaxGridYZ) return SAGE_ERR_INVALID_ARG;  // token blocks index grid.y
   if (B * H * pad128(N) > (static_cast<int64_t>(1) << 31) - 128) return SAGE_ERR_INVALID_ARG;
   return SAGE_OK;
 }
@@ -97,7 +98,7 @@ size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int
       return 0;
     case 1:
       if (check_shape(B, Nk, H, D) != SAGE_OK) return 0;
-      return static_cast<size_t>(B * H * v_partial_chunks(Nk) * D * 4);
+      return static_cast<size_t>(v_workspace_bytes(B, H));
     case 2: {
       if (check_shape(B, Nq, H, D) != SAGE_OK || check_shape(B, Nk, H, D) != SAGE_OK) return 0;
       const int64_t s = resolve_splits(num_splits, B, H, Nq, Nk);
@@ -140,7 +141,7 @@ sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64
   int* status = nullptr;
   if ((st = device_state(&status)) != SAGE_OK) return st;
   QuantVArgs a{static_cast<const uint16_t*>(v), vs.b, vs.n, vs.h, B, N, H, lens,
-               static_cast<uint8_t*>(v_q), v_scale, static_cast<float*>(workspace), status};
+               static_cast<uint8_t*>(v_q), v_scale, static_cast<int*>(workspace), status};
   return from_cuda(launch_quantize_v(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -85,6 +85,32 @@ def test_quantize_mxfp4_bitexact(N, lens):
     assert_qk_equal(1, xq, xs, rq, rs)
 
 
+def test_quantize_rounding_ties_bitexact():
+    """Codes whose quotient x / s sits exactly on a rounding boundary (INT8:
+    half-integers at s = 1; E4M3: midpoints between representable values at
+    s = 1) are rounded to even exactly like the oracle."""
+    N, H = 256, 2
+    x = torch.zeros((1, N, H, 128), dtype=torch.float32)
+    halves = torch.arange(-127, 127, dtype=torch.float32) + 0.5           # -126.5 .. 126.5
+    x[0, :, 0, :] = halves[torch.randint(0, len(halves), (N, 128), generator=torch.Generator().manual_seed(7))]
+    x[0, 0, 0, 0] = 127.0                                                  # block absmax 127 -> s = 1
+    x[0, 128, 0, 0] = -127.0
+    e4 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    vals = torch.unique(e4[torch.isfinite(e4) & (e4 > 0)])
+    mids = (vals[:-1] + vals[1:]) / 2                                      # E4M3 midpoints
+    x[0, :, 1, :] = mids[torch.randint(0, len(mids), (N, 128), generator=torch.Generator().manual_seed(8))]
+    x[0, 0, 1, :] = 448.0                                                  # channel absmax 448 -> s = 1
+    xb = x.to(torch.bfloat16)
+    assert torch.equal(xb.float(), x)  # every half-integer <= 126.5 and every E4M3 midpoint is exact in BF16
+    xc = xb.cuda()
+    q, qs = binding.sage_quantize_qk(xc, 0)
+    rq, rs = oracle.quantize_int8(bf16_bits(xb))
+    assert_qk_equal(0, q, qs, rq, rs)
+    vq, vs = binding.sage_quantize_v(xc)
+    rv, rvs = oracle.quantize_v_fp8(bf16_bits(xb))
+    assert_v_equal(vq, vs, rv, rvs)
+
+
 def test_quantize_strided_packed_qkv():
     """A packed [B, N, 3, H, D] QKV buffer quantizes like contiguous tensors."""
     w, q, k, v = _small(1, 2, 300, 300, seed=5)

@@ -42,7 +42,7 @@ def test_quantized_bytes():
 
 def test_workspace_bytes():
     assert binding.sage_workspace_bytes(0, 0, 1, 2, 256, 256) == 0
-    assert binding.sage_workspace_bytes(1, 0, 1, 2, 1000, 1000) == 1 * 2 * 2 * 128 * 4
+    assert binding.sage_workspace_bytes(1, 0, 1, 2, 1000, 1000) == 1 * 2 * 128 * 4  # channel maxima
     # forced splits: [splits][B][H][Nq][D] partial O + [splits][B][H][Nq] LSE, FP32
     assert binding.sage_workspace_bytes(2, 0, 1, 2, 256, 1024, 128, 3) == 3 * 2 * 256 * 129 * 4
     assert binding.sage_workspace_bytes(2, 0, 1, 2, 256, 1024, 128, 1) == 0

@@ -62,7 +62,7 @@ def test_noalloc_rejects_oversize(lib):
     v = torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device="cuda")
     f = lib.library().sage_quantize_v_noalloc
     f.restype = ctypes.c_int
-    # B * H * ceil(N / 512) * 128 floats beyond the 8 MiB array: rejected before any launch
-    st = f(ctypes.c_void_p(v.data_ptr()), lib.Strides(0, 0, 0), 1, 1 << 20, 40, 128, None,
+    # B * H * 128 words beyond the 8 MiB array (B * H > 16384): rejected before any launch
+    st = f(ctypes.c_void_p(v.data_ptr()), lib.Strides(0, 0, 0), 2, 128, 8200, 128, None,
            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(v.data_ptr()), None)
     assert st == -3  # SAGE_ERR_WORKSPACE
