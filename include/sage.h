@@ -160,6 +160,10 @@ typedef struct {
  * entrypoint", Motivation; "[None][feat] Add VisualGen FA4 autotuning",
  * first paragraph):
  *   t_ij  = S_ij * s_q * s_k * softmax_scale * log2(e)   (S exact integer)
+ *           for SAGE_FMT_QK_INT8_V_FP8; for SAGE_FMT_QK_MXFP4_V_FP8
+ *           t_ij  = (sum_d q_id 2^eq k_jd 2^ek) * softmax_scale * log2(e),
+ *           the E8M0 block scales eq, ek of each 32 channels applied inside
+ *           the sum ("new MHA v4 entrypoint ...", Technical Details)
  *   M_i   = ceil(max_j t_ij), raised tile by tile; O and l are rescaled by an
  *           exact power of two only when it grows (conditional rescaling)
  *   p_ij  = 2^(t_ij - M_i),  l_i = sum_j p_ij,  P8_ij = E4M3(p_ij * 2^8)

@@ -48,32 +48,65 @@ constexpr float kLn2 = 0.693147180559945309f;
 // row maximum).
 constexpr float kHeadroom = 2.0f;
 
-template <int NQT, int STAGES>
+// Operand format of Q and K (V is FP8 E4M3 in both).
+template <int FMT>
+struct QKFormat;
+// INT8 codes held as FP16: a 128-row tile is 32 KB, two 64-channel halves in
+// the 128-byte swizzled layout. S by kind::f16, one softmax step per 128 keys.
+template <>
+struct QKFormat<0> {
+  static constexpr int kTileBytes = 32768;
+  static constexpr int kSfBytes = 0;
+  static constexpr int kStep = 128;  // keys per softmax step
+};
+// MXFP4: rows of 64 bytes of packed E2M1 (64-byte swizzle), 8 KB per 128 rows,
+// plus 512 bytes of E8M0 scales per 128 rows staged for the copy to TMEM. S by
+// block-scaled kind::mxf4 MMAs in steps of 64 keys: next to two 128-column O
+// accumulators and the scale factors, two 128-column S tiles would not fit in
+// the 512 TMEM columns.
+template <>
+struct QKFormat<1> {
+  static constexpr int kTileBytes = 8192;
+  static constexpr int kSfBytes = 512;
+  static constexpr int kStep = 64;
+};
+
+template <int FMT, int NQT, int STAGES>
 struct SmemLayout {
-  static constexpr int kQ = 0;                          // NQT x 32 KB (FP16 128x128)
-  static constexpr int kK = kQ + NQT * 32768;           // STAGES x 32 KB
-  static constexpr int kV = kK + STAGES * 32768;        // STAGES x 16 KB (FP8 V^T 128x128)
-  static constexpr int kP = kV + STAGES * 16384;        // NQT x 2 x 16 KB (FP8 P, double buffer)
-  static constexpr int kBar = kP + NQT * 2 * 16384;
+  using F = QKFormat<FMT>;
+  static constexpr int kPSlots = 2 * (128 / F::kStep);  // P slots per query tile
+  static constexpr int kQ = 0;                             // NQT Q tiles
+  static constexpr int kK = kQ + NQT * F::kTileBytes;      // STAGES K tiles
+  static constexpr int kV = kK + STAGES * F::kTileBytes;   // STAGES x 16 KB (FP8 V^T 128x128)
+  static constexpr int kP = kV + STAGES * 16384;           // NQT x 2 x 16 KB (FP8 P, double buffer)
+  static constexpr int kSf = kP + NQT * 2 * 16384;         // (NQT + STAGES) scale blocks
+  static constexpr int kBar = kSf + (NQT + STAGES) * F::kSfBytes;
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
-  //           s_full[T], s_free[T], p_full[T][2], o_done[T][2], mma_final
-  static constexpr int kNumBars = 1 + 4 * STAGES + 6 * NQT + 1;
+  //           s_full[T], s_free[T], p_full[T][kPSlots], o_done[T][kPSlots], mma_final
+  static constexpr int kNumBars = 1 + 4 * STAGES + NQT * (2 + 2 * kPSlots) + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem slot, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynamic = kBytes + 1024;        // + alignment slack
 };
 
+// TMEM columns of query tile t: S (kStep FP32 columns) and O (128), and for
+// MXFP4 the scale factors (4 columns per 128 rows: Q per tile, K in two slots
+// that alternate between K tiles).
+template <int FMT, int NQT>
+struct TmemLayout {
+  static constexpr uint32_t kCols = NQT == 1 ? 256 : 512;
+  __host__ __device__ static constexpr uint32_t s(int t) { return FMT == 0 ? t * 256 : NQT * 128 + t * 64; }
+  __host__ __device__ static constexpr uint32_t o(int t) { return FMT == 0 ? t * 256 + 128 : t * 128; }
+  __host__ __device__ static constexpr uint32_t sfq(int t) { return NQT * 192 + t * 4; }
+  __host__ __device__ static constexpr uint32_t sfk(int slot) { return NQT * 196 + slot * 4; }
+};
+static_assert(TmemLayout<1, 2>::sfk(1) + 4 <= TmemLayout<1, 2>::kCols, "TMEM budget");
+static_assert(TmemLayout<1, 1>::sfk(1) + 4 <= TmemLayout<1, 1>::kCols, "TMEM budget");
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Two E4M3 codes: `lo` in bits 7..0, `hi` in bits 15..8.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
 }
 
 // Four E4M3 codes packed in a word, element i in bits 8i+7 .. 8i.
@@ -94,17 +127,21 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
-// Maximum of 128 values: eight independent 3-input-max chains, then a tree.
-__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+// Maximum of N (64 or 128) values: eight independent 3-input-max chains,
+// then a tree.
+template <int N>
+__device__ __forceinline__ float row_max(const float (&s)[N]) {
+  static_assert(N % 16 == 0 && N >= 32, "row length");
   float m[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) m[k] = max3f(s[k], s[k + 8], s[k + 16]);
+  constexpr int kTail = 24 + (N - 32) / 16 * 16;  // start of the last 8 values
 #pragma unroll
-  for (int base = 24; base < 120; base += 16)
+  for (int base = 24; base < kTail; base += 16)
 #pragma unroll
     for (int k = 0; k < 8; ++k) m[k] = max3f(m[k], s[base + k], s[base + 8 + k]);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], s[120 + k]);
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], s[kTail + k]);
   return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
@@ -150,17 +187,21 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 template <int NQT>
 constexpr int attn_threads() { return NQT == 1 ? 7 * 32 : 12 * 32; }
 
-template <int NQT, int STAGES>
+template <int FMT, int NQT, int STAGES>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
-    attn_i8f8_kernel(const __grid_constant__ CUtensorMap tmQ,
+    sage_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using L = SmemLayout<NQT, STAGES>;
+  using L = SmemLayout<FMT, NQT, STAGES>;
+  using F = QKFormat<FMT>;
+  using TM = TmemLayout<FMT, NQT>;
+  constexpr int kStep = F::kStep;
+  constexpr int kSteps = 128 / kStep;      // softmax steps per 128-key tile
+  constexpr int kPSlots = L::kPSlots;      // P slots per query tile (2 buffers x kSteps)
   constexpr int kSoftmaxWarps = NQT * 4;
   constexpr int kTmaWarp = kSoftmaxWarps;       // Q and K loads
   constexpr int kMmaWarp = kSoftmaxWarps + 1;
   constexpr int kTmaVWarp = kSoftmaxWarps + 2;  // V loads
-  constexpr uint32_t kTmemCols = NQT == 1 ? 256 : 512;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -169,6 +210,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   uint8_t* sK = smem + L::kK;
   uint8_t* sV = smem + L::kV;
   uint8_t* sP = smem + L::kP;
+  uint8_t* sSf = smem + L::kSf;  // MXFP4 scales: NQT query tiles, then STAGES K tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
@@ -178,11 +220,11 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   uint64_t* s_full = v_empty + STAGES;
   uint64_t* s_free = s_full + NQT;
   uint64_t* p_full = s_free + NQT;
-  // p_full[t * 2 + buffer]: all 128 rows of that P buffer written. One per
-  // buffer: a fast warp may finish tile j+1 before a slow warp of its
-  // warpgroup has arrived for tile j, so the two must not share a barrier.
-  uint64_t* o_done = p_full + 2 * NQT;  // [t * 2 + buffer]: P V of that P buffer done
-  uint64_t* mma_final = o_done + 2 * NQT;
+  // p_full[t * kPSlots + slot]: all 128 rows of that P slot written. One per
+  // slot: a fast warp may finish step u+1 before a slow warp of its
+  // warpgroup has arrived for step u, so the two must not share a barrier.
+  uint64_t* o_done = p_full + kPSlots * NQT;  // [t * kPSlots + slot]: P V of that slot done
+  uint64_t* mma_final = o_done + kPSlots * NQT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -212,6 +254,10 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   const int64_t j0 = static_cast<int64_t>(split) * per_split;
   const int64_t j1 = j0 + per_split < nkv ? j0 + per_split : nkv;
   const int64_t niter = j1 > j0 ? j1 - j0 : 0;
+  // Softmax steps; a last key tile with at most 64 valid keys needs only its
+  // first 64-key step.
+  int64_t nsteps = niter * kSteps;
+  if (kSteps == 2 && niter > 0 && j1 == nkv && nk - (nkv - 1) * 128 <= 64) nsteps -= 1;
 
   if (niter == 0) {
     // No keys for this (batch, split): empty softmax, O = 0, LSE = -inf.
@@ -245,17 +291,17 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     for (int t = 0; t < NQT; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&s_free[t], 128);
-      mbar_init(&p_full[2 * t], 128);
-      mbar_init(&p_full[2 * t + 1], 128);
-      mbar_init(&o_done[2 * t], 1);
-      mbar_init(&o_done[2 * t + 1], 1);
+      for (int q = 0; q < kPSlots; ++q) {
+        mbar_init(&p_full[t * kPSlots + q], 128);
+        mbar_init(&o_done[t * kPSlots + q], 1);
+      }
     }
     mbar_init(mma_final, 1);
     *abort = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, TM::kCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -274,30 +320,73 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   // descriptors live in uniform registers) and one elected lane issues.
   if (warp == kTmaWarp) {
     // ================================================================ TMA producer (Q, K)
+    if constexpr (FMT == 1) {
+      // E8M0 scales of the query tiles, written in the order the TMEM copy
+      // reads: lane L stores the 16-byte line of rows L, L+32, L+64, L+96.
+      for (int t = 0; t < NQT; ++t) {
+        const int64_t qt = static_cast<int64_t>(blockIdx.x) * NQT + t;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (qt < p.nbq) {
+          const uint32_t* src = p.q_sf + bh * Nq_pad + qt * 128 + lane;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[c] = __ldg(src + 32 * c);
+        }
+        st_shared_v4(smem_u32(sSf + t * 512) + lane * 16, w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
     if (elect_one()) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      mbar_arrive_expect_tx(q_full, NQT * 32768);
+      mbar_arrive_expect_tx(q_full, NQT * F::kTileBytes);
       for (int t = 0; t < NQT; ++t) {
         const int y = static_cast<int>(bh * Nq_pad + (static_cast<int64_t>(blockIdx.x) * NQT + t) * 128);
-        tma_load_2d(sQ + t * 32768, &tmQ, q_full, 0, y);
-        tma_load_2d(sQ + t * 32768 + 16384, &tmQ, q_full, 64, y);
+        if constexpr (FMT == 0) {
+          tma_load_2d(sQ + t * 32768, &tmQ, q_full, 0, y);
+          tma_load_2d(sQ + t * 32768 + 16384, &tmQ, q_full, 64, y);
+        } else {
+          tma_load_2d(sQ + t * 8192, &tmQ, q_full, 0, y);
+        }
       }
     }
     __syncwarp();
+    // MXFP4: the next K tile's scale words, loaded one fill ahead.
+    uint32_t kw[4] = {0u, 0u, 0u, 0u};
+    const uint32_t* ksf = nullptr;
+    if constexpr (FMT == 1) {
+      ksf = p.k_sf + bh * Nk_pad + lane;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) kw[c] = __ldg(ksf + j0 * 128 + 32 * c);
+    }
     int kfills[STAGES];
     for (int s = 0; s < STAGES; ++s) kfills[s] = 0;
     for (int64_t it = 0; it < niter; ++it) {
       const int s = static_cast<int>(it % STAGES);
       const uint32_t u = static_cast<uint32_t>(it / STAGES);
       if (u > 0 && !warp_wait(&k_empty[s], (u - 1) & 1, abort, p.status)) break;
+      if constexpr (FMT == 1) {
+        st_shared_v4(smem_u32(sSf + (NQT + s) * 512) + lane * 16, kw[0], kw[1], kw[2], kw[3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (elect_one()) {
-        mbar_arrive_expect_tx(&k_full[s], 32768);
+        mbar_arrive_expect_tx(&k_full[s], F::kTileBytes);
         const int yk = static_cast<int>(bh * Nk_pad + (j0 + it) * 128);
-        tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
-        tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
+        if constexpr (FMT == 0) {
+          tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
+          tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
+        } else {
+          tma_load_2d(sK + s * 8192, &tmK, &k_full[s], 0, yk);
+        }
       }
       __syncwarp();
+      if constexpr (FMT == 1) {
+        if (it + 1 < niter) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) kw[c] = __ldg(ksf + (j0 + it + 1) * 128 + 32 * c);
+        }
+      }
       ++kfills[s];
     }
     // Drain: no TMA write may still be in flight when the CTA exits.
@@ -326,36 +415,65 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       if (vfills[s] > 0) drain_wait(&v_full[s], static_cast<uint32_t>(vfills[s] - 1) & 1, p.status);
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
-    constexpr uint32_t kIdescS = idesc_f32acc(128, 128);  // f16 x f16 -> f32
+    constexpr uint32_t kIdescS = idesc_f32acc(128, 128);  // f16 x f16 -> f32 (INT8 codes)
     constexpr uint32_t kIdescO = idesc_f32acc(128, 128);  // e4m3 x e4m3 -> f32
     // Descriptor low words of every operand buffer (k slices add a constant).
-    const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ));    // + t * 2048 per Q tile
-    const uint32_t k_lo = sw128_desc_lo(smem_u32(sK));    // + stage * 2048
+    // The 64- and 128-byte swizzled layouts share the low-word encoding.
+    const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ));    // + tile bytes / 16 per Q tile
+    const uint32_t k_lo = sw128_desc_lo(smem_u32(sK));    // + tile bytes / 16 per stage
     const uint32_t p_lo = sw128_desc_lo(smem_u32(sP));    // + (2t + buffer) * 1024
     const uint32_t v_lo = sw128_desc_lo(smem_u32(sV));    // + stage * 1024
     // The elected lane is the same (lowest) lane every time, so the commits
     // track the MMAs that lane issued.
-    auto issue_s = [&](int t, int stage) {
-      const uint32_t d = tbase + t * 256;
-      const uint32_t qa = q_lo + t * 2048, ka = k_lo + stage * 2048;
-      if (elect_one()) {
+    auto issue_s = [&](int t, int64_t v) {
+      const int stage = static_cast<int>((v / kSteps) % STAGES);
+      const uint32_t d = tbase + TM::s(t);
+      if constexpr (FMT == 0) {
+        const uint32_t qa = q_lo + t * 2048, ka = k_lo + stage * 2048;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-          mma_f16_ss_lo(d, qa + off, ka + off, kIdescS, k > 0);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+            mma_f16_ss_lo(d, qa + off, ka + off, kIdescS, k > 0);
+          }
+          mma_commit(&s_full[t]);
         }
-        mma_commit(&s_full[t]);
+      } else {
+        // Keys 64h .. 64h+63 of the stage: B rows at +4096 bytes, their
+        // scales two TMEM columns further (rows 64..127 of the 128-row copy).
+        const int half = static_cast<int>(v % kSteps);
+        const uint32_t qa = q_lo + t * 512, ka = k_lo + stage * 512 + half * 256;
+        const uint32_t sfa = tbase + TM::sfq(t);
+        const uint32_t sfb = tbase + TM::sfk(static_cast<int>((v / kSteps) & 1)) + half * 2;
+        if (elect_one()) {
+          mma_mxf4_ss_lo(d, qa, ka, idesc_mxf4(128, 64, 0), sfa, sfb, 0u);
+          mma_mxf4_ss_lo(d, qa + 2, ka + 2, idesc_mxf4(128, 64, 2), sfa, sfb, 1u);
+          mma_commit(&s_full[t]);
+        }
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int t, int pbuf, int stage, bool acc) {
-      const uint32_t d = tbase + t * 256 + 128;
+    // MXFP4: scales of local K tile i to TMEM slot i & 1. The slot was last
+    // read by the S MMAs of tile i - 2, which completed before the S of the
+    // step before this tile's first step, whose s_free has been waited for.
+    auto copy_k_scales = [&](int64_t i) {
+      if (elect_one())
+        tmem_cp_sf512(tbase + TM::sfk(static_cast<int>(i & 1)),
+                      smem_u32(sSf + (NQT + static_cast<int>(i % STAGES)) * 512));
+      __syncwarp();
+    };
+    auto issue_pv = [&](int t, int slot, int stage, int half, bool acc) {
+      const uint32_t d = tbase + TM::o(t);
+      const int pbuf = slot / kSteps;
       const uint32_t pa = p_lo + (t * 2 + pbuf) * 1024, va = v_lo + stage * 1024;
+      constexpr int kK = kStep / 32;  // K = 32 slices per step
       if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_f8_ss_lo(d, pa + k * 2, va + k * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
-        mma_commit(&o_done[2 * t + pbuf]);
+        for (int k = 0; k < kK; ++k) {
+          const int kk = half * kK + k;
+          mma_f8_ss_lo(d, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&o_done[t * kPSlots + slot]);
       }
       __syncwarp();
     };
@@ -367,40 +485,56 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     if (ok) ok = warp_wait(&k_full[0], 0, abort, p.status);
     tc_fence_after();
     if (ok) {
+      if constexpr (FMT == 1) {
+        if (elect_one())
+          for (int t = 0; t < NQT; ++t) tmem_cp_sf512(tbase + TM::sfq(t), smem_u32(sSf + t * 512));
+        __syncwarp();
+        copy_k_scales(0);
+      }
       for (int t = 0; t < NQT; ++t) issue_s(t, 0);
-      commit(&k_empty[0]);
+      if (kSteps == 1) commit(&k_empty[0]);
     }
-    for (int64_t it = 0; ok && it < niter; ++it) {
-      const int s = static_cast<int>(it % STAGES);
-      const uint32_t u = static_cast<uint32_t>(it / STAGES);
-      const bool has_next = it + 1 < niter;
-      const int sn = static_cast<int>((it + 1) % STAGES);
-      const uint32_t un = static_cast<uint32_t>((it + 1) / STAGES);
-      // Next S tiles first (each needs only its softmax warpgroup to have
-      // read the previous S), then this tile's P V products. V is waited
-      // for only right before the P V MMAs.
-      if (has_next) {
-        if (!(ok = warp_wait(&k_full[sn], un & 1, abort, p.status))) break;
-        tc_fence_after();
-        for (int t = 0; t < NQT && ok; ++t) {
-          if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
+    for (int64_t u = 0; ok && u < nsteps; ++u) {
+      // Next S first (each needs only its softmax warpgroup to have read the
+      // previous S), then this step's P V products. V is waited for only
+      // right before the P V MMAs.
+      const int64_t v = u + 1;
+      if (v < nsteps) {
+        const int64_t iv = v / kSteps;
+        const int sv = static_cast<int>(iv % STAGES);
+        const bool first_half = (v % kSteps) == 0;
+        if (first_half) {
+          if (!(ok = warp_wait(&k_full[sv], static_cast<uint32_t>(iv / STAGES) & 1, abort, p.status))) break;
           tc_fence_after();
-          issue_s(t, sn);
+        }
+        for (int t = 0; t < NQT && ok; ++t) {
+          if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(u) & 1, abort, p.status))) break;
+          tc_fence_after();
+          if constexpr (FMT == 1) {
+            if (first_half && t == 0) copy_k_scales(iv);
+          }
+          issue_s(t, v);
         }
         if (!ok) break;
-        commit(&k_empty[sn]);
+        if ((v % kSteps) == kSteps - 1) commit(&k_empty[sv]);
       }
-      if (!(ok = warp_wait(&v_full[s], u & 1, abort, p.status))) break;
-      tc_fence_after();
+      const int64_t iu = u / kSteps;
+      const int su = static_cast<int>(iu % STAGES);
+      const int hu = static_cast<int>(u % kSteps);
+      const int slot = static_cast<int>(u % kPSlots);
+      if (hu == 0) {
+        if (!(ok = warp_wait(&v_full[su], static_cast<uint32_t>(iu / STAGES) & 1, abort, p.status))) break;
+        tc_fence_after();
+      }
       for (int t = 0; t < NQT && ok; ++t) {
-        if (!(ok = warp_wait(&p_full[2 * t + (it & 1)], static_cast<uint32_t>(it >> 1) & 1, abort,
-                             p.status)))
+        if (!(ok = warp_wait(&p_full[t * kPSlots + slot], static_cast<uint32_t>(u / kPSlots) & 1,
+                             abort, p.status)))
           break;
         tc_fence_after();
-        issue_pv(t, static_cast<int>(it & 1), s, it > 0);
+        issue_pv(t, slot, su, hu, u > 0);
       }
       if (!ok) break;
-      commit(&v_empty[s]);
+      if (hu == kSteps - 1) commit(&v_empty[su]);
     }
     // All MMAs issued by the elected lane must finish before TMEM is freed.
     commit(mma_final);
@@ -412,54 +546,70 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     const int t = warp / 4;
     const int r = static_cast<int>(threadIdx.x & 127);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tbase + lane_base + t * 256;
-    const uint32_t tO = tS + 128;
+    const uint32_t tS = tbase + lane_base + TM::s(t);
+    const uint32_t tO = tbase + lane_base + TM::o(t);
     const int64_t qt = static_cast<int64_t>(blockIdx.x) * NQT + t;
     const int64_t row = qt * 128 + r;
-    const float sq = qt < p.nbq ? __ldg(&p.q_scale[bh * p.nbq + qt]) : 0.0f;
-    const float alpha_q = sq * p.scale_log2;
-    const float* kscale = p.k_scale + bh * p.nbk;
+    // INT8: logit multiplier s_q s_k softmax_scale log2(e) per K tile. MXFP4:
+    // the block scales are inside S already, the multiplier is constant.
+    float alpha_q = p.scale_log2;
+    const float* kscale = nullptr;
+    float sk_next = 1.0f;  // K block scale, loaded one tile ahead
+    if constexpr (FMT == 0) {
+      const float sq = qt < p.nbq ? __ldg(&p.q_scale[bh * p.nbq + qt]) : 0.0f;
+      alpha_q = sq * p.scale_log2;
+      kscale = p.k_scale + bh * p.nbk;
+      sk_next = __ldg(&kscale[j0]);
+    }
     float m = -INFINITY;  // running integer row maximum (log2 units)
     float l = 0.0f;       // running row sum of 2^(t - m + 8)
     bool ok = true;
     const uint32_t p_row0 = smem_u32(sP + (t * 2) * 16384) + r * 128;  // P buffer 0; buffer 1 at +16 KB
     const uint32_t swz = static_cast<uint32_t>(r & 7);
 
-    float sk_next = __ldg(&kscale[j0]);  // K block scale, loaded one tile ahead
-    for (int64_t it = 0; it < niter; ++it) {
-      const int64_t j = j0 + it;
-      const float sk = sk_next;
-      if (it + 1 < niter) sk_next = __ldg(&kscale[j + 1]);
-      if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(it) & 1, abort, p.status))) break;
+    float sk = 1.0f;
+    for (int64_t u = 0; u < nsteps; ++u) {
+      const int64_t iu = u / kSteps;
+      const int hu = static_cast<int>(u % kSteps);
+      const int64_t j = j0 + iu;
+      if constexpr (FMT == 0) {
+        sk = sk_next;
+        if (iu + 1 < niter) sk_next = __ldg(&kscale[j + 1]);
+      }
+      if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(u) & 1, abort, p.status))) break;
       tc_fence_after();
-      float s[128];
+      float s[kStep];
       {
-        uint32_t v[128];
-        tmem_ld128(tS, v);
+        uint32_t v[kStep];
+        if constexpr (kStep == 128)
+          tmem_ld128(tS, v);
+        else
+          tmem_ld64(tS, v);
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(v[i]);
+        for (int i = 0; i < kStep; ++i) s[i] = __uint_as_float(v[i]);
       }
       tc_fence_before();
       mbar_arrive(&s_free[t]);
 
       const float alpha = alpha_q * sk;
-      const int nvalid = static_cast<int>(nk - j * 128 < 128 ? nk - j * 128 : 128);
-      if (nvalid < 128) {
+      const int64_t key0 = j * 128 + hu * kStep;
+      const int nvalid = static_cast<int>(nk - key0 < kStep ? nk - key0 : kStep);
+      if (nvalid < kStep) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < kStep; ++c)
           if (c >= nvalid) s[c] = -INFINITY;
       }
-      const float mx = row_max128(s);
+      const float mx = row_max<kStep>(s);
       const float cand = ceilf(mx * alpha);
-      // First tile: set the reference. Later: raise it only past the headroom.
-      const float m_new = (it == 0) ? cand : (cand > m + kHeadroom ? cand : m);
-      const bool rescale = (it > 0) && (m_new > m);
-      bool o_prev_done = false;  // P V of the previous tile known complete
+      // First step: set the reference. Later: raise it only past the headroom.
+      const float m_new = (u == 0) ? cand : (cand > m + kHeadroom ? cand : m);
+      const bool rescale = (u > 0) && (m_new > m);
+      bool o_prev_done = false;  // P V of the previous step known complete
       if (__any_sync(0xffffffffu, rescale)) {
-        // Conditional rescale: O_t must hold P V up to the previous tile.
-        const int pb = static_cast<int>((it - 1) & 1);
-        if (!(ok = warp_wait(&o_done[2 * t + pb], static_cast<uint32_t>((it - 1) >> 1) & 1, abort,
-                             p.status)))
+        // Conditional rescale: O_t must hold P V up to the previous step.
+        const int ps = static_cast<int>((u - 1) % kPSlots);
+        if (!(ok = warp_wait(&o_done[t * kPSlots + ps], static_cast<uint32_t>((u - 1) / kPSlots) & 1,
+                             abort, p.status)))
           break;
         o_prev_done = true;
         tc_fence_after();
@@ -477,13 +627,14 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       }
       m = m_new;
       const float bias = 8.0f - kHeadroom - m;
-      const uint32_t p_row = p_row0 + static_cast<uint32_t>(it & 1) * 16384;
+      const int slot = static_cast<int>(u % kPSlots);
+      const uint32_t p_row = p_row0 + static_cast<uint32_t>(slot / kSteps) * 16384;
 
-      // P buffer it%2 is free once P V of tile it-2 (same buffer) is complete.
-      if (it >= 2 && !o_prev_done) {
-        const int pb = static_cast<int>(it & 1);
-        if (!(ok = warp_wait(&o_done[2 * t + pb], static_cast<uint32_t>((it - 2) >> 1) & 1, abort,
-                             p.status)))
+      // The P slot is free once P V of step u - kPSlots (same slot) is
+      // complete; P V of step u - 1 being complete implies it (in order).
+      if (u >= kPSlots && !o_prev_done) {
+        if (!(ok = warp_wait(&o_done[t * kPSlots + slot],
+                             static_cast<uint32_t>((u - kPSlots) / kPSlots) & 1, abort, p.status)))
           break;
       }
       // x = S * alpha + (8 - m) two at a time (packed FP32x2 FMA), p8 = 2^x,
@@ -491,14 +642,14 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       const float2 alpha2 = make_float2(alpha, alpha), bias2 = make_float2(bias, bias);
       float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int ch = 0; ch < kStep / 16; ++ch) {
         uint32_t pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int c = ch * 16 + q * 4;
           float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), alpha2, bias2);
           float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), alpha2, bias2);
-          if (nvalid < 128) {  // masked keys contribute exactly 0
+          if (nvalid < kStep) {  // masked keys contribute exactly 0
             x01.x = c + 0 < nvalid ? x01.x : -INFINITY;
             x01.y = c + 1 < nvalid ? x01.y : -INFINITY;
             x23.x = c + 2 < nvalid ? x23.x : -INFINITY;
@@ -510,17 +661,19 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
           acc1 = __fadd2_rn(acc1, e23);
           pk[q] = e4m3x4(e01.x, e01.y, e23.x, e23.y);
         }
-        st_shared_v4(p_row + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+        // 16-byte chunk of this step's keys within the 128-key P row.
+        const uint32_t chunk = static_cast<uint32_t>(hu * (kStep / 16) + ch);
+        st_shared_v4(p_row + ((chunk ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
       }
       l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       fence_proxy_async_smem();
-      mbar_arrive(&p_full[2 * t + (it & 1)]);
+      mbar_arrive(&p_full[t * kPSlots + slot]);
     }
 
     // ---- epilogue
     if (ok)
-      ok = warp_wait(&o_done[2 * t + static_cast<int>((niter - 1) & 1)],
-                     static_cast<uint32_t>((niter - 1) >> 1) & 1, abort, p.status);
+      ok = warp_wait(&o_done[t * kPSlots + static_cast<int>((nsteps - 1) % kPSlots)],
+                     static_cast<uint32_t>((nsteps - 1) / kPSlots) & 1, abort, p.status);
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
@@ -576,7 +729,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tbase, kTmemCols);
+    tmem_dealloc(tbase, TM::kCols);
   }
 }
 
@@ -618,28 +771,33 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const AttnParams p) {
 
 // ------------------------------------------------------------------ host side
 bool make_map_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize,
-                 uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+                 uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle) {
   const uint64_t dims[2] = {inner, rows};
   const uint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
   const uint32_t box[2] = {box_inner, box_rows};
-  return encode_tiled(m, dt, 2, ptr, dims, strides, box, true);
+  return encode_tiled(m, dt, 2, ptr, dims, strides, box, swizzle);
 }
 
-template <int NQT, int STAGES>
+template <int FMT, int NQT, int STAGES>
 cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const AttnParams& p, cudaStream_t stream) {
-  using L = SmemLayout<NQT, STAGES>;
+  using L = SmemLayout<FMT, NQT, STAGES>;
   static_assert(L::kDynamic <= 232448, "shared memory budget");
-  auto kern = attn_i8f8_kernel<NQT, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
+  constexpr auto kern = sage_attn_kernel<FMT, NQT, STAGES>;
+  cudaError_t e = once_per_device<kern>([]() {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
+    if (r != cudaSuccess) return r;
+    if constexpr (NQT == 2) {
+      // setmaxnreg can only hand out the registers the CTA was launched with.
+      cudaFuncAttributes fa;
+      if ((r = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return r;
+      if (static_cast<long>(fa.numRegs) * attn_threads<NQT>() < 128L * (232 + 232 + 40))
+        return cudaErrorInvalidConfiguration;
+    }
+    return cudaSuccess;
+  });
   if (e != cudaSuccess) return e;
-  if constexpr (NQT == 2) {
-    // setmaxnreg can only hand out the registers the CTA was launched with.
-    cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    if (static_cast<long>(fa.numRegs) * attn_threads<NQT>() < 128L * (232 + 232 + 40))
-      return cudaErrorInvalidConfiguration;
-  }
   dim3 grid(static_cast<unsigned>((p.nbq + NQT - 1) / NQT), static_cast<unsigned>(p.H),
             static_cast<unsigned>(p.B * p.num_splits));
   kern<<<grid, attn_threads<NQT>(), L::kDynamic, stream>>>(mq, mk, mv, p);
@@ -662,21 +820,34 @@ int attn_auto_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
   return s < 1 ? 1 : static_cast<int>(s);
 }
 
-cudaError_t launch_attention_i8f8(const AttnLaunch& a, cudaStream_t stream) {
+cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   const int64_t Nq_pad = pad128(a.p.Nq), Nk_pad = pad128(a.p.Nk);
+  const uint64_t q_rows = static_cast<uint64_t>(a.p.B * a.p.H * Nq_pad);
+  const uint64_t k_rows = static_cast<uint64_t>(a.p.B * a.p.H * Nk_pad);
   CUtensorMap mq, mk, mv;
-  if (!make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128,
-                   static_cast<uint64_t>(a.p.B * a.p.H * Nq_pad), 64, 128) ||
-      !make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128,
-                   static_cast<uint64_t>(a.p.B * a.p.H * Nk_pad), 64, 128) ||
+  bool maps_ok;
+  if (a.fmt == 0)  // FP16-held INT8 codes: 128-byte boxes of 64 channels
+    maps_ok = make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128, q_rows, 64, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128, k_rows, 64, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  else  // packed E2M1: one 64-byte row per token
+    maps_ok = make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, q_rows, 64, 128,
+                          CU_TENSOR_MAP_SWIZZLE_64B) &&
+              make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, k_rows, 64, 128,
+                          CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!maps_ok ||
       !make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(Nk_pad),
-                   static_cast<uint64_t>(a.p.B * a.p.H * 128), 128, 128))
+                   static_cast<uint64_t>(a.p.B * a.p.H * 128), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  const bool two = attn_q_tiles_per_cta(a.p.nbq) == 2;
   cudaError_t e;
-  if (attn_q_tiles_per_cta(a.p.nbq) == 2)
-    e = launch_variant<2, 2>(mq, mk, mv, a.p, stream);
+  if (a.fmt == 0)
+    e = two ? launch_variant<0, 2, 2>(mq, mk, mv, a.p, stream)
+            : launch_variant<0, 1, 3>(mq, mk, mv, a.p, stream);
   else
-    e = launch_variant<1, 3>(mq, mk, mv, a.p, stream);
+    e = two ? launch_variant<1, 2, 4>(mq, mk, mv, a.p, stream)
+            : launch_variant<1, 1, 4>(mq, mk, mv, a.p, stream);
   if (e != cudaSuccess || a.p.num_splits <= 1) return e;
   const int64_t rows = a.p.B * a.p.H * a.p.Nq;
   const int64_t blocks = (rows * 32 + 255) / 256;

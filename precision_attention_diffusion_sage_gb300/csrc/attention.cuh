@@ -8,8 +8,10 @@
 namespace sage {
 
 struct AttnParams {
-  const float* q_scale;  // [B][H][nbq]
-  const float* k_scale;  // [B][H][nbk]
+  const float* q_scale;  // INT8: [B][H][nbq]
+  const float* k_scale;  // INT8: [B][H][nbk]
+  const uint32_t* q_sf;  // MXFP4: E8M0 bytes [B][H][Nq_pad][4], one word per row
+  const uint32_t* k_sf;  // MXFP4: [B][H][Nk_pad][4]
   const float* v_scale;  // [B][H][128]
   const int32_t* k_lens; // nullable [B]
   int64_t B, H, Nq, Nk;
@@ -25,14 +27,15 @@ struct AttnParams {
 };
 
 struct AttnLaunch {
-  const void* q;  // FP16-held INT8 codes [B][H][Nq_pad][128]
-  const void* k;  // [B][H][Nk_pad][128]
+  int fmt;        // 0: INT8 Q/K, 1: MXFP4 Q/K
+  const void* q;  // INT8: FP16-held codes [B][H][Nq_pad][128]; MXFP4: packed E2M1 [B][H][Nq_pad][64]
+  const void* k;  // same layout with Nk_pad
   const void* v;  // FP8 [B][H][128][Nk_pad]
   AttnParams p;
 };
 
 int attn_q_tiles_per_cta(int64_t nbq);
 int attn_auto_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk);
-cudaError_t launch_attention_i8f8(const AttnLaunch& a, cudaStream_t stream);
+cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);
 
 }  // namespace sage

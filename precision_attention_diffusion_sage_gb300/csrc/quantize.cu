@@ -609,16 +609,15 @@ __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
 namespace {
 
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      return 152;
-  }
-  return n;
+  static std::atomic<int> n{0};
+  int v = n.load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    return 152;
+  n.store(v, std::memory_order_relaxed);
+  return v;
 }
 
 // 4-D map of a BF16 [B][N][H][128] tensor with element strides (sb, sn, sh):
@@ -631,7 +630,8 @@ bool bnhd_map(CUtensorMap* m, const uint16_t* x, int64_t sb, int64_t sn, int64_t
   const uint64_t strides[3] = {static_cast<uint64_t>(sh) * 2, static_cast<uint64_t>(sn) * 2,
                                static_cast<uint64_t>(sb) * 2};
   const uint32_t box[4] = {128, 1, 128, 1};
-  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box, false);
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 unsigned persistent_grid(int64_t blocks) {
@@ -639,9 +639,11 @@ unsigned persistent_grid(int64_t blocks) {
   return static_cast<unsigned>(blocks < g ? blocks : g);
 }
 
-template <class K>
-cudaError_t set_smem(K kern, int bytes) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+template <auto Kern>
+cudaError_t set_smem(int bytes) {
+  return once_per_device<Kern>([bytes]() {
+    return cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
 }
 
 }  // namespace
@@ -653,7 +655,7 @@ cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s) {
   CUtensorMap m;
   if (bnhd_map(&m, a.x, a.sb, a.sn, a.sh, a.B, a.N, a.H)) {
     const int smem = kQStages * kBlockBytes + kQStages * 8 + 128;
-    cudaError_t e = set_smem(quantize_qk_int8_tma_kernel, smem);
+    cudaError_t e = set_smem<quantize_qk_int8_tma_kernel>(smem);
     if (e != cudaSuccess) return e;
     const int64_t blocks = a.B * a.H * (pad128(a.N) / 128);
     quantize_qk_int8_tma_kernel<<<persistent_grid(blocks), 256, smem, s>>>(m, a);
@@ -680,8 +682,8 @@ cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s) {
     const int64_t blocks = a.B * a.H * (pad128(a.N) / 128);
     const int smem1 = kQStages * kBlockBytes + kQStages * 8 + 128;
     const int smem2 = kVStages * kBlockBytes + kVStages * 8 + 128;
-    if ((e = set_smem(v_amax_tma_kernel, smem1)) != cudaSuccess) return e;
-    if ((e = set_smem(v_quantize_tma_kernel, smem2)) != cudaSuccess) return e;
+    if ((e = set_smem<v_amax_tma_kernel>(smem1)) != cudaSuccess) return e;
+    if ((e = set_smem<v_quantize_tma_kernel>(smem2)) != cudaSuccess) return e;
     v_amax_tma_kernel<<<persistent_grid(blocks), 256, smem1, s>>>(m, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     v_quantize_tma_kernel<<<persistent_grid(blocks), 256, smem2, s>>>(m, a);

@@ -157,7 +157,6 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   sage_status_t st = check_shape(B, Nq, H, D);
   if (st != SAGE_OK) return st;
   if ((st = check_shape(B, Nk, H, D)) != SAGE_OK) return st;
-  if (fmt != SAGE_FMT_QK_INT8_V_FP8) return SAGE_ERR_UNSUPPORTED;
   if (!q_q || !q_scale || !k_q || !k_scale || !v_q || !v_scale || !o) return SAGE_ERR_INVALID_ARG;
   if (!aligned(q_q, 16) || !aligned(k_q, 16) || !aligned(v_q, 16) || !aligned(o, 16) ||
       !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
@@ -173,13 +172,17 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   int* status = nullptr;
   if ((st = device_state(&status)) != SAGE_OK) return st;
   const float c = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8;
   AttnLaunch a;
+  a.fmt = mx ? 1 : 0;
   a.q = q_q;
   a.k = k_q;
   a.v = v_q;
   AttnParams& p = a.p;
-  p.q_scale = static_cast<const float*>(q_scale);
-  p.k_scale = static_cast<const float*>(k_scale);
+  p.q_scale = mx ? nullptr : static_cast<const float*>(q_scale);
+  p.k_scale = mx ? nullptr : static_cast<const float*>(k_scale);
+  p.q_sf = mx ? static_cast<const uint32_t*>(q_scale) : nullptr;
+  p.k_sf = mx ? static_cast<const uint32_t*>(k_scale) : nullptr;
   p.v_scale = v_scale;
   p.k_lens = k_lens;
   p.B = B;
@@ -198,7 +201,7 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   p.o_part = splits > 1 ? static_cast<float*>(workspace) : nullptr;
   p.lse_part = splits > 1 ? static_cast<float*>(workspace) + splits * B * H * Nq * D : nullptr;
   p.status = status;
-  return from_cuda(launch_attention_i8f8(a, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_attention(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* sage_status_string(sage_status_t st) {

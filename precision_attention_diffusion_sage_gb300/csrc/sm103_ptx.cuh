@@ -209,6 +209,50 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, uint32_t a_fmt
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- block-scaled MXFP4 MMA
+// K-major operand in the 64-byte swizzled layout: rows of 64 bytes (128 packed
+// E2M1 values), 8-row atoms of 512 bytes stacked along M/N. High descriptor
+// word: stride 512, version 1, 64-byte swizzle; low word as for 128-byte
+// swizzle, (address >> 4) | (1 << 16).
+constexpr uint32_t kSw64DescHi = (512u >> 4) | (1u << 14) | (4u << 29);
+
+// Instruction descriptor of kind::mxf4 with E8M0 scales, one per 32 elements
+// (scale_vec::2X: a K = 64 MMA reads two scale bytes per row). `sf_id` picks
+// the byte of each 32-bit scale column where that pair starts (0 or 2), the
+// same for A and B. Operand codes 1 = E2M1; bit 23 selects E8M0 scales.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
+}
+
+// D (+)= (A * 2^sfa) (B * 2^sfb)^T over K = 64, A and B E2M1 in shared memory
+// (64-byte swizzle), the scale factors in tensor memory.
+__device__ __forceinline__ void mma_mxf4_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %4, 0;\n"
+      " mov.b64 a, {%1, %7};\n mov.b64 b, {%2, %7};\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a, b, %3, [%5], [%6], "
+      "p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem),
+      "n"(kSw64DescHi)
+      : "memory");
+}
+
+// Copies 512 bytes of scale factors from shared memory to four TMEM columns
+// of every 32-lane quarter (32 rows of 16 bytes, replicated to the four warp
+// quarters). Source rows are contiguous 16-byte lines: line L holds the four
+// scale bytes of matrix rows L, L + 32, L + 64 and L + 96, so that TMEM lane
+// r, column r / 32 carries row r's scales.
+__device__ __forceinline__ void tmem_cp_sf512(uint32_t taddr, uint32_t saddr) {
+  const uint64_t desc = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+                        (static_cast<uint64_t>(128 >> 4) << 16) |
+                        (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+
 // TMEM address: lane in bits 31..16, column in bits 15..0.
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
   return base + (lane << 16) + col;
@@ -228,6 +272,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Loads 64 consecutive 32-bit columns of this thread's lane (one 32x32b.x64
+// load) and waits for completion.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr)
       : "memory");
 }

@@ -16,7 +16,7 @@ std::once_flag g_encode_once;
 
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* ptr,
                   const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
-                  bool swizzle128) {
+                  CUtensorMapSwizzle swizzle) {
   std::call_once(g_encode_once, []() {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -37,7 +37,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const v
   }
   return g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), d, st, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

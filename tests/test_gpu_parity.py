@@ -255,3 +255,94 @@ def test_full_size_workload(name, heads):
     rows = _sample_rows(w.Nq)
     ro, rl = _oracle_attention(0, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
     assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+
+
+# ------------------------------------------------------------------ MXFP4 Q/K attention
+# Keys are processed in 64-key steps; a last 128-key tile with at most 64 valid
+# keys takes only its first step. The shapes below put the tail on both sides
+# of that line (64, 65, 104, 44 valid keys in the last tile).
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (127, 64), (129, 65), (256, 192), (300, 300),
+                                   (128, 1000), (513, 77), (256, 384)])
+def test_attention_mxfp4_ragged_tails(Nq, Nk):
+    w, q, k, v = _small(1, 2, Nq, Nk, seed=Nq * 5 + Nk)
+    (qq, qs), (kq, ks), _, o, lse = _run_gpu(1, q, k, v)
+    qz, kz, vz = oracle_quantize(1, q, k, v)
+    assert_qk_equal(1, qq, qs, *qz)
+    assert_qk_equal(1, kq, ks, *kz)
+    ro, rl = _oracle_attention(1, qz, kz, vz, Nq, Nk)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_mxfp4_outlier_channels():
+    """Per-channel K offsets spread the 32-channel block exponents of one row
+    over several binades (the tiny workload's structure)."""
+    w, q, k, v = _small(1, 2, 256, 256, seed=50, structure="k_offset_std2")
+    _, _, _, o, lse = _run_gpu(1, q, k, v)
+    qz, kz, vz = oracle_quantize(1, q, k, v)
+    ro, rl = _oracle_attention(1, qz, kz, vz, 256, 256)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_mxfp4_cross_ragged_k_lens():
+    w, q, k, v = _small(2, 2, 300, 512, seed=51)
+    lens = [512, 300]
+    _, _, _, o, lse = _run_gpu(1, q, k, v, k_lens=lens)
+    qz, kz, vz = oracle_quantize(1, q, k, v, k_lens=lens)
+    ro, rl = _oracle_attention(1, qz, kz, vz, 300, 512, k_lens=lens)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_mxfp4_zero_length_batch():
+    w, q, k, v = _small(2, 2, 200, 256, seed=52)
+    lens = [0, 256]
+    _, _, _, o, lse = _run_gpu(1, q, k, v, k_lens=lens)
+    assert torch.all(o[0] == 0)
+    assert torch.all(torch.isneginf(lse[0]))
+    qz, kz, vz = oracle_quantize(1, q, k, v, k_lens=lens)
+    ro, rl = _oracle_attention(1, qz, kz, vz, 200, 256, k_lens=lens)
+    assert_attention_close(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("Nk,splits", [(1000, 1), (1000, 2), (1000, 3), (1000, 7), (960, 3)])
+def test_attention_mxfp4_split_kv(Nk, splits):
+    w, q, k, v = _small(1, 2, 256, Nk, seed=53 + splits)
+    _, _, _, o, lse = _run_gpu(1, q, k, v, num_splits=splits)
+    qz, kz, vz = oracle_quantize(1, q, k, v)
+    ro, rl = _oracle_attention(1, qz, kz, vz, 256, Nk)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_mxfp4_softmax_scale():
+    w, q, k, v = _small(1, 2, 256, 320, seed=54)
+    _, _, _, o, lse = _run_gpu(1, q, k, v, softmax_scale=0.2)
+    qz, kz, vz = oracle_quantize(1, q, k, v)
+    ro, rl = _oracle_attention(1, qz, kz, vz, 256, 320, softmax_scale=0.2)
+    assert_attention_close(o, lse, ro, rl)
+
+
+@pytest.mark.parametrize("name", ["mxfp4_self", "cross_ragged_mxfp4"])
+def test_attention_mxfp4_deterministic(name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    o1, l1 = binding.sage_attention(q, k, v, fmt=1, k_lens=w.k_lens)
+    for _ in range(3):
+        o2, l2 = binding.sage_attention(q, k, v, fmt=1, k_lens=w.k_lens)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+
+
+@pytest.mark.parametrize("name,heads", [("mxfp4_self", [0, 11, 23]), ("cross_ragged_mxfp4", None)])
+def test_full_size_workload_mxfp4(name, heads):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(1, q, k, v, k_lens=w.k_lens)
+    hs = list(range(w.H)) if heads is None else heads
+    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
+    qz, kz, vz = oracle_quantize(1, sub(q), sub(k), sub(v), k_lens=w.k_lens)
+    assert_qk_equal(1, qq[:, hs], qs[:, hs], *qz)
+    assert_qk_equal(1, kq[:, hs], ks[:, hs], *kz)
+    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
+    rows = _sample_rows(w.Nq)
+    ro, rl = _oracle_attention(1, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
+    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
