@@ -41,11 +41,69 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def _roofline_peak(p16: float) -> float:
+# Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
+_FP8_RATIO, _FP4_RATIO = 2.0, 6.0
+
+
+def _roofline_peak(p16: float, fmt: int) -> float:
     """Tensor roofline of the attention: half the flops (Q K^T) on the 16-bit
-    pipe, half (P V) on the FP8 pipe at twice that rate."""
-    p8 = 2.0 * p16
-    return 2.0 / (1.0 / p16 + 1.0 / p8)
+    pipe (INT8 codes held as FP16) or the FP4 pipe (MXFP4), half (P V) on the
+    FP8 pipe; the two halves run back to back, so the rates combine
+    harmonically."""
+    p_qk = p16 * (_FP4_RATIO if fmt == 1 else 1.0)
+    p_pv = p16 * _FP8_RATIO
+    return 2.0 / (1.0 / p_qk + 1.0 / p_pv)
+
+
+def _kernel_sources_sha256() -> str:
+    """Hash of the sources that define the attention kernel, to tell whether
+    committed profiler counters still describe it."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "precision_attention_diffusion_sage_gb300", "csrc")
+    for name in ("attention.cu", "attention.cuh", "sm103_ptx.cuh", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+    `kernel` on `workload` from the committed profile summaries, if they were
+    taken on the current kernel sources; else None. A summary states it on a
+    line `traffic: kernel=<name> workload=<name> sources_sha256=<hex>
+    dram_bytes_per_launch=<int>`."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = _kernel_sources_sha256()
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for line in f:
+                line = line.strip().strip("`")
+                if not line.startswith("traffic:"):
+                    continue
+                kv = dict(tok.split("=", 1) for tok in line[len("traffic:"):].split() if "=" in tok)
+                if (kv.get("kernel") == kernel and kv.get("workload") == workload
+                        and kv.get("sources_sha256") == sha):
+                    try:
+                        return int(kv["dram_bytes_per_launch"])
+                    except (KeyError, ValueError):
+                        return None
+    return None
+
+
+def _quant_bytes(w, Nqp: int, Nkp: int) -> float:
+    """Bytes the quantization step moves: Q and K read once (BF16) and written
+    as codes (FP16-held INT8, or packed E2M1 plus one E8M0 byte per 32), V read
+    by both passes (channel maxima, then encoding) and written as FP8."""
+    B, H, D = w.B, w.H, w.D
+    code = 2.0 if w.fmt == 0 else 0.5 + 1.0 / 32
+    qk = (B * w.Nq * H * D * 2 + B * H * Nqp * D * code + B * w.Nk * H * D * 2
+          + B * H * Nkp * D * code)
+    return qk + B * w.Nk * H * D * 2 * 2 + B * H * D * Nkp
 
 
 class ClockSampler:
@@ -114,10 +172,11 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64):
     def run(nh, rows):
         qb, kb, vb = (bf16_bits(t[:, :, :nh]) for t in (q, k, v))
         t0 = time.perf_counter()
-        qz = oracle.quantize_int8(qb)
-        kz = oracle.quantize_int8(kb, lens=lens)
+        quant_qk = oracle.quantize_int8 if w.fmt == 0 else oracle.quantize_mxfp4
+        qz = quant_qk(qb)
+        kz = quant_qk(kb, lens=lens)
         vz = oracle.quantize_v_fp8(vb, lens=lens)
-        oracle.attention(0, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows)
+        oracle.attention(w.fmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows)
         return time.perf_counter() - t0
 
     def rows_of(n):
@@ -206,15 +265,22 @@ def main():
             dist.barrier()
 
     q, k, v = make_qkv(w, device="cuda")
-    fmt = 0
+    fmt = w.fmt
     B, Nq, H, D = q.shape
     Nk = k.shape[1]
+    Nqp, Nkp = binding.pad128(Nq), binding.pad128(Nk)
     k_lens = None if w.k_lens is None else torch.tensor(w.k_lens, dtype=torch.int32, device=dev)
-    qq = torch.empty((B, H, binding.pad128(Nq), D), dtype=torch.float16, device=dev)
-    qs = torch.empty((B, H, binding.pad128(Nq) // 128), dtype=torch.float32, device=dev)
-    kq = torch.empty((B, H, binding.pad128(Nk), D), dtype=torch.float16, device=dev)
-    ks = torch.empty((B, H, binding.pad128(Nk) // 128), dtype=torch.float32, device=dev)
-    vq = torch.empty((B, H, D, binding.pad128(Nk)), dtype=torch.uint8, device=dev)
+    if fmt == binding.FMT_INT8:
+        qq = torch.empty((B, H, Nqp, D), dtype=torch.float16, device=dev)
+        qs = torch.empty((B, H, Nqp // 128), dtype=torch.float32, device=dev)
+        kq = torch.empty((B, H, Nkp, D), dtype=torch.float16, device=dev)
+        ks = torch.empty((B, H, Nkp // 128), dtype=torch.float32, device=dev)
+    else:
+        qq = torch.empty((B, H, Nqp, D // 2), dtype=torch.uint8, device=dev)
+        qs = torch.empty((B, H, Nqp, D // 32), dtype=torch.uint8, device=dev)
+        kq = torch.empty((B, H, Nkp, D // 2), dtype=torch.uint8, device=dev)
+        ks = torch.empty((B, H, Nkp, D // 32), dtype=torch.uint8, device=dev)
+    vq = torch.empty((B, H, D, Nkp), dtype=torch.uint8, device=dev)
     vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
     vws = torch.empty(max(16, binding.sage_workspace_bytes(1, fmt, B, H, Nk, Nk)), dtype=torch.uint8,
                       device=dev)
@@ -228,13 +294,9 @@ def main():
     # lands on the next kernel).
     flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
 
-    def quant(evs=None):
+    def quant():
         binding.sage_quantize_qk(q, fmt, out=qq, scale=qs)
-        if evs:
-            evs[0].record()
         binding.sage_quantize_qk(k, fmt, lens=k_lens, out=kq, scale=ks)
-        if evs:
-            evs[1].record()
         binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
 
     def attn():
@@ -247,35 +309,51 @@ def main():
     torch.cuda.synchronize()
     assert binding.sage_last_device_status() == 0
 
+    # The timed step replays two CUDA graphs holding exactly the library's
+    # launches (quantize Q, K, V; attention), so the device time carries no
+    # host launch gaps. The same calls issued eagerly are timed as well.
+    g_quant, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_quant):
+        quant()
+    with torch.cuda.graph(g_attn):
+        attn()
+    for _ in range(args.warmup):
+        g_quant.replay()
+        g_attn.replay()
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+
+    def timed(run_quant, run_attn):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.sum()
+            evs[i][0].record()
+            run_quant()
+            evs[i][1].record()
+            run_attn()
+            evs[i][2].record()
+        torch.cuda.synchronize()
+        barrier()
+        return ([e[0].elapsed_time(e[1]) for e in evs], [e[1].elapsed_time(e[2]) for e in evs])
+
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = str(local)
     clocks = ClockSampler(gpu_id)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks.start()
     time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.sum()
-        ev[i][0].record()
-        quant((ev[i][3], ev[i][4]))
-        ev[i][1].record()
-        attn()
-        ev[i][2].record()
-    torch.cuda.synchronize()
-    barrier()
+    t_quant, t_attn = timed(g_quant.replay, g_attn.replay)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     assert binding.sage_last_device_status() == 0
-    t_quant = [e[0].elapsed_time(e[1]) for e in ev]
-    t_qk = (statistics.mean(e[0].elapsed_time(e[3]) for e in ev),
-            statistics.mean(e[3].elapsed_time(e[4]) for e in ev),
-            statistics.mean(e[4].elapsed_time(e[1]) for e in ev))
-    t_attn = [e[1].elapsed_time(e[2]) for e in ev]
+    t_quant_eager, t_attn_eager = timed(quant, attn)
+    assert binding.sage_last_device_status() == 0
     total_ms = sum(t_quant) + sum(t_attn)
+    eager_ms = (sum(t_quant_eager) + sum(t_attn_eager)) / args.steps
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -284,7 +362,7 @@ def main():
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
     attn_ms = statistics.mean(t_attn)
     hbm, p16, peak_kind = _peaks()
-    peak = _roofline_peak(p16)
+    peak = _roofline_peak(p16, fmt)
     achieved = flops / (attn_ms * 1e-3) / 1e12
 
     # end to end through the public call, host buffers, copies inside the timed region
@@ -299,7 +377,8 @@ def main():
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
-            oo, ll = binding.sage_attention(qd, kd, vd, k_lens=k_lens, num_splits=args.splits)
+            oo, ll = binding.sage_attention(qd, kd, vd, fmt=fmt, k_lens=k_lens,
+                                            num_splits=args.splits)
             oh.copy_(oo, non_blocking=True)
             lh.copy_(ll, non_blocking=True)
 
@@ -333,30 +412,35 @@ def main():
                "kind": "oracle", "sample": desc, "seconds": dt}
 
     launches_per_step = 2 + 2 + 1 + (1 if nsplit > 1 else 0)
-    quant_bytes = (2 * (B * Nq * H * D * 2 + B * H * binding.pad128(Nq) * D * 2)
-                   if Nq == Nk else
-                   B * Nq * H * D * 4 + B * Nk * H * D * 2 + B * H * binding.pad128(Nk) * D * 2
-                   + B * H * binding.pad128(Nq) * D * 2)
-    quant_bytes += B * Nk * H * D * 4 + B * H * D * binding.pad128(Nk)
+    quant_bytes = _quant_bytes(w, Nqp, Nkp)
+    nqt = 2 if Nqp >= 256 else 1
+    kernel = f"sage_attn_kernel<{fmt},{nqt},{(2 if nqt == 2 else 3) if fmt == 0 else 4}>"
+    traffic = _profiled_traffic(kernel, w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8 QK^T (exact, fp16 tensor pipe) + fp8e4m3 PV", "data": "synthetic",
+        "dtype": "int8+fp8e4m3" if fmt == 0 else "mxfp4+fp8e4m3", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
-                   "k_lens": w.k_lens, "format": "int8_qk_fp8_v", "splits": nsplit,
+                   "k_lens": w.k_lens,
+                   "format": "int8_qk_fp8_v" if fmt == 0 else "mxfp4_qk_fp8_v",
+                   "splits": nsplit,
                    "l2": "flushed between steps (256 MiB read outside the timed events)",
+                   "launch": "CUDA graphs of the library calls (quantize Q/K/V; attention)",
                    "parallelism": f"replicas x{world}"},
+        "eager_ms_per_step": eager_ms,
         "attn_only_tflops": achieved,
         "quant_ms_per_step": statistics.mean(t_quant),
-        "quant_q_k_v_ms": [round(t, 4) for t in t_qk],
         "attn_ms_per_step": attn_ms,
         "quant_gbs": quant_bytes / (statistics.mean(t_quant) * 1e-3) / 1e9,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "peak_basis": f"{peak_kind} bf16 {p16} TFLOP/s for Q K^T (fp16 pipe), "
-                                   f"x2 nominal fp8 ratio for P V, harmonic combination",
-                     "kernel": "attn_i8f8_kernel"},
+                     "frac": achieved / peak,
+                     "traffic": None if traffic is None else traffic,
+                     "algorithmic_flops_per_launch": flops,
+                     "peak_basis": (f"{peak_kind} bf16 {p16} TFLOP/s x nominal ratios: Q K^T "
+                                    f"{'fp16 x1' if fmt == 0 else 'fp4 x6'}, P V fp8 x2, "
+                                    f"harmonic combination"),
+                     "kernel": kernel},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk, "wall_s": wall,
     }
