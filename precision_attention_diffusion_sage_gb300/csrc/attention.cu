@@ -591,10 +591,14 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       tc_fence_before();
       mbar_arrive(&s_free[t]);
 
-      const float alpha = alpha_q * sk;
+      // Kept strictly positive, so that a masked score (-inf) gives x = -inf
+      // and p = 0 with no per-element test in the exponential loop. A zero
+      // scale (an all-zero block) only has exact-zero scores, for which
+      // FLT_MIN gives the same x as zero would.
+      const float alpha = fmaxf(alpha_q * sk, 1.17549435e-38f);
       const int64_t key0 = j * 128 + hu * kStep;
       const int nvalid = static_cast<int>(nk - key0 < kStep ? nk - key0 : kStep);
-      if (nvalid < kStep) {
+      if (nvalid < kStep) {  // keys past the end: -inf, p = 0
 #pragma unroll
         for (int c = 0; c < kStep; ++c)
           if (c >= nvalid) s[c] = -INFINITY;
@@ -647,14 +651,8 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int c = ch * 16 + q * 4;
-          float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), alpha2, bias2);
-          float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), alpha2, bias2);
-          if (nvalid < kStep) {  // masked keys contribute exactly 0
-            x01.x = c + 0 < nvalid ? x01.x : -INFINITY;
-            x01.y = c + 1 < nvalid ? x01.y : -INFINITY;
-            x23.x = c + 2 < nvalid ? x23.x : -INFINITY;
-            x23.y = c + 3 < nvalid ? x23.y : -INFINITY;
-          }
+          const float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), alpha2, bias2);
+          const float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), alpha2, bias2);
           const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
           const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
           acc0 = __fadd2_rn(acc0, e01);
