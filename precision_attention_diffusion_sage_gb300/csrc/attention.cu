@@ -1,29 +1,36 @@
-// Fused quantized attention forward for sm_103a (INT8 Q/K, FP8 V).
+// Fused quantized attention forward for sm_103a (INT8 or MXFP4 Q/K, FP8 V).
 //
 // Restates the kernel described on "[ROCm] Add aiter_sage_attn attention
 // backend for gfx1201 (RDNA4)" ("Changes": INT8 QK^T, FP8 PV, FP32
 // accumulation, head dim 128, non-causal) and "new MHA v4 entrypoint ..."
 // ("Motivation": conditional softmax rescaling, base-2 exponentials,
-// pipelines that keep loads, vector ALUs and matrix units busy at once),
-// with the output plus float32 LSE and split-KV of "[None][feat] Add
-// VisualGen FA4 autotuning ..." (first paragraph).
+// pipelines that keep loads, vector ALUs and matrix units busy at once;
+// "Technical Details": MXFP4 E2M1 Q/K), with the output plus float32 LSE and
+// split-KV of "[None][feat] Add VisualGen FA4 autotuning ..." (first
+// paragraph).
 //
 // GB300 design, per CTA (NQT query tiles of 128 rows of one (b, h)):
 //   warps 0 .. 4*NQT-1 : one softmax warpgroup per query tile; thread r owns
 //                        row r (TMEM lane r) of its tile.
 //   warp 4*NQT         : TMA producer of Q (once) and the K ring.
-//   warp 4*NQT+1       : tcgen05 MMA issuer; allocates/frees TMEM.
+//   warp 4*NQT+1       : tcgen05 MMA issuer of query tile 0; allocates/frees
+//                        TMEM.
 //   warp 4*NQT+2       : TMA producer of the V ring (separate so that a K
 //                        load never waits for a V slot to free up).
-// TMEM per tile: S (128 FP32 columns) and O (128 FP32 columns).
-// S = Q K^T runs as kind::f16 on the INT8 codes held as FP16 (sm_103a has no
+//   warp 4*NQT+3       : tcgen05 MMA issuer of query tile 1 (two tiles), so
+//                        that each tile's MMAs wait only for its own softmax.
+// TMEM per tile: S (FP32, one column per key of a step) and O (128 FP32
+// columns), plus the E8M0 scale factors for MXFP4.
+// INT8: S = Q K^T runs as kind::f16 on the codes held as FP16 (sm_103a has no
 // 8-bit integer MMA): products and partial sums are integers below 2^24, so
-// the FP32 accumulator holds the INT32 dot product exactly.
-// Softmax: t = S * alpha, alpha = s_q s_k softmax_scale log2(e); the running
-// row reference m is an integer (ceil of the maximum), raised only when a tile
-// exceeds it by more than kHeadroom; O and l are then rescaled by the exact
-// power of two 2^(m_old - m_new). P8 = E4M3(2^(t - m + 8 - kHeadroom)) goes to
-// a double-buffered 128-byte-swizzled K-major tile in shared memory and
+// the FP32 accumulator holds the INT32 dot product exactly. MXFP4: S runs as
+// block-scaled kind::mxf4 with the 32-channel scales applied in the MMA.
+// Softmax: t = S * alpha, alpha = s_q s_k softmax_scale log2(e) (INT8) or
+// softmax_scale log2(e) (MXFP4); the running row reference m is an integer
+// (ceil of the maximum), raised only when a step exceeds it by more than
+// kHeadroom; O and l are then rescaled by the exact power of two
+// 2^(m_old - m_new). P8 = E4M3(2^(t - m + 8 - kHeadroom)) goes to a
+// double-buffered 128-byte-swizzled K-major tile in shared memory and
 // O += P8 * V8^T runs as kind::f8f6f4. Epilogue: O * s_v / l -> BF16,
 // LSE = (m + log2 l - 8 + kHeadroom) ln 2 (l is kept in P8 units).
 #include <cuda_bf16.h>
@@ -98,10 +105,13 @@ struct TmemLayout {
   __host__ __device__ static constexpr uint32_t s(int t) { return FMT == 0 ? t * 256 : NQT * 128 + t * 64; }
   __host__ __device__ static constexpr uint32_t o(int t) { return FMT == 0 ? t * 256 + 128 : t * 128; }
   __host__ __device__ static constexpr uint32_t sfq(int t) { return NQT * 192 + t * 4; }
-  __host__ __device__ static constexpr uint32_t sfk(int slot) { return NQT * 196 + slot * 4; }
+  // K scales: two slots per query tile (each tile's MMA warp copies its own).
+  __host__ __device__ static constexpr uint32_t sfk(int t, int slot) {
+    return NQT * 196 + (t * 2 + slot) * 4;
+  }
 };
-static_assert(TmemLayout<1, 2>::sfk(1) + 4 <= TmemLayout<1, 2>::kCols, "TMEM budget");
-static_assert(TmemLayout<1, 1>::sfk(1) + 4 <= TmemLayout<1, 1>::kCols, "TMEM budget");
+static_assert(TmemLayout<1, 2>::sfk(1, 1) + 4 <= TmemLayout<1, 2>::kCols, "TMEM budget");
+static_assert(TmemLayout<1, 1>::sfk(0, 1) + 4 <= TmemLayout<1, 1>::kCols, "TMEM budget");
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -161,9 +171,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-// Warp-collective variant: every lane waits, the result is uniform.
+// Warp-collective variant: every lane waits, the result is uniform. The
+// common case (phase already complete) costs one try_wait: the whole warp
+// executes it on the same barrier state, so its result is uniform already.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
   const bool r = wait_or_abort(bar, parity, abort, status);
   return __all_sync(0xffffffffu, r);
 }
@@ -200,7 +213,8 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   constexpr int kPSlots = L::kPSlots;      // P slots per query tile (2 buffers x kSteps)
   constexpr int kSoftmaxWarps = NQT * 4;
   constexpr int kTmaWarp = kSoftmaxWarps;       // Q and K loads
-  constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  constexpr int kMmaWarp = kSoftmaxWarps + 1;   // MMAs of query tile 0; owns TMEM
+  constexpr int kMmaWarp1 = kSoftmaxWarps + 3;  // MMAs of query tile 1 (two tiles only)
   constexpr int kTmaVWarp = kSoftmaxWarps + 2;  // V loads
 
   extern __shared__ uint8_t smem_raw[];
@@ -241,22 +255,24 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   if (*reinterpret_cast<volatile int*>(p.status) & kStatusTimeout) return;
 
   // ---- per-batch key range (uniform over the CTA)
-  int64_t nk = p.Nk;
+  // Token counts fit in 32 bits (the host caps N at 4,194,240).
+  int nk = static_cast<int>(p.Nk);
   if (p.k_lens) {
-    nk = p.k_lens[b];
-    if (nk < 0 || nk > p.Nk) {
+    const int32_t len = p.k_lens[b];
+    if (len < 0 || len > p.Nk) {
       if (threadIdx.x == 0) atomicOr(p.status, kStatusDeviceArg);
       return;
     }
+    nk = len;
   }
-  const int64_t nkv = (nk + 127) / 128;
-  const int64_t per_split = (nkv + p.num_splits - 1) / p.num_splits;
-  const int64_t j0 = static_cast<int64_t>(split) * per_split;
-  const int64_t j1 = j0 + per_split < nkv ? j0 + per_split : nkv;
-  const int64_t niter = j1 > j0 ? j1 - j0 : 0;
+  const int nkv = (nk + 127) / 128;
+  const int per_split = (nkv + p.num_splits - 1) / p.num_splits;
+  const int j0 = split * per_split;
+  const int j1 = j0 + per_split < nkv ? j0 + per_split : nkv;
+  const int niter = j1 > j0 ? j1 - j0 : 0;
   // Softmax steps; a last key tile with at most 64 valid keys needs only its
   // first 64-key step.
-  int64_t nsteps = niter * kSteps;
+  int nsteps = niter * kSteps;
   if (kSteps == 2 && niter > 0 && j1 == nkv && nk - (nkv - 1) * 128 <= 64) nsteps -= 1;
 
   if (niter == 0) {
@@ -284,9 +300,9 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], NQT);  // one commit per query tile's MMA warp
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], NQT);
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(&s_full[t], 1);
@@ -296,7 +312,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         mbar_init(&o_done[t * kPSlots + q], 1);
       }
     }
-    mbar_init(mma_final, 1);
+    mbar_init(mma_final, NQT);
     *abort = 0;
     fence_barrier_init();
   }
@@ -359,12 +375,12 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) kw[c] = __ldg(ksf + j0 * 128 + 32 * c);
     }
-    int kfills[STAGES];
-    for (int s = 0; s < STAGES; ++s) kfills[s] = 0;
-    for (int64_t it = 0; it < niter; ++it) {
-      const int s = static_cast<int>(it % STAGES);
-      const uint32_t u = static_cast<uint32_t>(it / STAGES);
-      if (u > 0 && !warp_wait(&k_empty[s], (u - 1) & 1, abort, p.status)) break;
+    // Fill `it` goes to stage it % STAGES once the fill STAGES earlier has
+    // been consumed; `rph` is the parity of the current round of stages.
+    int s = 0, filled = 0;
+    uint32_t rph = 0;
+    for (int it = 0; it < niter; ++it) {
+      if (it >= STAGES && !warp_wait(&k_empty[s], rph ^ 1u, abort, p.status)) break;
       if constexpr (FMT == 1) {
         st_shared_v4(smem_u32(sSf + (NQT + s) * 512) + lane * 16, kw[0], kw[1], kw[2], kw[3]);
         fence_proxy_async_smem();
@@ -372,7 +388,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       }
       if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], F::kTileBytes);
-        const int yk = static_cast<int>(bh * Nk_pad + (j0 + it) * 128);
+        const int yk = static_cast<int>(bh * Nk_pad) + (j0 + it) * 128;
         if constexpr (FMT == 0) {
           tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
           tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
@@ -387,91 +403,104 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
           for (int c = 0; c < 4; ++c) kw[c] = __ldg(ksf + (j0 + it + 1) * 128 + 32 * c);
         }
       }
-      ++kfills[s];
+      filled = it + 1;
+      if (++s == STAGES) {
+        s = 0;
+        rph ^= 1u;
+      }
     }
     // Drain: no TMA write may still be in flight when the CTA exits.
     drain_wait(q_full, 0, p.status);
-    for (int s = 0; s < STAGES; ++s)
-      if (kfills[s] > 0) drain_wait(&k_full[s], static_cast<uint32_t>(kfills[s] - 1) & 1, p.status);
+    for (int st = 0; st < STAGES; ++st) {
+      const int fills = (filled - st + STAGES - 1) / STAGES;
+      if (fills > 0) drain_wait(&k_full[st], static_cast<uint32_t>(fills - 1) & 1u, p.status);
+    }
   } else if (warp == kTmaVWarp) {
     // ================================================================ TMA producer (V)
     if (elect_one()) tma_prefetch_desc(&tmV);
     __syncwarp();
-    int vfills[STAGES];
-    for (int s = 0; s < STAGES; ++s) vfills[s] = 0;
-    for (int64_t it = 0; it < niter; ++it) {
-      const int s = static_cast<int>(it % STAGES);
-      const uint32_t u = static_cast<uint32_t>(it / STAGES);
-      if (u > 0 && !warp_wait(&v_empty[s], (u - 1) & 1, abort, p.status)) break;
+    int s = 0, filled = 0;
+    uint32_t rph = 0;
+    for (int it = 0; it < niter; ++it) {
+      if (it >= STAGES && !warp_wait(&v_empty[s], rph ^ 1u, abort, p.status)) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(&v_full[s], 16384);
-        tma_load_2d(sV + s * 16384, &tmV, &v_full[s], static_cast<int>((j0 + it) * 128),
-                    static_cast<int>(bh * 128));
+        tma_load_2d(sV + s * 16384, &tmV, &v_full[s], (j0 + it) * 128, static_cast<int>(bh * 128));
       }
       __syncwarp();
-      ++vfills[s];
+      filled = it + 1;
+      if (++s == STAGES) {
+        s = 0;
+        rph ^= 1u;
+      }
     }
-    for (int s = 0; s < STAGES; ++s)
-      if (vfills[s] > 0) drain_wait(&v_full[s], static_cast<uint32_t>(vfills[s] - 1) & 1, p.status);
-  } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issuer
+    for (int st = 0; st < STAGES; ++st) {
+      const int fills = (filled - st + STAGES - 1) / STAGES;
+      if (fills > 0) drain_wait(&v_full[st], static_cast<uint32_t>(fills - 1) & 1u, p.status);
+    }
+  } else if (warp == kMmaWarp || (NQT == 2 && warp == kMmaWarp1)) {
+    // ================================================================ MMA issuers
+    // One warp per query tile issues that tile's MMAs, so neither tile's
+    // tensor work waits in line behind the other tile's softmax. Both read
+    // the same K/V stages; a stage is released once both have committed.
+    const int t = warp == kMmaWarp ? 0 : 1;
     constexpr uint32_t kIdescS = idesc_f32acc(128, 128);  // f16 x f16 -> f32 (INT8 codes)
     constexpr uint32_t kIdescO = idesc_f32acc(128, 128);  // e4m3 x e4m3 -> f32
-    // Descriptor low words of every operand buffer (k slices add a constant).
-    // The 64- and 128-byte swizzled layouts share the low-word encoding.
-    const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ));    // + tile bytes / 16 per Q tile
+    // Descriptor low words of this tile's operand buffers (k slices add a
+    // constant). The 64- and 128-byte swizzled layouts share the encoding.
+    const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ + t * F::kTileBytes));
     const uint32_t k_lo = sw128_desc_lo(smem_u32(sK));    // + tile bytes / 16 per stage
-    const uint32_t p_lo = sw128_desc_lo(smem_u32(sP));    // + (2t + buffer) * 1024
+    const uint32_t p_lo = sw128_desc_lo(smem_u32(sP + t * 2 * 16384));  // + buffer * 1024
     const uint32_t v_lo = sw128_desc_lo(smem_u32(sV));    // + stage * 1024
+    const uint32_t d_s = tbase + TM::s(t), d_o = tbase + TM::o(t);
+    constexpr int kPSlotShift = kPSlots == 4 ? 2 : 1;  // log2(kPSlots)
     // The elected lane is the same (lowest) lane every time, so the commits
     // track the MMAs that lane issued.
-    auto issue_s = [&](int t, int64_t v) {
-      const int stage = static_cast<int>((v / kSteps) % STAGES);
-      const uint32_t d = tbase + TM::s(t);
+    // S for a step using K stage `stage`, 64-key half `half` (MXFP4) and
+    // K-scale TMEM slot `sf_slot`.
+    auto issue_s = [&](int stage, int half, int sf_slot) {
       if constexpr (FMT == 0) {
-        const uint32_t qa = q_lo + t * 2048, ka = k_lo + stage * 2048;
+        const uint32_t ka = k_lo + stage * 2048;
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-            mma_f16_ss_lo(d, qa + off, ka + off, kIdescS, k > 0);
+            mma_f16_ss_lo(d_s, q_lo + off, ka + off, kIdescS, k > 0);
           }
           mma_commit(&s_full[t]);
         }
       } else {
         // Keys 64h .. 64h+63 of the stage: B rows at +4096 bytes, their
         // scales two TMEM columns further (rows 64..127 of the 128-row copy).
-        const int half = static_cast<int>(v % kSteps);
-        const uint32_t qa = q_lo + t * 512, ka = k_lo + stage * 512 + half * 256;
+        const uint32_t ka = k_lo + stage * 512 + half * 256;
         const uint32_t sfa = tbase + TM::sfq(t);
-        const uint32_t sfb = tbase + TM::sfk(static_cast<int>((v / kSteps) & 1)) + half * 2;
+        const uint32_t sfb = tbase + TM::sfk(t, sf_slot) + half * 2;
         if (elect_one()) {
-          mma_mxf4_ss_lo(d, qa, ka, idesc_mxf4(128, 64, 0), sfa, sfb, 0u);
-          mma_mxf4_ss_lo(d, qa + 2, ka + 2, idesc_mxf4(128, 64, 2), sfa, sfb, 1u);
+          mma_mxf4_ss_lo(d_s, q_lo, ka, idesc_mxf4(128, 64, 0), sfa, sfb, 0u);
+          mma_mxf4_ss_lo(d_s, q_lo + 2, ka + 2, idesc_mxf4(128, 64, 2), sfa, sfb, 1u);
           mma_commit(&s_full[t]);
         }
       }
       __syncwarp();
     };
-    // MXFP4: scales of local K tile i to TMEM slot i & 1. The slot was last
-    // read by the S MMAs of tile i - 2, which completed before the S of the
-    // step before this tile's first step, whose s_free has been waited for.
-    auto copy_k_scales = [&](int64_t i) {
+    // MXFP4: scales of K stage `stage` to this tile's TMEM slot `sf_slot`
+    // (local K tile index & 1). The slot was last read by this tile's S MMAs
+    // of tile i - 2, complete once the S of the step before this tile's
+    // first step has been read (its s_free was waited for).
+    auto copy_k_scales = [&](int stage, int sf_slot) {
       if (elect_one())
-        tmem_cp_sf512(tbase + TM::sfk(static_cast<int>(i & 1)),
-                      smem_u32(sSf + (NQT + static_cast<int>(i % STAGES)) * 512));
+        tmem_cp_sf512(tbase + TM::sfk(t, sf_slot), smem_u32(sSf + (NQT + stage) * 512));
       __syncwarp();
     };
-    auto issue_pv = [&](int t, int slot, int stage, int half, bool acc) {
-      const uint32_t d = tbase + TM::o(t);
+    auto issue_pv = [&](int slot, int stage, int half, bool acc) {
       const int pbuf = slot / kSteps;
-      const uint32_t pa = p_lo + (t * 2 + pbuf) * 1024, va = v_lo + stage * 1024;
+      const uint32_t pa = p_lo + pbuf * 1024, va = v_lo + stage * 1024;
       constexpr int kK = kStep / 32;  // K = 32 slices per step
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < kK; ++k) {
           const int kk = half * kK + k;
-          mma_f8_ss_lo(d, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+          mma_f8_ss_lo(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
         }
         mma_commit(&o_done[t * kPSlots + slot]);
       }
@@ -481,62 +510,65 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       if (elect_one()) mma_commit(bar);
       __syncwarp();
     };
+    // K ring position of the S steps (stage, parity of its fill round) and
+    // V ring position of the P V steps; both advance after a tile's last step.
+    int ks = 0, vs = 0;
+    uint32_t kph = 0, vph = 0;
     bool ok = warp_wait(q_full, 0, abort, p.status);
     if (ok) ok = warp_wait(&k_full[0], 0, abort, p.status);
     tc_fence_after();
     if (ok) {
       if constexpr (FMT == 1) {
-        if (elect_one())
-          for (int t = 0; t < NQT; ++t) tmem_cp_sf512(tbase + TM::sfq(t), smem_u32(sSf + t * 512));
+        if (elect_one()) tmem_cp_sf512(tbase + TM::sfq(t), smem_u32(sSf + t * 512));
         __syncwarp();
-        copy_k_scales(0);
+        copy_k_scales(0, 0);
       }
-      for (int t = 0; t < NQT; ++t) issue_s(t, 0);
-      if (kSteps == 1) commit(&k_empty[0]);
+      issue_s(0, 0, 0);
+      if constexpr (kSteps == 1) {
+        commit(&k_empty[0]);
+        if (++ks == STAGES) { ks = 0; kph ^= 1u; }
+      }
     }
-    for (int64_t u = 0; ok && u < nsteps; ++u) {
-      // Next S first (each needs only its softmax warpgroup to have read the
-      // previous S), then this step's P V products. V is waited for only
-      // right before the P V MMAs.
-      const int64_t v = u + 1;
+    for (int u = 0; ok && u < nsteps; ++u) {
+      // Next S first (it needs only the softmax warpgroup to have read the
+      // previous S), then this step's P V. V is waited for only right before
+      // the P V MMAs.
+      const int v = u + 1;
       if (v < nsteps) {
-        const int64_t iv = v / kSteps;
-        const int sv = static_cast<int>(iv % STAGES);
-        const bool first_half = (v % kSteps) == 0;
-        if (first_half) {
-          if (!(ok = warp_wait(&k_full[sv], static_cast<uint32_t>(iv / STAGES) & 1, abort, p.status))) break;
+        const int hv = v & (kSteps - 1);
+        if (hv == 0) {
+          if (!(ok = warp_wait(&k_full[ks], kph, abort, p.status))) break;
           tc_fence_after();
         }
-        for (int t = 0; t < NQT && ok; ++t) {
-          if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(u) & 1, abort, p.status))) break;
-          tc_fence_after();
-          if constexpr (FMT == 1) {
-            if (first_half && t == 0) copy_k_scales(iv);
-          }
-          issue_s(t, v);
+        if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(u) & 1u, abort, p.status))) break;
+        tc_fence_after();
+        const int sf_slot = (v / kSteps) & 1;
+        if constexpr (FMT == 1) {
+          if (hv == 0) copy_k_scales(ks, sf_slot);
         }
-        if (!ok) break;
-        if ((v % kSteps) == kSteps - 1) commit(&k_empty[sv]);
+        issue_s(ks, hv, sf_slot);
+        if (hv == kSteps - 1) {
+          commit(&k_empty[ks]);
+          if (++ks == STAGES) { ks = 0; kph ^= 1u; }
+        }
       }
-      const int64_t iu = u / kSteps;
-      const int su = static_cast<int>(iu % STAGES);
-      const int hu = static_cast<int>(u % kSteps);
-      const int slot = static_cast<int>(u % kPSlots);
+      const int hu = u & (kSteps - 1);
+      const int slot = u & (kPSlots - 1);
       if (hu == 0) {
-        if (!(ok = warp_wait(&v_full[su], static_cast<uint32_t>(iu / STAGES) & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(&v_full[vs], vph, abort, p.status))) break;
         tc_fence_after();
       }
-      for (int t = 0; t < NQT && ok; ++t) {
-        if (!(ok = warp_wait(&p_full[t * kPSlots + slot], static_cast<uint32_t>(u / kPSlots) & 1,
-                             abort, p.status)))
-          break;
-        tc_fence_after();
-        issue_pv(t, slot, su, hu, u > 0);
+      if (!(ok = warp_wait(&p_full[t * kPSlots + slot],
+                           static_cast<uint32_t>(u >> kPSlotShift) & 1u, abort, p.status)))
+        break;
+      tc_fence_after();
+      issue_pv(slot, vs, hu, u > 0);
+      if (hu == kSteps - 1) {
+        commit(&v_empty[vs]);
+        if (++vs == STAGES) { vs = 0; vph ^= 1u; }
       }
-      if (!ok) break;
-      if (hu == kSteps - 1) commit(&v_empty[su]);
     }
-    // All MMAs issued by the elected lane must finish before TMEM is freed.
+    // All MMAs issued by both MMA warps must finish before TMEM is freed.
     commit(mma_final);
     drain_wait(mma_final, 0, p.status);
   }
@@ -567,16 +599,17 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     const uint32_t p_row0 = smem_u32(sP + (t * 2) * 16384) + r * 128;  // P buffer 0; buffer 1 at +16 KB
     const uint32_t swz = static_cast<uint32_t>(r & 7);
 
+    constexpr int kPSlotShift = kPSlots == 4 ? 2 : 1;  // log2(kPSlots)
     float sk = 1.0f;
-    for (int64_t u = 0; u < nsteps; ++u) {
-      const int64_t iu = u / kSteps;
-      const int hu = static_cast<int>(u % kSteps);
-      const int64_t j = j0 + iu;
+    for (int u = 0; u < nsteps; ++u) {
+      const int iu = u / kSteps;
+      const int hu = u & (kSteps - 1);
+      const int j = j0 + iu;
       if constexpr (FMT == 0) {
         sk = sk_next;
         if (iu + 1 < niter) sk_next = __ldg(&kscale[j + 1]);
       }
-      if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(u) & 1, abort, p.status))) break;
+      if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(u) & 1u, abort, p.status))) break;
       tc_fence_after();
       float s[kStep];
       {
@@ -596,8 +629,8 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       // scale (an all-zero block) only has exact-zero scores, for which
       // FLT_MIN gives the same x as zero would.
       const float alpha = fmaxf(alpha_q * sk, 1.17549435e-38f);
-      const int64_t key0 = j * 128 + hu * kStep;
-      const int nvalid = static_cast<int>(nk - key0 < kStep ? nk - key0 : kStep);
+      const int key0 = j * 128 + hu * kStep;
+      const int nvalid = nk - key0 < kStep ? nk - key0 : kStep;
       if (nvalid < kStep) {  // keys past the end: -inf, p = 0
 #pragma unroll
         for (int c = 0; c < kStep; ++c)
@@ -608,14 +641,12 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       // First step: set the reference. Later: raise it only past the headroom.
       const float m_new = (u == 0) ? cand : (cand > m + kHeadroom ? cand : m);
       const bool rescale = (u > 0) && (m_new > m);
-      bool o_prev_done = false;  // P V of the previous step known complete
       if (__any_sync(0xffffffffu, rescale)) {
         // Conditional rescale: O_t must hold P V up to the previous step.
-        const int ps = static_cast<int>((u - 1) % kPSlots);
-        if (!(ok = warp_wait(&o_done[t * kPSlots + ps], static_cast<uint32_t>((u - 1) / kPSlots) & 1,
-                             abort, p.status)))
+        const int ps = (u - 1) & (kPSlots - 1);
+        if (!(ok = warp_wait(&o_done[t * kPSlots + ps],
+                             static_cast<uint32_t>((u - 1) >> kPSlotShift) & 1u, abort, p.status)))
           break;
-        o_prev_done = true;
         tc_fence_after();
         const float f = rescale ? exp2_neg_int(m - m_new) : 1.0f;
 #pragma unroll
@@ -631,16 +662,13 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       }
       m = m_new;
       const float bias = 8.0f - kHeadroom - m;
-      const int slot = static_cast<int>(u % kPSlots);
+      const int slot = u & (kPSlots - 1);
       const uint32_t p_row = p_row0 + static_cast<uint32_t>(slot / kSteps) * 16384;
-
-      // The P slot is free once P V of step u - kPSlots (same slot) is
-      // complete; P V of step u - 1 being complete implies it (in order).
-      if (u >= kPSlots && !o_prev_done) {
-        if (!(ok = warp_wait(&o_done[t * kPSlots + slot],
-                             static_cast<uint32_t>((u - kPSlots) / kPSlots) & 1, abort, p.status)))
-          break;
-      }
+      // The P slot was last read by P V of step u - kPSlots. No wait is
+      // needed for it: the MMA warp issued that P V before the S of step u
+      // (its loop issues S of step w + 1 after P V of step w - 1, and
+      // u - kPSlots <= u - 2), and the s_full commit this warp waited for
+      // completes only after every earlier MMA of that warp.
       // x = S * alpha + (8 - m) two at a time (packed FP32x2 FMA), p8 = 2^x,
       // four partial row sums (packed FP32x2 adds).
       const float2 alpha2 = make_float2(alpha, alpha), bias2 = make_float2(bias, bias);
@@ -670,8 +698,8 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
 
     // ---- epilogue
     if (ok)
-      ok = warp_wait(&o_done[t * kPSlots + static_cast<int>((nsteps - 1) % kPSlots)],
-                     static_cast<uint32_t>((nsteps - 1) / kPSlots) & 1, abort, p.status);
+      ok = warp_wait(&o_done[t * kPSlots + ((nsteps - 1) & (kPSlots - 1))],
+                     static_cast<uint32_t>((nsteps - 1) >> kPSlotShift) & 1u, abort, p.status);
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
