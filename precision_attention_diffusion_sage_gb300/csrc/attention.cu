@@ -87,7 +87,8 @@ struct SmemLayout {
   static constexpr int kV = kK + STAGES * F::kTileBytes;   // STAGES x 16 KB (FP8 V^T 128x128)
   static constexpr int kP = kV + STAGES * 16384;           // NQT x 2 x 16 KB (FP8 P, double buffer)
   static constexpr int kSf = kP + NQT * 2 * 16384;         // (NQT + STAGES) scale blocks
-  static constexpr int kBar = kSf + (NQT + STAGES) * F::kSfBytes;
+  static constexpr int kSv = kSf + (NQT + STAGES) * F::kSfBytes;  // 128 V channel scales
+  static constexpr int kBar = kSv + 512;
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
   //           s_full[T], s_free[T], p_full[T][kPSlots], o_done[T][kPSlots], mma_final
   static constexpr int kNumBars = 1 + 4 * STAGES + NQT * (2 + 2 * kPSlots) + 1;
@@ -204,7 +205,8 @@ template <int FMT, int NQT, int STAGES>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     sage_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmO, const AttnParams p) {
   using L = SmemLayout<FMT, NQT, STAGES>;
   using F = QKFormat<FMT>;
   using TM = TmemLayout<FMT, NQT>;
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   uint8_t* sV = smem + L::kV;
   uint8_t* sP = smem + L::kP;
   uint8_t* sSf = smem + L::kSf;  // MXFP4 scales: NQT query tiles, then STAGES K tiles
+  float* sSv = reinterpret_cast<float*>(smem + L::kSv);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
@@ -296,6 +299,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   }
 
   // ---- setup
+  if (threadIdx.x < 128) sSv[threadIdx.x] = __ldg(&p.v_scale[bh * 128 + threadIdx.x]);
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
@@ -703,7 +707,6 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const float* sv = p.v_scale + bh * 128;
       const float lse = (m + log2f(l) - 8.0f + kHeadroom) * kLn2;
       const bool store = row < p.Nq;
       if (p.num_splits > 1) {
@@ -716,15 +719,45 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               float4 o4;
-              o4.x = __uint_as_float(v[i + 0]) * (__ldg(&sv[c * 32 + i + 0]) * inv_l);
-              o4.y = __uint_as_float(v[i + 1]) * (__ldg(&sv[c * 32 + i + 1]) * inv_l);
-              o4.z = __uint_as_float(v[i + 2]) * (__ldg(&sv[c * 32 + i + 2]) * inv_l);
-              o4.w = __uint_as_float(v[i + 3]) * (__ldg(&sv[c * 32 + i + 3]) * inv_l);
+              o4.x = __uint_as_float(v[i + 0]) * (sSv[c * 32 + i + 0] * inv_l);
+              o4.y = __uint_as_float(v[i + 1]) * (sSv[c * 32 + i + 1] * inv_l);
+              o4.z = __uint_as_float(v[i + 2]) * (sSv[c * 32 + i + 2] * inv_l);
+              o4.w = __uint_as_float(v[i + 3]) * (sSv[c * 32 + i + 3] * inv_l);
               *reinterpret_cast<float4*>(op + c * 32 + i) = o4;
             }
           }
         }
         if (store) p.lse_part[(static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row] = lse;
+      } else if (p.o_tma) {
+        // Row r as BF16 into this tile's two P buffers (free now: the last
+        // P V has completed), laid out as the two 64-channel halves of the
+        // 128-byte swizzled box the O tensor map stores from; one thread
+        // stores every tile after the final barrier.
+        const uint32_t obase = smem_u32(sP + t * 2 * 16384) + r * 128;
+        const uint32_t rsw = static_cast<uint32_t>(r & 7);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + c * 32, v);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float4 sa = *reinterpret_cast<const float4*>(sSv + c * 32 + g * 8);
+            const float4 sb = *reinterpret_cast<const float4*>(sSv + c * 32 + g * 8 + 4);
+            const float sc[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a0 = __uint_as_float(v[g * 8 + 2 * k]) * (sc[2 * k] * inv_l);
+              const float a1 = __uint_as_float(v[g * 8 + 2 * k + 1]) * (sc[2 * k + 1] * inv_l);
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+              w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + g);
+            st_shared_v4(obase + (c >> 1) * 16384 + ((chunk ^ rsw) << 4), w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        if (store && p.lse) p.lse[bh * p.Nq + row] = lse;
       } else {
         __nv_bfloat16* orow = p.o + b * p.osb + row * p.osn + h * p.osh;
 #pragma unroll
@@ -737,8 +770,8 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
               uint32_t w[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const float a0 = __uint_as_float(v[i + 2 * k]) * (__ldg(&sv[c * 32 + i + 2 * k]) * inv_l);
-                const float a1 = __uint_as_float(v[i + 2 * k + 1]) * (__ldg(&sv[c * 32 + i + 2 * k + 1]) * inv_l);
+                const float a0 = __uint_as_float(v[i + 2 * k]) * (sSv[c * 32 + i + 2 * k] * inv_l);
+                const float a1 = __uint_as_float(v[i + 2 * k + 1]) * (sSv[c * 32 + i + 2 * k + 1] * inv_l);
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
                 w[k] = *reinterpret_cast<const uint32_t*>(&h2);
               }
@@ -756,6 +789,20 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, TM::kCols);
+  } else if (warp == kTmaWarp && p.o_tma && !*abort) {
+    // Store the staged O tiles (rows past Nq are clipped by the tensor map).
+    if (elect_one()) {
+      for (int t = 0; t < NQT; ++t) {
+        const int qt = static_cast<int>(blockIdx.x) * NQT + t;
+        if (qt >= p.nbq) break;
+        tma_store_4d(&tmO, sP + t * 2 * 16384, 0, static_cast<int>(h), qt * 128, static_cast<int>(b));
+        tma_store_4d(&tmO, sP + t * 2 * 16384 + 16384, 64, static_cast<int>(h), qt * 128,
+                     static_cast<int>(b));
+      }
+      tma_store_commit();
+      tma_store_wait_read();
+    }
+    __syncwarp();
   }
 }
 
@@ -807,7 +854,7 @@ bool make_map_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int es
 
 template <int FMT, int NQT, int STAGES>
 cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                           const AttnParams& p, cudaStream_t stream) {
+                           const CUtensorMap& mo, const AttnParams& p, cudaStream_t stream) {
   using L = SmemLayout<FMT, NQT, STAGES>;
   static_assert(L::kDynamic <= 232448, "shared memory budget");
   constexpr auto kern = sage_attn_kernel<FMT, NQT, STAGES>;
@@ -826,7 +873,7 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const C
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>((p.nbq + NQT - 1) / NQT), static_cast<unsigned>(p.H),
             static_cast<unsigned>(p.B * p.num_splits));
-  kern<<<grid, attn_threads<NQT>(), L::kDynamic, stream>>>(mq, mk, mv, p);
+  kern<<<grid, attn_threads<NQT>(), L::kDynamic, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -866,14 +913,32 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
       !make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(Nk_pad),
                    static_cast<uint64_t>(a.p.B * a.p.H * 128), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const bool two = attn_q_tiles_per_cta(a.p.nbq) == 2;
+  // O through a 4-D map over the caller's [B][Nq][H][D] strides (boxes of
+  // 128 rows x 64 channels); the kernel falls back to direct stores when the
+  // strides cannot be described (e.g. a zero stride) or the keys are split.
+  AttnParams p = a.p;
+  CUtensorMap mo;
+  p.o_tma = 0;
+  if (p.num_splits <= 1) {
+    const uint64_t dims[4] = {128, static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.Nq),
+                              static_cast<uint64_t>(p.B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(p.osh) * 2, static_cast<uint64_t>(p.osn) * 2,
+                                 static_cast<uint64_t>(p.osb) * 2};
+    const uint32_t box[4] = {64, 1, 128, 1};
+    if (p.osh > 0 && p.osn > 0 && p.osb > 0 &&
+        encode_tiled(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.o, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      p.o_tma = 1;
+  }
+  if (!p.o_tma) mo = mv;  // unused by the kernel
+  const bool two = attn_q_tiles_per_cta(p.nbq) == 2;
   cudaError_t e;
   if (a.fmt == 0)
-    e = two ? launch_variant<0, 2, 2>(mq, mk, mv, a.p, stream)
-            : launch_variant<0, 1, 3>(mq, mk, mv, a.p, stream);
+    e = two ? launch_variant<0, 2, 2>(mq, mk, mv, mo, p, stream)
+            : launch_variant<0, 1, 3>(mq, mk, mv, mo, p, stream);
   else
-    e = two ? launch_variant<1, 2, 4>(mq, mk, mv, a.p, stream)
-            : launch_variant<1, 1, 4>(mq, mk, mv, a.p, stream);
+    e = two ? launch_variant<1, 2, 4>(mq, mk, mv, mo, p, stream)
+            : launch_variant<1, 1, 4>(mq, mk, mv, mo, p, stream);
   if (e != cudaSuccess || a.p.num_splits <= 1) return e;
   const int64_t rows = a.p.B * a.p.H * a.p.Nq;
   const int64_t blocks = (rows * 32 + 255) / 256;

@@ -21,6 +21,7 @@ struct AttnParams {
   int64_t osb, osn, osh;
   float* lse;            // nullable [B][H][Nq]
   int num_splits;
+  int o_tma;             // 1: O stored through the tensor map (set by the launcher)
   float* o_part;         // [splits][B][H][Nq][128] when num_splits > 1
   float* lse_part;       // [splits][B][H][Nq]
   int* status;

@@ -102,6 +102,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+// 4-D tiled store of one box from shared memory to global memory (bulk
+// async-group completion). Coordinates past the tensor's extent are clipped.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int32_t c0,
+                                             int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Returns once every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Makes generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
