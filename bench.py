@@ -43,6 +43,9 @@ def _peaks():
 
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
 _FP8_RATIO, _FP4_RATIO = 2.0, 6.0
+# Hardware exp2 (MUFU) throughput per SM per clock, measured on GB300 with a
+# microbenchmark of back-to-back ex2.approx.ftz.f32.
+_EX2_PER_CLK_SM = 32
 
 
 def _roofline_peak(p16: float, fmt: int) -> float:
@@ -157,7 +160,7 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64):
+def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64, nthreads: int = 0):
     """Time the CPU oracle (as it stands) on a bounded sample of workload w:
     quantization of the first `nh` heads' Q/K/V plus attention for `n` query
     rows of those heads, sized from a short calibration run to take about
@@ -176,7 +179,8 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64):
         qz = quant_qk(qb)
         kz = quant_qk(kb, lens=lens)
         vz = oracle.quantize_v_fp8(vb, lens=lens)
-        oracle.attention(w.fmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows)
+        oracle.attention(w.fmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows,
+                         nthreads=nthreads)
         return time.perf_counter() - t0
 
     def rows_of(n):
@@ -237,11 +241,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads (a smaller case for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
+    from dataclasses import replace as _replace
     from precision_attention_diffusion_sage_gb300.inputs import WORKLOADS, make_qkv
     w = WORKLOADS[args.workload]
+    if args.heads > 0:
+        w = _replace(w, H=args.heads)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -294,49 +303,63 @@ def main():
     # lands on the next kernel).
     flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
 
-    def quant():
+    def quant_q():
         binding.sage_quantize_qk(q, fmt, out=qq, scale=qs)
+
+    def quant_k():
         binding.sage_quantize_qk(k, fmt, lens=k_lens, out=kq, scale=ks)
+
+    def quant_v():
         binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
 
     def attn():
         binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens, out=o,
                               lse=lse, num_splits=args.splits, workspace=aws)
 
+    calls = (quant_q, quant_k, quant_v, attn)
     for _ in range(args.warmup):
-        quant()
-        attn()
+        for c in calls:
+            c()
     torch.cuda.synchronize()
     assert binding.sage_last_device_status() == 0
 
     # The timed step replays two CUDA graphs holding exactly the library's
-    # launches (quantize Q, K, V; attention), so the device time carries no
-    # host launch gaps. The same calls issued eagerly are timed as well.
-    g_quant, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_quant):
-        quant()
-    with torch.cuda.graph(g_attn):
-        attn()
+    # launches (quantize Q, K and V; attention), so the device time carries
+    # no host launch gaps. Also timed: each call in a graph of its own (the
+    # per-call split; every graph launch adds a few microseconds), and the
+    # same calls issued eagerly.
+    def capture(fns):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for fn in fns:
+                fn()
+        return g
+
+    g_quant, g_attn = capture(calls[:3]), capture(calls[3:])
+    per_call_graphs = [capture([c]) for c in calls]
     for _ in range(args.warmup):
         g_quant.replay()
         g_attn.replay()
+        for g in per_call_graphs:
+            g.replay()
     torch.cuda.synchronize()
     assert binding.sage_last_device_status() == 0
 
-    def timed(run_quant, run_attn):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    def timed(runs):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)]
+               for _ in range(args.steps)]
         barrier()
         torch.cuda.synchronize()
         for i in range(args.steps):
             flush.sum()
             evs[i][0].record()
-            run_quant()
-            evs[i][1].record()
-            run_attn()
-            evs[i][2].record()
+            for j, r in enumerate(runs):
+                r()
+                evs[i][j + 1].record()
         torch.cuda.synchronize()
         barrier()
-        return ([e[0].elapsed_time(e[1]) for e in evs], [e[1].elapsed_time(e[2]) for e in evs])
+        # per call: list over steps
+        return [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(len(runs))]
 
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -346,11 +369,14 @@ def main():
     clocks.start()
     time.sleep(0.3)
     wall0 = time.perf_counter()
-    t_quant, t_attn = timed(g_quant.replay, g_attn.replay)
+    t_quant, t_attn = timed([g_quant.replay, g_attn.replay])
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     assert binding.sage_last_device_status() == 0
-    t_quant_eager, t_attn_eager = timed(quant, attn)
+    per_call = timed([g.replay for g in per_call_graphs])
+    eager_calls = timed(list(calls))
+    t_quant_eager = [a + b + c for a, b, c in zip(*eager_calls[:3])]
+    t_attn_eager = eager_calls[3]
     assert binding.sage_last_device_status() == 0
     total_ms = sum(t_quant) + sum(t_attn)
     eager_ms = (sum(t_quant_eager) + sum(t_attn_eager)) / args.steps
@@ -408,14 +434,22 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, dt, desc, n = _cpu_oracle_sample(w, args.cpu_seconds)
+        f1, dt1, desc1, _ = _cpu_oracle_sample(w, args.cpu_seconds / 3, nthreads=1)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-               "kind": "oracle", "sample": desc, "seconds": dt}
+               "kind": "oracle", "sample": desc, "seconds": dt,
+               "value_1core": f1 / dt1 / 1e12, "sample_1core": desc1, "seconds_1core": dt1}
 
     launches_per_step = 2 + 2 + 1 + (1 if nsplit > 1 else 0)
     quant_bytes = _quant_bytes(w, Nqp, Nkp)
+    # Secondary bound: one exp2 per logit on the MUFU pipe (no FMA-polynomial
+    # exponentials are used), at the SM clock sampled during the run.
+    nk_sum = sum(w.k_lens) if w.k_lens else w.B * w.Nk
+    exp2_count = float(w.H) * w.Nq * nk_sum
+    mhz = (clk or {}).get("sm_mhz") or 2070.0
+    exp2_ms = exp2_count / (_EX2_PER_CLK_SM * 152 * mhz * 1e6) * 1e3
     nqt = 2 if Nqp >= 256 else 1
     kernel = f"sage_attn_kernel<{fmt},{nqt},{(2 if nqt == 2 else 3) if fmt == 0 else 4}>"
-    traffic = _profiled_traffic(kernel, w.name)
+    traffic = _profiled_traffic(kernel, w.name) if args.heads == 0 else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -423,16 +457,23 @@ def main():
         "dtype": "int8+fp8e4m3" if fmt == 0 else "mxfp4+fp8e4m3", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
                    "k_lens": w.k_lens,
+                   "heads_override": args.heads > 0,
                    "format": "int8_qk_fp8_v" if fmt == 0 else "mxfp4_qk_fp8_v",
                    "splits": nsplit,
                    "l2": "flushed between steps (256 MiB read outside the timed events)",
-                   "launch": "CUDA graphs of the library calls (quantize Q/K/V; attention)",
+                   "launch": "one CUDA graph per library call (quantize Q, K, V; attention)",
+                   "cta": ("1-CTA tiles (cta_group::1), "
+                           f"{nqt} query tile(s) of 128 rows per CTA, one MMA warp per tile"),
                    "parallelism": f"replicas x{world}"},
         "eager_ms_per_step": eager_ms,
         "attn_only_tflops": achieved,
         "quant_ms_per_step": statistics.mean(t_quant),
+        "quant_q_k_v_ms": [round(statistics.mean(c), 5) for c in per_call[:3]],
         "attn_ms_per_step": attn_ms,
         "quant_gbs": quant_bytes / (statistics.mean(t_quant) * 1e-3) / 1e9,
+        "quant_hbm_frac": quant_bytes / (statistics.mean(t_quant) * 1e-3) / 1e9 / hbm,
+        "exp2_bound": {"exp2_per_step": exp2_count, "mufu_ex2_per_clk_sm": _EX2_PER_CLK_SM,
+                       "ms": exp2_ms, "vs_tensor_bound_ms": flops / (peak * 1e12) * 1e3},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "traffic": None if traffic is None else traffic,

@@ -80,18 +80,39 @@ __device__ __forceinline__ float int8_code(float x, float s, float inv) {
   return fminf(fmaxf(n, -127.0f), 127.0f);
 }
 
-// Branch-free form for the streaming kernels: n = rne(x * inv) via one FMA
-// with the 1.5 * 2^23 rounding constant, and `exact` set when the exact
-// product x * inv lies within 2^-14 of a half-integer (then x / s, which is
-// within 1.2e-5 of that product, may round the other way: the caller redoes
-// those few elements with the division). |n| <= 127 needs no clamp: x / s
-// never exceeds amax / s = 127 (1 + 2^-23).
-__device__ __forceinline__ float int8_code_fast(float x, float inv, bool& exact) {
-  const float t = __fmaf_rn(x, inv, 12582912.0f);
-  const float n = __fsub_rn(t, 12582912.0f);
-  const float d = __fmaf_rn(x, inv, -n);  // exact residual of the product
-  exact |= !(fabsf(d) <= 0.5f - 0x1p-14f);
-  return n;
+// Running maximum of |x| over packed BF16 pairs (exact: a maximum of BF16
+// values; NaN inputs are passed over as in a scalar fmax).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w & 0x7FFF7FFFu));
+  return r;
+}
+__device__ __forceinline__ float bf16x2_hmax(uint32_t m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
+
+// INT8 codes of eight BF16 values (one 16-byte row chunk) at inv = 1/s, as
+// exact FP16 pairs, two lanes at a time (packed FP32x2 FMA / add): n =
+// rne(x * inv) via one FMA with the 1.5 * 2^23 rounding constant, and the
+// exact residual d = x * inv - n. `dmax` keeps the largest |d|: when it
+// comes within 2^-14 of 1/2, x / s (within 1.2e-5 of the product) may round
+// the other way and the caller redoes the chunk with the division. |n| <=
+// 127 needs no clamp: x / s never exceeds amax / s = 127 (1 + 2^-23).
+__device__ __forceinline__ uint4 int8_codes8(const uint4& raw, float inv, float& dmax) {
+  float f[8];
+  unpack8(raw, f);
+  const float2 inv2 = make_float2(inv, inv);
+  const float2 mag = make_float2(12582912.0f, 12582912.0f), nmag = make_float2(-12582912.0f, -12582912.0f);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 x = make_float2(f[2 * q], f[2 * q + 1]);
+    const float2 t = __ffma2_rn(x, inv2, mag);
+    const float2 n = __fadd2_rn(t, nmag);
+    const float2 d = __ffma2_rn(x, inv2, make_float2(-n.x, -n.y));
+    dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
+    const __half2 h2 = __floats2half2_rn(n.x, n.y);  // exact (|n| <= 127)
+    w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // One CTA per (128-token block, h, b); 256 threads, each owning 8 channels of
@@ -258,14 +279,16 @@ __device__ __forceinline__ uint32_t e4m3x2_div(float x0, float x1, float s, floa
   return e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
 }
 
-// Branch-free form: codes of r = x * inv shrunk and grown by 2^-21; when they
-// differ (`exact` set) the caller redoes the pair with the division.
+// Branch-free form: codes of r = x * inv shrunk and grown by 2^-21 (the
+// three products two lanes at a time); when they differ (`exact` set) the
+// caller redoes the pair with the division.
 __device__ __forceinline__ uint32_t e4m3x2_fast(float x0, float x1, float inv, bool& exact) {
-  const float r0 = __fmul_rn(x0, inv), r1 = __fmul_rn(x1, inv);
-  const uint32_t lo = e4m3x2(__fmul_rn(r0, 1.0f - 0x1p-21f), __fmul_rn(r1, 1.0f - 0x1p-21f));
-  const uint32_t hi = e4m3x2(__fmul_rn(r0, 1.0f + 0x1p-21f), __fmul_rn(r1, 1.0f + 0x1p-21f));
-  exact |= (lo != hi);
-  return lo;
+  const float2 r = __fmul2_rn(make_float2(x0, x1), make_float2(inv, inv));
+  const float2 lo = __fmul2_rn(r, make_float2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f));
+  const float2 hi = __fmul2_rn(r, make_float2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f));
+  const uint32_t clo = e4m3x2(lo.x, lo.y), chi = e4m3x2(hi.x, hi.y);
+  exact |= (clo != chi);
+  return clo;
 }
 
 // V pass 2: finalize the channel scales, quantize one 128-token tile and
@@ -429,45 +452,41 @@ __global__ void __launch_bounds__(256, 2) quantize_qk_int8_tma_kernel(
     const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
     const uint8_t* tile = ring.stage(k);
     uint4 raw[8];
-    float amax = 0.0f;
+    uint32_t am2 = 0;  // packed BF16 |x| maximum
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int rr = r0 + 16 * j;
       raw[j] = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
       if (c.blk * 128 + rr >= nv) raw[j] = make_uint4(0, 0, 0, 0);
-      float f[8];
-      unpack8(raw[j], f);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+      am2 = bf16x2_absmax(am2, raw[j].x);
+      am2 = bf16x2_absmax(am2, raw[j].y);
+      am2 = bf16x2_absmax(am2, raw[j].z);
+      am2 = bf16x2_absmax(am2, raw[j].w);
     }
-    amax = block_max_256(amax, red);
+    const float amax = block_max_256(bf16x2_hmax(am2), red);
     const float s = __fdiv_rn(amax, 127.0f);
     const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
     const int64_t bh = c.b * a.H + c.h;
     if (threadIdx.x == 0) scale[bh * nb + c.blk] = s;
+    __half* orow0 = out + (bh * Np + c.blk * 128 + r0) * 128 + col;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int64_t row = c.blk * 128 + r0 + 16 * j;
-      float f[8], n[8];
-      unpack8(raw[j], f);
-      bool redo = false;
+      float dmax = 0.0f;
+      uint4 cw = int8_codes8(raw[j], inv, dmax);
+      if (!(dmax <= 0.5f - 0x1p-14f) && s > 0.0f) {
+        float f[8];
+        unpack8(raw[j], f);
+        uint32_t w[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) n[q] = int8_code_fast(f[q], inv, redo);
-      if (s == 0.0f) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) n[q] = 0.0f;
-      } else if (redo) {  // rare: a near-tie (or a subnormal scale) in this row
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          n[q] = fminf(fmaxf(round_rne(__fdiv_rn(f[q], s)), -127.0f), 127.0f);
+        for (int q = 0; q < 4; ++q) {
+          const float n0 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q], s)), -127.0f), 127.0f);
+          const float n1 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q + 1], s)), -127.0f), 127.0f);
+          const __half2 h2 = __floats2half2_rn(n0, n1);
+          w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        cw = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const __half2 h2 = __floats2half2_rn(n[2 * q], n[2 * q + 1]);  // exact
-        w[q] = *reinterpret_cast<const uint32_t*>(&h2);
-      }
-      *reinterpret_cast<uint4*>(out + (bh * Np + row) * 128 + col) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
     }
     __syncthreads();  // stage k % kQStages (and red[]) free again
   }
@@ -496,17 +515,20 @@ __global__ void __launch_bounds__(256, 2) v_amax_tma_kernel(const __grid_constan
     const BlockCoord c = block_coord(i, a.H, nb);
     const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
     const uint8_t* tile = ring.stage(k);
-    float m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint4 m2 = make_uint4(0, 0, 0, 0);  // packed BF16 |x| maxima of 8 channels
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int rr = rg + 16 * j;
       if (c.blk * 128 + rr < nv) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2), f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) m[q] = fmaxf(m[q], fabsf(f[q]));
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
+        m2.x = bf16x2_absmax(m2.x, w.x);
+        m2.y = bf16x2_absmax(m2.y, w.y);
+        m2.z = bf16x2_absmax(m2.z, w.z);
+        m2.w = bf16x2_absmax(m2.w, w.w);
       }
     }
+    float m[8];
+    unpack8(m2, m);
 #pragma unroll
     for (int q = 0; q < 8; ++q) red[rg][col + q] = m[q];
     __syncthreads();
