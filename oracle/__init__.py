@@ -63,7 +63,8 @@ def _L():
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
         lib.oracle_bf16_from_double.argtypes = [D]
         q_args = [P, I64, I64, I64, I64, I64, I64, I64, P, P, P]
-        for name in ("oracle_quantize_int8", "oracle_quantize_v_fp8", "oracle_quantize_mxfp4"):
+        for name in ("oracle_quantize_int8", "oracle_quantize_v_fp8", "oracle_quantize_mxfp4",
+                     "oracle_quantize_fp8_qk"):
             getattr(lib, name).restype = None
             getattr(lib, name).argtypes = q_args
         lib.oracle_attention.restype = None
@@ -149,6 +150,17 @@ def quantize_v_fp8(v: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
     return v8, sv
 
 
+def quantize_fp8_qk(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
+    """E4M3 codes [B,H,Npad,D] and FP32 block scales [B,H,Npad/128] (absmax/448)."""
+    B, N, H, D, sb, sn, sh = _bnhd(x)
+    Np = pad128(N)
+    q = np.zeros((B, H, Np, D), np.uint8)
+    s = np.zeros((B, H, Np // 128), np.float32)
+    ln = _lens(lens)
+    _L().oracle_quantize_fp8_qk(_ptr(x), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(q), _ptr(s))
+    return q, s
+
+
 def quantize_mxfp4(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
     """Packed E2M1 codes [B,H,Npad,D/2] and E8M0 scales [B,H,Npad,D/32]."""
     B, N, H, D, sb, sn, sh = _bnhd(x)
@@ -164,7 +176,7 @@ def quantize_mxfp4(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
 def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: int = 128,
               softmax_scale: Optional[float] = None, k_lens=None, rows=None,
               want_weights: bool = False, nthreads: int = 0):
-    """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K. V is E4M3.
+    """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K; fmt 2: E4M3 Q/K. V is E4M3.
 
     Returns (o [B,H,nrows,D] float64, lse [B,H,nrows] float64, w or None).
     """

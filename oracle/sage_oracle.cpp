@@ -30,6 +30,10 @@
 //  - MXFP4: OCP Microscaling shared exponent floor(log2 amax) - 2 per 32
 //    channels (E8M0, clamped to [0, 254]); E2M1 elements with round to
 //    nearest even and saturation at 6.
+//  - FP8 Q/K ("new MHA v4 entrypoint ...", "Test Result": the FP8 QK^T / FP8
+//    PV row): one FP32 absmax/448 scale per 128-token block per (b,h), codes
+//    E4M3 (rne, saturating) of the FP32 quotient x/s, as for V but with the
+//    Q/K block granularity.
 #include "sage_oracle.h"
 
 #include <algorithm>
@@ -198,6 +202,34 @@ void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
   }
 }
 
+void oracle_quantize_fp8_qk(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+                            int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* q,
+                            float* scale) {
+  const int64_t Np = pad128(N), nb = Np / 128;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t nv = valid_len(lens, b, N);
+    for (int64_t h = 0; h < H; ++h)
+      for (int64_t blk = 0; blk < nb; ++blk) {
+        const int64_t n0 = blk * 128, n1 = std::min(n0 + 128, nv);
+        float amax = 0.0f;
+        for (int64_t n = n0; n < n1; ++n)
+          for (int64_t d = 0; d < D; ++d)
+            amax = std::max(amax, std::fabs(bf16_to_float(x[b * sb + n * sn + h * sh + d])));
+        const float s = amax / 448.0f;
+        scale[(b * H + h) * nb + blk] = s;
+        for (int64_t n = n0; n < n0 + 128; ++n)
+          for (int64_t d = 0; d < D; ++d) {
+            uint8_t c = 0;
+            if (n < n1 && s > 0.0f) {
+              const float r = bf16_to_float(x[b * sb + n * sn + h * sh + d]) / s;  // binary32
+              c = oracle_e4m3_encode(static_cast<double>(r));
+            }
+            q[((b * H + h) * Np + n) * D + d] = c;
+          }
+      }
+  }
+}
+
 void oracle_quantize_v_fp8(const uint16_t* v, int64_t sb, int64_t sn, int64_t sh, int64_t B,
                            int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* v8,
                            float* sv) {
@@ -296,6 +328,17 @@ void oracle_attention(int fmt, const void* q_data, const void* q_scale, const vo
           S += static_cast<int64_t>(q[d]) * static_cast<int64_t>(k[j * D + d]);
         t[j] = static_cast<double>(S) * sq * static_cast<double>(sk[j / 128]) * softmax_scale *
                kLog2e;
+      }
+    } else if (fmt == 2) {
+      const uint8_t* q = static_cast<const uint8_t*>(q_data) + (bh * Nqp + i) * D;
+      const uint8_t* k = static_cast<const uint8_t*>(k_data) + bh * Nkp * D;
+      const double sq = static_cast<const float*>(q_scale)[bh * (Nqp / 128) + i / 128];
+      const float* sk = static_cast<const float*>(k_scale) + bh * (Nkp / 128);
+      for (int64_t j = 0; j < nk; ++j) {
+        double S = 0.0;  // exact: every product of two E4M3 values and the sum fit FP64
+        for (int64_t d = 0; d < D; ++d)
+          S += oracle_e4m3_decode(q[d]) * oracle_e4m3_decode(k[j * D + d]);
+        t[j] = S * sq * static_cast<double>(sk[j / 128]) * softmax_scale * kLog2e;
       }
     } else {
       const int64_t G = D / 32;

@@ -45,11 +45,20 @@ void oracle_quantize_mxfp4(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh
                            int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* codes,
                            uint8_t* e8m0);
 
+/* FP8 E4M3 Q/K per-(b,h,128-token block) absmax: scale absmax/448 (binary32),
+ * codes E4M3 (RNE, saturating) of the binary32 quotient x/s.
+ * q: uint8 [B][H][Npad][D], padding rows 0; scale: float [B][H][Npad/128]. */
+void oracle_quantize_fp8_qk(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+                            int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* q,
+                            float* scale);
+
 /* ---- attention ---- */
 /* fmt 0: q_data/k_data are int8 [B][H][Npad][D] with float block scales
  *        [B][H][Npad/128];
  * fmt 1: q_data/k_data are MXFP4 codes [B][H][Npad][D/2] with e8m0 scales
- *        [B][H][Npad][D/32] (passed through q_scale/k_scale as bytes).
+ *        [B][H][Npad][D/32] (passed through q_scale/k_scale as bytes);
+ * fmt 2: q_data/k_data are E4M3 codes [B][H][Npad][D] with float block
+ *        scales [B][H][Npad/128].
  * V: fp8 [B][H][D][Nk_pad] + sv [B][H][D].
  * rows (nullable): the query indices to evaluate (same set for every b,h);
  * nrows = number of them (rows == NULL: all Nq).

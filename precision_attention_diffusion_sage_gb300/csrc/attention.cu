@@ -200,6 +200,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // setmaxnreg (each SM sub-partition holds one warp of every warpgroup).
 template <int NQT>
 constexpr int attn_threads() { return NQT == 1 ? 7 * 32 : 12 * 32; }
+template <int FMT, int NQT>
+__host__ __device__ constexpr bool attn_split_regs() { return FMT == 0 && NQT == 2; }
 
 template <int FMT, int NQT, int STAGES>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   constexpr int kMmaWarp = kSoftmaxWarps + 1;   // MMAs of query tile 0; owns TMEM
   constexpr int kMmaWarp1 = kSoftmaxWarps + 3;  // MMAs of query tile 1 (two tiles only)
   constexpr int kTmaVWarp = kSoftmaxWarps + 2;  // V loads
+  constexpr bool kSplitRegs = attn_split_regs<FMT, NQT>();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -328,13 +331,14 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  // With two query tiles, 384 threads launch with 168 registers each, a pool
-  // of 384 * 168 = 64512 that setmaxnreg redistributes: the two softmax
+  // INT8 with two query tiles: 384 threads launch with 168 registers each, a
+  // pool of 384 * 168 = 64512 that setmaxnreg redistributes: the two softmax
   // warpgroups take 232 and the producer/MMA warpgroup keeps 40
   // (128 * (232 + 232 + 40) = 64512). The host refuses to launch if the
-  // compiled register count would leave the pool smaller than that.
+  // compiled register count would leave the pool smaller than that. (The
+  // MXFP4 kernel, with 64-key steps, runs faster without the split.)
   if (warp >= kSoftmaxWarps) {
-    if constexpr (NQT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
+    if constexpr (kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
   // The producer and MMA warps run their loops warp-converged (every lane
   // waits; values stay warp-uniform, so the TMA coordinates and the MMA
   // descriptors live in uniform registers) and one elected lane issues.
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     drain_wait(mma_final, 0, p.status);
   }
   } else {
-      if constexpr (NQT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
+      if constexpr (kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
     // ================================================================ softmax
     const int t = warp / 4;
     const int r = static_cast<int>(threadIdx.x & 127);
@@ -861,7 +865,7 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const C
   cudaError_t e = once_per_device<kern>([]() {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
     if (r != cudaSuccess) return r;
-    if constexpr (NQT == 2) {
+    if constexpr (attn_split_regs<FMT, NQT>()) {
       // setmaxnreg can only hand out the registers the CTA was launched with.
       cudaFuncAttributes fa;
       if ((r = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return r;

@@ -163,6 +163,36 @@ def test_quantize_int8(N, lens):
                     np.testing.assert_array_equal(cc, ref)
 
 
+@pytest.mark.parametrize("N,lens", [(256, None), (300, [211]), (129, None)])
+def test_quantize_fp8_qk(N, lens):
+    """FP8 E4M3 Q/K: absmax/448 per 128-token block (binary32 division) and the
+    E4M3 encoding of the binary32 quotient, checked against numpy's division
+    and torch's float32 -> float8_e4m3fn conversion."""
+    w, q, k, v = _tiny(N=N)
+    x = bf16_bits(k)
+    codes, scale = oracle.quantize_fp8_qk(x, lens=lens)
+    xf = _f32(x)
+    B, _, H, D = xf.shape
+    nv = lens[0] if lens else N
+    assert codes.shape == (B, H, oracle.pad128(N), D) and scale.shape == (B, H, oracle.pad128(N) // 128)
+    for b in range(B):
+        for h in range(H):
+            for blk in range(scale.shape[2]):
+                n0, n1 = blk * 128, min(blk * 128 + 128, nv)
+                c = codes[b, h, blk * 128:(blk + 1) * 128]
+                assert np.all(c[max(0, n1 - n0):] == 0)            # padding / past lens
+                if n1 <= n0:
+                    assert scale[b, h, blk] == 0
+                    continue
+                blkx = xf[b, n0:n1, h, :]
+                s = np.float32(np.float32(np.abs(blkx).max()) / np.float32(448.0))
+                assert scale[b, h, blk] == s
+                ratio = (blkx / s).astype(np.float32)
+                want = torch.from_numpy(ratio).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                np.testing.assert_array_equal(c[:n1 - n0], want)
+                assert (c[:n1 - n0] & 0x7F).max() == 0x7E   # the absmax encodes to +-448
+
+
 @pytest.mark.parametrize("N,lens", [(256, None), (300, [211])])
 def test_quantize_v_fp8(N, lens):
     w, q, k, v = _tiny(N=N)
@@ -234,6 +264,11 @@ def _dequant_int8(codes, scale):
     return codes.astype(np.float64) * np.repeat(scale.astype(np.float64), 128, axis=2)[..., None]
 
 
+def _dequant_fp8qk(codes, scale):
+    tab = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    return tab[codes] * np.repeat(scale.astype(np.float64), 128, axis=2)[..., None]
+
+
 def _dequant_mxfp4(codes, e8):
     lo = codes & 0xF
     hi = codes >> 4
@@ -253,6 +288,10 @@ def _quantize_all(q, k, v, fmt, k_lens=None):
         qq, qs = oracle.quantize_int8(qb)
         kq, ks = oracle.quantize_int8(kb, lens=k_lens)
         qd, kd = _dequant_int8(qq, qs), _dequant_int8(kq, ks)
+    elif fmt == 2:
+        qq, qs = oracle.quantize_fp8_qk(qb)
+        kq, ks = oracle.quantize_fp8_qk(kb, lens=k_lens)
+        qd, kd = _dequant_fp8qk(qq, qs), _dequant_fp8qk(kq, ks)
     else:
         qq, qs = oracle.quantize_mxfp4(qb)
         kq, ks = oracle.quantize_mxfp4(kb, lens=k_lens)
@@ -261,7 +300,7 @@ def _quantize_all(q, k, v, fmt, k_lens=None):
     return (qq, qs, kq, ks, v8, sv), (qd, kd, _dequant_v(v8, sv))
 
 
-@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_attention_lse_weights_and_output(fmt):
     w, q, k, v = _tiny()
     Nq, Nk, D = w.Nq, w.Nk, w.D
@@ -369,7 +408,7 @@ def test_exact_attention_matches_torch_sdpa():
     np.testing.assert_array_equal(o2, o)
 
 
-@pytest.mark.parametrize("fmt,min_cos", [(0, 0.999), (1, 0.95)])
+@pytest.mark.parametrize("fmt,min_cos", [(0, 0.999), (1, 0.95), (2, 0.995)])
 def test_quantized_close_to_exact(fmt, min_cos):
     w, q, k, v = _tiny()
     qz, _ = _quantize_all(q, k, v, fmt)
