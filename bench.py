@@ -50,10 +50,10 @@ _EX2_PER_CLK_SM = 32
 
 def _roofline_peak(p16: float, fmt: int) -> float:
     """Tensor roofline of the attention: half the flops (Q K^T) on the 16-bit
-    pipe (INT8 codes held as FP16) or the FP4 pipe (MXFP4), half (P V) on the
-    FP8 pipe; the two halves run back to back, so the rates combine
-    harmonically."""
-    p_qk = p16 * (_FP4_RATIO if fmt == 1 else 1.0)
+    pipe (INT8 codes held as FP16), the FP4 pipe (MXFP4) or the FP8 pipe (FP8
+    Q/K), half (P V) on the FP8 pipe; the two halves run back to back, so the
+    rates combine harmonically."""
+    p_qk = p16 * {0: 1.0, 1: _FP4_RATIO, 2: _FP8_RATIO}[fmt]
     p_pv = p16 * _FP8_RATIO
     return 2.0 / (1.0 / p_qk + 1.0 / p_pv)
 
@@ -103,7 +103,7 @@ def _quant_bytes(w, Nqp: int, Nkp: int) -> float:
     as codes (FP16-held INT8, or packed E2M1 plus one E8M0 byte per 32), V read
     by both passes (channel maxima, then encoding) and written as FP8."""
     B, H, D = w.B, w.H, w.D
-    code = 2.0 if w.fmt == 0 else 0.5 + 1.0 / 32
+    code = {0: 2.0, 1: 0.5 + 1.0 / 32, 2: 1.0}[w.fmt]
     qk = (B * w.Nq * H * D * 2 + B * H * Nqp * D * code + B * w.Nk * H * D * 2
           + B * H * Nkp * D * code)
     return qk + B * w.Nk * H * D * 2 * 2 + B * H * D * Nkp
@@ -175,7 +175,7 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64, nthreads: int = 0
     def run(nh, rows):
         qb, kb, vb = (bf16_bits(t[:, :, :nh]) for t in (q, k, v))
         t0 = time.perf_counter()
-        quant_qk = oracle.quantize_int8 if w.fmt == 0 else oracle.quantize_mxfp4
+        quant_qk = {0: oracle.quantize_int8, 1: oracle.quantize_mxfp4, 2: oracle.quantize_fp8_qk}[w.fmt]
         qz = quant_qk(qb)
         kz = quant_qk(kb, lens=lens)
         vz = oracle.quantize_v_fp8(vb, lens=lens)
@@ -283,6 +283,11 @@ def main():
         qq = torch.empty((B, H, Nqp, D), dtype=torch.float16, device=dev)
         qs = torch.empty((B, H, Nqp // 128), dtype=torch.float32, device=dev)
         kq = torch.empty((B, H, Nkp, D), dtype=torch.float16, device=dev)
+        ks = torch.empty((B, H, Nkp // 128), dtype=torch.float32, device=dev)
+    elif fmt == binding.FMT_FP8:
+        qq = torch.empty((B, H, Nqp, D), dtype=torch.uint8, device=dev)
+        qs = torch.empty((B, H, Nqp // 128), dtype=torch.float32, device=dev)
+        kq = torch.empty((B, H, Nkp, D), dtype=torch.uint8, device=dev)
         ks = torch.empty((B, H, Nkp // 128), dtype=torch.float32, device=dev)
     else:
         qq = torch.empty((B, H, Nqp, D // 2), dtype=torch.uint8, device=dev)
@@ -449,16 +454,18 @@ def main():
     exp2_ms = exp2_count / (_EX2_PER_CLK_SM * 152 * mhz * 1e6) * 1e3
     nqt = 2 if Nqp >= 256 else 1
     kernel = f"sage_attn_kernel<{fmt},{nqt},{(2 if nqt == 2 else 3) if fmt == 0 else 4}>"
+    fmt_names = {0: ("int8+fp8e4m3", "int8_qk_fp8_v"), 1: ("mxfp4+fp8e4m3", "mxfp4_qk_fp8_v"),
+                 2: ("fp8e4m3", "fp8_qk_fp8_v")}
     traffic = _profiled_traffic(kernel, w.name) if args.heads == 0 else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8+fp8e4m3" if fmt == 0 else "mxfp4+fp8e4m3", "data": "synthetic",
+        "dtype": fmt_names[fmt][0], "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "D": D,
                    "k_lens": w.k_lens,
                    "heads_override": args.heads > 0,
-                   "format": "int8_qk_fp8_v" if fmt == 0 else "mxfp4_qk_fp8_v",
+                   "format": fmt_names[fmt][1],
                    "splits": nsplit,
                    "l2": "flushed between steps (256 MiB read outside the timed events)",
                    "launch": "one CUDA graph per library call (quantize Q, K, V; attention)",
@@ -479,7 +486,7 @@ def main():
                      "traffic": None if traffic is None else traffic,
                      "algorithmic_flops_per_launch": flops,
                      "peak_basis": (f"{peak_kind} bf16 {p16} TFLOP/s x nominal ratios: Q K^T "
-                                    f"{'fp16 x1' if fmt == 0 else 'fp4 x6'}, P V fp8 x2, "
+                                    f"{ {0: 'fp16 x1', 1: 'fp4 x6', 2: 'fp8 x2'}[fmt] }, P V fp8 x2, "
                                     f"harmonic combination"),
                      "kernel": kernel},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

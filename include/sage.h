@@ -62,7 +62,9 @@ typedef enum {
 /* Operand formats ("new MHA v4 entrypoint", Technical Details / Test Result). */
 typedef enum {
   SAGE_FMT_QK_INT8_V_FP8 = 0,  /* Q/K INT8 per-128-token-block scales, V FP8 E4M3 */
-  SAGE_FMT_QK_MXFP4_V_FP8 = 1  /* Q/K MXFP4 E2M1 + E8M0 per 32 channels, V FP8 E4M3 */
+  SAGE_FMT_QK_MXFP4_V_FP8 = 1, /* Q/K MXFP4 E2M1 + E8M0 per 32 channels, V FP8 E4M3 */
+  SAGE_FMT_QK_FP8_V_FP8 = 2    /* Q/K FP8 E4M3 per-128-token-block scales, V FP8 E4M3
+                                  ("Test Result": the FP8 QK^T / FP8 PV row) */
 } sage_format_t;
 
 typedef struct {
@@ -85,7 +87,10 @@ typedef struct {
  *   data  : [B][H][Npad][D/2] bytes, two E2M1 codes per byte, element 2i in
  *           the low nibble.
  *   scale : [B][H][Npad][D/32] E8M0 bytes (2^(byte-127)).
- * V (both formats):
+ * SAGE_FMT_QK_FP8_V_FP8, Q or K:
+ *   data  : [B][H][Npad][D] FP8 E4M3 codes (one byte each).
+ *   scale : [B][H][Npad/128] float, absmax/448 of each 128-token block.
+ * V (every format):
  *   data  : [B][H][D][Npad] FP8 E4M3 codes, token-contiguous (V transposed).
  *   scale : [B][H][D] float, absmax/448 of each channel over valid tokens.
  * ------------------------------------------------------------------------- */
@@ -106,7 +111,9 @@ size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int
  * 128-token block per (b,h), codes clamp(rne(x/s), -127, 127) with an IEEE
  * FP32 division; MXFP4 reading: OCP Microscaling shared exponent
  * floor(log2 amax) - 2 per 32 channels, E2M1 codes rounded to nearest even
- * with saturation at 6).
+ * with saturation at 6; FP8 reading: one FP32 scale absmax/448 per 128-token
+ * block per (b,h), codes E4M3 (round to nearest even, saturating) of the
+ * IEEE FP32 quotient x/s).
  *   x       : BF16 [B][N][H][D] with strides xs.
  *   lens    : nullable int32 [B] device array of valid token counts
  *             (0 <= lens[b] <= N); tokens >= lens[b] are excluded from the
@@ -160,7 +167,9 @@ typedef struct {
  * entrypoint", Motivation; "[None][feat] Add VisualGen FA4 autotuning",
  * first paragraph):
  *   t_ij  = S_ij * s_q * s_k * softmax_scale * log2(e)   (S exact integer)
- *           for SAGE_FMT_QK_INT8_V_FP8; for SAGE_FMT_QK_MXFP4_V_FP8
+ *           for SAGE_FMT_QK_INT8_V_FP8; the same with S the dot product of
+ *           the E4M3 values (FP32 accumulation) for SAGE_FMT_QK_FP8_V_FP8;
+ *           for SAGE_FMT_QK_MXFP4_V_FP8
  *           t_ij  = (sum_d q_id 2^eq k_jd 2^ek) * softmax_scale * log2(e),
  *           the E8M0 block scales eq, ek of each 32 channels applied inside
  *           the sum ("new MHA v4 entrypoint ...", Technical Details)

@@ -77,6 +77,15 @@ struct QKFormat<1> {
   static constexpr int kSfBytes = 512;
   static constexpr int kStep = 64;
 };
+// FP8 E4M3: rows of 128 one-byte codes, one 128-byte swizzled box per 128
+// rows (16 KB). S by kind::f8f6f4 (the P V kind), one softmax step per 128
+// keys; block scales as for INT8.
+template <>
+struct QKFormat<2> {
+  static constexpr int kTileBytes = 16384;
+  static constexpr int kSfBytes = 0;
+  static constexpr int kStep = 128;
+};
 
 template <int FMT, int NQT, int STAGES>
 struct SmemLayout {
@@ -103,8 +112,8 @@ struct SmemLayout {
 template <int FMT, int NQT>
 struct TmemLayout {
   static constexpr uint32_t kCols = NQT == 1 ? 256 : 512;
-  __host__ __device__ static constexpr uint32_t s(int t) { return FMT == 0 ? t * 256 : NQT * 128 + t * 64; }
-  __host__ __device__ static constexpr uint32_t o(int t) { return FMT == 0 ? t * 256 + 128 : t * 128; }
+  __host__ __device__ static constexpr uint32_t s(int t) { return FMT != 1 ? t * 256 : NQT * 128 + t * 64; }
+  __host__ __device__ static constexpr uint32_t o(int t) { return FMT != 1 ? t * 256 + 128 : t * 128; }
   __host__ __device__ static constexpr uint32_t sfq(int t) { return NQT * 192 + t * 4; }
   // K scales: two slots per query tile (each tile's MMA warp copies its own).
   __host__ __device__ static constexpr uint32_t sfk(int t, int slot) {
@@ -201,7 +210,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 template <int NQT>
 constexpr int attn_threads() { return NQT == 1 ? 7 * 32 : 12 * 32; }
 template <int FMT, int NQT>
-__host__ __device__ constexpr bool attn_split_regs() { return FMT == 0 && NQT == 2; }
+__host__ __device__ constexpr bool attn_split_regs() { return FMT != 1 && NQT == 2; }
 
 template <int FMT, int NQT, int STAGES>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
           tma_load_2d(sQ + t * 32768, &tmQ, q_full, 0, y);
           tma_load_2d(sQ + t * 32768 + 16384, &tmQ, q_full, 64, y);
         } else {
-          tma_load_2d(sQ + t * 8192, &tmQ, q_full, 0, y);
+          tma_load_2d(sQ + t * F::kTileBytes, &tmQ, q_full, 0, y);
         }
       }
     }
@@ -401,7 +410,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
           tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
           tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
         } else {
-          tma_load_2d(sK + s * 8192, &tmK, &k_full[s], 0, yk);
+          tma_load_2d(sK + s * F::kTileBytes, &tmK, &k_full[s], 0, yk);
         }
       }
       __syncwarp();
@@ -475,6 +484,14 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
             const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
             mma_f16_ss_lo(d_s, q_lo + off, ka + off, kIdescS, k > 0);
           }
+          mma_commit(&s_full[t]);
+        }
+      } else if constexpr (FMT == 2) {
+        // E4M3 x E4M3 over K = 128: four K = 32 slices of the 128-byte rows.
+        const uint32_t ka = k_lo + stage * 1024;
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_f8_ss_lo(d_s, q_lo + k * 2, ka + k * 2, kIdescO, k > 0);
           mma_commit(&s_full[t]);
         }
       } else {
@@ -590,12 +607,12 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     const uint32_t tO = tbase + lane_base + TM::o(t);
     const int64_t qt = static_cast<int64_t>(blockIdx.x) * NQT + t;
     const int64_t row = qt * 128 + r;
-    // INT8: logit multiplier s_q s_k softmax_scale log2(e) per K tile. MXFP4:
+    // INT8 / FP8: logit multiplier s_q s_k softmax_scale log2(e) per K tile. MXFP4:
     // the block scales are inside S already, the multiplier is constant.
     float alpha_q = p.scale_log2;
     const float* kscale = nullptr;
     float sk_next = 1.0f;  // K block scale, loaded one tile ahead
-    if constexpr (FMT == 0) {
+    if constexpr (FMT != 1) {
       const float sq = qt < p.nbq ? __ldg(&p.q_scale[bh * p.nbq + qt]) : 0.0f;
       alpha_q = sq * p.scale_log2;
       kscale = p.k_scale + bh * p.nbk;
@@ -613,7 +630,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       const int iu = u / kSteps;
       const int hu = u & (kSteps - 1);
       const int j = j0 + iu;
-      if constexpr (FMT == 0) {
+      if constexpr (FMT != 1) {
         sk = sk_next;
         if (iu + 1 < niter) sk_next = __ldg(&kscale[j + 1]);
       }
@@ -908,6 +925,11 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
                           CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128, k_rows, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B);
+  else if (a.fmt == 2)  // E4M3 codes: one 128-byte row per token
+    maps_ok = make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, q_rows, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, k_rows, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
   else  // packed E2M1: one 64-byte row per token
     maps_ok = make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, q_rows, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_64B) &&
@@ -940,6 +962,9 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   if (a.fmt == 0)
     e = two ? launch_variant<0, 2, 2>(mq, mk, mv, mo, p, stream)
             : launch_variant<0, 1, 3>(mq, mk, mv, mo, p, stream);
+  else if (a.fmt == 2)
+    e = two ? launch_variant<2, 2, 4>(mq, mk, mv, mo, p, stream)
+            : launch_variant<2, 1, 4>(mq, mk, mv, mo, p, stream);
   else
     e = two ? launch_variant<1, 2, 4>(mq, mk, mv, mo, p, stream)
             : launch_variant<1, 1, 4>(mq, mk, mv, mo, p, stream);

@@ -28,7 +28,7 @@ struct AttnParams {
 };
 
 struct AttnLaunch {
-  int fmt;        // 0: INT8 Q/K, 1: MXFP4 Q/K
+  int fmt;        // 0: INT8 Q/K, 1: MXFP4 Q/K, 2: FP8 E4M3 Q/K
   const void* q;  // INT8: FP16-held codes [B][H][Nq_pad][128]; MXFP4: packed E2M1 [B][H][Nq_pad][64]
   const void* k;  // same layout with Nk_pad
   const void* v;  // FP8 [B][H][128][Nk_pad]

@@ -48,12 +48,13 @@ struct QuantQKArgs {
   int64_t sb, sn, sh;
   int64_t B, N, H;
   const int32_t* lens;
-  void* out;      // fp16 codes or packed e2m1
-  void* scale;    // float scales or e8m0 bytes
+  void* out;      // fp16-held int8 codes, e4m3 codes or packed e2m1
+  void* scale;    // float block scales or e8m0 bytes
   int* status;
 };
 cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s);
 cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s);
+cudaError_t launch_quantize_qk_fp8(const QuantQKArgs& a, cudaStream_t s);
 
 struct QuantVArgs {
   const uint16_t* v;

@@ -117,7 +117,58 @@ __device__ __forceinline__ uint4 int8_codes8(const uint4& raw, float inv, float&
 
 // One CTA per (128-token block, h, b); 256 threads, each owning 8 channels of
 // 8 token rows.
-__global__ void __launch_bounds__(256) quantize_qk_int8_kernel(QuantQKArgs a) {
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes of x / s (IEEE binary32 quotient) for s > 0, inv = 1/s.
+// r = x * inv is within 1.5 ulp of the quotient; when the codes of r shrunk
+// and grown by 2^-21 agree, every value in between (the quotient included)
+// has that code; otherwise the exact divisions decide.
+__device__ __forceinline__ uint32_t e4m3x2_div(float x0, float x1, float s, float inv) {
+  const float r0 = __fmul_rn(x0, inv), r1 = __fmul_rn(x1, inv);
+  const uint32_t lo = e4m3x2(__fmul_rn(r0, 1.0f - 0x1p-21f), __fmul_rn(r1, 1.0f - 0x1p-21f));
+  const uint32_t hi = e4m3x2(__fmul_rn(r0, 1.0f + 0x1p-21f), __fmul_rn(r1, 1.0f + 0x1p-21f));
+  if (lo == hi && inv < INFINITY) return lo;  // (1/s overflows only for a subnormal s)
+  return e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+}
+
+// Branch-free form: codes of r = x * inv shrunk and grown by 2^-21 (the
+// three products two lanes at a time); when they differ (`exact` set) the
+// caller redoes the pair with the division.
+__device__ __forceinline__ uint32_t e4m3x2_fast(float x0, float x1, float inv, bool& exact) {
+  const float2 r = __fmul2_rn(make_float2(x0, x1), make_float2(inv, inv));
+  const float2 lo = __fmul2_rn(r, make_float2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f));
+  const float2 hi = __fmul2_rn(r, make_float2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f));
+  const uint32_t clo = e4m3x2(lo.x, lo.y), chi = e4m3x2(hi.x, hi.y);
+  exact |= (clo != chi);
+  return clo;
+}
+
+// E4M3 codes of eight BF16 values (one row chunk) at scale s > 0, inv = 1/s,
+// eight bytes (element i in byte i): the codes of the IEEE binary32 quotients
+// x / s, exact as in e4m3x2_fast (the rare bracketed pairs, or a subnormal
+// s whose reciprocal overflows, take the divisions).
+__device__ __forceinline__ uint2 fp8_codes8(const uint4& raw, float s, float inv) {
+  float f[8];
+  unpack8(raw, f);
+  bool exact = !(inv < INFINITY);
+  uint32_t c[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) c[q] = e4m3x2_fast(f[2 * q], f[2 * q + 1], inv, exact);
+  if (exact) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = e4m3x2(__fdiv_rn(f[2 * q], s), __fdiv_rn(f[2 * q + 1], s));
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// CODE 0: INT8 codes held as FP16 (absmax/127); CODE 1: FP8 E4M3 codes
+// (absmax/448), one byte each.
+template <int CODE>
+__global__ void __launch_bounds__(256) quantize_qk_block_kernel(QuantQKArgs a) {
   __shared__ float red[8];
   const int64_t h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
   const int64_t Np = pad128(a.N), nb = Np / 128;
@@ -140,28 +191,34 @@ __global__ void __launch_bounds__(256) quantize_qk_int8_kernel(QuantQKArgs a) {
     }
   }
   amax = block_max_256(amax, red);
-  const float s = __fdiv_rn(amax, 127.0f);
+  const float s = __fdiv_rn(amax, CODE == 0 ? 127.0f : 448.0f);
   const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
   const int64_t bh = b * a.H + h;
   if (threadIdx.x == 0) static_cast<float*>(a.scale)[bh * nb + blk] = s;
-  __half* out = static_cast<__half*>(a.out);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t n = blk * 128 + r0 + i * 16;
-    float f[8];
-    unpack8(raw[i], f);
-    uint32_t w[4];
+    if constexpr (CODE == 0) {
+      float f[8];
+      unpack8(raw[i], f);
+      uint32_t w[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float c0 = 0.0f, c1 = 0.0f;
-      if (n < nv && s > 0.0f) {
-        c0 = int8_code(f[2 * k], s, inv);
-        c1 = int8_code(f[2 * k + 1], s, inv);
+      for (int k = 0; k < 4; ++k) {
+        float c0 = 0.0f, c1 = 0.0f;
+        if (n < nv && s > 0.0f) {
+          c0 = int8_code(f[2 * k], s, inv);
+          c1 = int8_code(f[2 * k + 1], s, inv);
+        }
+        const __half2 h2 = __floats2half2_rn(c0, c1);  // exact: |c| <= 127
+        w[k] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      const __half2 h2 = __floats2half2_rn(c0, c1);  // exact: |c| <= 127
-      w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+      __half* out = static_cast<__half*>(a.out);
+      *reinterpret_cast<uint4*>(out + (bh * Np + n) * 128 + col) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      const uint2 c = (n < nv && s > 0.0f) ? fp8_codes8(raw[i], s, inv) : make_uint2(0, 0);
+      uint8_t* out = static_cast<uint8_t*>(a.out);
+      *reinterpret_cast<uint2*>(out + (bh * Np + n) * 128 + col) = c;
     }
-    *reinterpret_cast<uint4*>(out + (bh * Np + n) * 128 + col) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -259,36 +316,6 @@ __global__ void __launch_bounds__(256) v_amax_kernel(QuantVArgs a) {
     for (int g = 1; g < 16; ++g) r = fmaxf(r, red[g][threadIdx.x]);
     if (r > 0.0f) atomicMax(&a.amax[(b * a.H + h) * 128 + threadIdx.x], __float_as_int(r));
   }
-}
-
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Two E4M3 codes of x / s (IEEE binary32 quotient) for s > 0, inv = 1/s.
-// r = x * inv is within 1.5 ulp of the quotient; when the codes of r shrunk
-// and grown by 2^-21 agree, every value in between (the quotient included)
-// has that code; otherwise the exact divisions decide.
-__device__ __forceinline__ uint32_t e4m3x2_div(float x0, float x1, float s, float inv) {
-  const float r0 = __fmul_rn(x0, inv), r1 = __fmul_rn(x1, inv);
-  const uint32_t lo = e4m3x2(__fmul_rn(r0, 1.0f - 0x1p-21f), __fmul_rn(r1, 1.0f - 0x1p-21f));
-  const uint32_t hi = e4m3x2(__fmul_rn(r0, 1.0f + 0x1p-21f), __fmul_rn(r1, 1.0f + 0x1p-21f));
-  if (lo == hi && inv < INFINITY) return lo;  // (1/s overflows only for a subnormal s)
-  return e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-}
-
-// Branch-free form: codes of r = x * inv shrunk and grown by 2^-21 (the
-// three products two lanes at a time); when they differ (`exact` set) the
-// caller redoes the pair with the division.
-__device__ __forceinline__ uint32_t e4m3x2_fast(float x0, float x1, float inv, bool& exact) {
-  const float2 r = __fmul2_rn(make_float2(x0, x1), make_float2(inv, inv));
-  const float2 lo = __fmul2_rn(r, make_float2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f));
-  const float2 hi = __fmul2_rn(r, make_float2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f));
-  const uint32_t clo = e4m3x2(lo.x, lo.y), chi = e4m3x2(hi.x, hi.y);
-  exact |= (clo != chi);
-  return clo;
 }
 
 // V pass 2: finalize the channel scales, quantize one 128-token tile and
@@ -427,7 +454,8 @@ struct BlockRing {
   }
 };
 
-__global__ void __launch_bounds__(256, 2) quantize_qk_int8_tma_kernel(
+template <int CODE>  // as quantize_qk_block_kernel
+__global__ void __launch_bounds__(256, 2) quantize_qk_tma_kernel(
     const __grid_constant__ CUtensorMap tmX, QuantQKArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ float red[8];
@@ -439,7 +467,7 @@ __global__ void __launch_bounds__(256, 2) quantize_qk_int8_tma_kernel(
   const int64_t Np = pad128(a.N), nb = Np / 128, total = a.B * a.H * nb;
   const int col = (threadIdx.x & 15) * 8;
   const int r0 = threadIdx.x >> 4;
-  __half* out = static_cast<__half*>(a.out);
+  __half* out = static_cast<__half*>(a.out);  // CODE 0
   float* scale = static_cast<float*>(a.scale);
   for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmX, k, total, a.H, nb);
   int64_t k = 0;
@@ -464,29 +492,38 @@ __global__ void __launch_bounds__(256, 2) quantize_qk_int8_tma_kernel(
       am2 = bf16x2_absmax(am2, raw[j].w);
     }
     const float amax = block_max_256(bf16x2_hmax(am2), red);
-    const float s = __fdiv_rn(amax, 127.0f);
+    const float s = __fdiv_rn(amax, CODE == 0 ? 127.0f : 448.0f);
     const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
     const int64_t bh = c.b * a.H + c.h;
     if (threadIdx.x == 0) scale[bh * nb + c.blk] = s;
-    __half* orow0 = out + (bh * Np + c.blk * 128 + r0) * 128 + col;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float dmax = 0.0f;
-      uint4 cw = int8_codes8(raw[j], inv, dmax);
-      if (!(dmax <= 0.5f - 0x1p-14f) && s > 0.0f) {
-        float f[8];
-        unpack8(raw[j], f);
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float n0 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q], s)), -127.0f), 127.0f);
-          const float n1 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q + 1], s)), -127.0f), 127.0f);
-          const __half2 h2 = __floats2half2_rn(n0, n1);
-          w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+    if constexpr (CODE == 0) {
+      __half* orow0 = out + (bh * Np + c.blk * 128 + r0) * 128 + col;
+  #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float dmax = 0.0f;
+        uint4 cw = int8_codes8(raw[j], inv, dmax);
+        if (!(dmax <= 0.5f - 0x1p-14f) && s > 0.0f) {
+          float f[8];
+          unpack8(raw[j], f);
+          uint32_t w[4];
+  #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float n0 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q], s)), -127.0f), 127.0f);
+            const float n1 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q + 1], s)), -127.0f), 127.0f);
+            const __half2 h2 = __floats2half2_rn(n0, n1);
+            w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          cw = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        cw = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
       }
-      *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
+    } else {
+      uint8_t* orow0 = static_cast<uint8_t*>(a.out) + (bh * Np + c.blk * 128 + r0) * 128 + col;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint2 cw = s > 0.0f ? fp8_codes8(raw[j], s, inv) : make_uint2(0, 0);
+        *reinterpret_cast<uint2*>(orow0 + j * 16 * 128) = cw;
+      }
     }
     __syncthreads();  // stage k % kQStages (and red[]) free again
   }
@@ -673,20 +710,29 @@ cudaError_t set_smem(int bytes) {
 // The TMA-fed persistent kernels serve every input a tensor map can describe
 // (positive strides); the direct-load kernels (grid with the head index
 // fastest, so concurrent CTAs read contiguous token rows) serve the rest.
-cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s) {
+template <int CODE>
+cudaError_t launch_quantize_qk_block(const QuantQKArgs& a, cudaStream_t s) {
   CUtensorMap m;
   if (bnhd_map(&m, a.x, a.sb, a.sn, a.sh, a.B, a.N, a.H)) {
     const int smem = kQStages * kBlockBytes + kQStages * 8 + 128;
-    cudaError_t e = set_smem<quantize_qk_int8_tma_kernel>(smem);
+    cudaError_t e = set_smem<quantize_qk_tma_kernel<CODE>>(smem);
     if (e != cudaSuccess) return e;
     const int64_t blocks = a.B * a.H * (pad128(a.N) / 128);
-    quantize_qk_int8_tma_kernel<<<persistent_grid(blocks), 256, smem, s>>>(m, a);
+    quantize_qk_tma_kernel<CODE><<<persistent_grid(blocks), 256, smem, s>>>(m, a);
     return cudaGetLastError();
   }
   dim3 grid(static_cast<unsigned>(a.H), static_cast<unsigned>(pad128(a.N) / 128),
             static_cast<unsigned>(a.B));
-  quantize_qk_int8_kernel<<<grid, 256, 0, s>>>(a);
+  quantize_qk_block_kernel<CODE><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s) {
+  return launch_quantize_qk_block<0>(a, s);
+}
+
+cudaError_t launch_quantize_qk_fp8(const QuantQKArgs& a, cudaStream_t s) {
+  return launch_quantize_qk_block<1>(a, s);
 }
 
 cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s) {

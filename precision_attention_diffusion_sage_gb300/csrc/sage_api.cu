@@ -59,6 +59,11 @@ sage_status_t check_shape(int64_t B, int64_t N, int64_t H, int64_t D) {
 
 sage_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA; }
 
+bool known_format(sage_format_t fmt) {
+  return fmt == SAGE_FMT_QK_INT8_V_FP8 || fmt == SAGE_FMT_QK_MXFP4_V_FP8 ||
+         fmt == SAGE_FMT_QK_FP8_V_FP8;
+}
+
 int64_t resolve_splits(int num_splits, int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
   if (num_splits > 0) return num_splits;
   return attn_auto_splits(B, H, Nq, Nk);
@@ -74,13 +79,15 @@ extern "C" {
 size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, int64_t H,
                             int64_t D) {
   if (check_shape(B, N, H, D) != SAGE_OK) return 0;
-  if (fmt != SAGE_FMT_QK_INT8_V_FP8 && fmt != SAGE_FMT_QK_MXFP4_V_FP8) return 0;
+  if (!known_format(fmt)) return 0;
   const int64_t Np = pad128(N);
+  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8;
   switch (which) {
-    case 0:
-      return static_cast<size_t>(fmt == SAGE_FMT_QK_INT8_V_FP8 ? B * H * Np * D * 2 : B * H * Np * D / 2);
+    case 0:  // FP16-held INT8 codes: 2 B, E4M3: 1 B, packed E2M1: 1/2 B per element
+      return static_cast<size_t>(mx ? B * H * Np * D / 2
+                                    : B * H * Np * D * (fmt == SAGE_FMT_QK_INT8_V_FP8 ? 2 : 1));
     case 1:
-      return static_cast<size_t>(fmt == SAGE_FMT_QK_INT8_V_FP8 ? B * H * (Np / 128) * 4 : B * H * Np * (D / 32));
+      return static_cast<size_t>(mx ? B * H * Np * (D / 32) : B * H * (Np / 128) * 4);
     case 2:
       return static_cast<size_t>(B * H * D * Np);
     case 3:
@@ -92,7 +99,7 @@ size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, 
 
 size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int64_t Nq,
                             int64_t Nk, int64_t D, int num_splits) {
-  if (fmt != SAGE_FMT_QK_INT8_V_FP8 && fmt != SAGE_FMT_QK_MXFP4_V_FP8) return 0;
+  if (!known_format(fmt)) return 0;
   switch (op) {
     case 0:
       return 0;
@@ -113,7 +120,7 @@ size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int
 sage_status_t sage_quantize_qk(sage_format_t fmt, const void* x, sage_strides_t xs, int64_t B,
                                int64_t N, int64_t H, int64_t D, const int32_t* lens, void* x_q,
                                void* x_scale, sage_stream_t stream) {
-  if (fmt != SAGE_FMT_QK_INT8_V_FP8 && fmt != SAGE_FMT_QK_MXFP4_V_FP8) return SAGE_ERR_UNSUPPORTED;
+  if (!known_format(fmt)) return SAGE_ERR_UNSUPPORTED;
   sage_status_t st = check_shape(B, N, H, D);
   if (st != SAGE_OK) return st;
   if (!x || !x_q || !x_scale || !aligned(x, 16) || !aligned(x_q, 16) || !aligned(x_scale, 4) ||
@@ -124,8 +131,11 @@ sage_status_t sage_quantize_qk(sage_format_t fmt, const void* x, sage_strides_t 
   QuantQKArgs a{static_cast<const uint16_t*>(x), xs.b, xs.n, xs.h, B, N, H, lens, x_q, x_scale,
                 status};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return from_cuda(fmt == SAGE_FMT_QK_INT8_V_FP8 ? launch_quantize_qk_int8(a, s)
-                                                 : launch_quantize_qk_mxfp4(a, s));
+  switch (fmt) {
+    case SAGE_FMT_QK_INT8_V_FP8: return from_cuda(launch_quantize_qk_int8(a, s));
+    case SAGE_FMT_QK_FP8_V_FP8: return from_cuda(launch_quantize_qk_fp8(a, s));
+    default: return from_cuda(launch_quantize_qk_mxfp4(a, s));
+  }
 }
 
 sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64_t N, int64_t H,
@@ -152,7 +162,7 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
                             void* o, sage_strides_t os, float* lse, void* workspace,
                             size_t ws_bytes, const sage_attn_options_t* opts,
                             sage_stream_t stream) {
-  if (fmt != SAGE_FMT_QK_INT8_V_FP8 && fmt != SAGE_FMT_QK_MXFP4_V_FP8) return SAGE_ERR_UNSUPPORTED;
+  if (!known_format(fmt)) return SAGE_ERR_UNSUPPORTED;
   if (causal != 0) return SAGE_ERR_UNSUPPORTED;
   sage_status_t st = check_shape(B, Nq, H, D);
   if (st != SAGE_OK) return st;
@@ -174,7 +184,7 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   const float c = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8;
   AttnLaunch a;
-  a.fmt = mx ? 1 : 0;
+  a.fmt = mx ? 1 : (fmt == SAGE_FMT_QK_FP8_V_FP8 ? 2 : 0);
   a.q = q_q;
   a.k = k_q;
   a.v = v_q;

@@ -23,7 +23,7 @@ class Workload:
     Nq: int
     Nk: int
     seed: int
-    fmt: int = 0                      # 0: INT8 Q/K, 1: MXFP4 Q/K (V is FP8 in both)
+    fmt: int = 0                      # 0: INT8 Q/K, 1: MXFP4 Q/K, 2: FP8 Q/K (V is FP8)
     structure: str = "plain"
     k_lens: Optional[List[int]] = field(default=None)
     D: int = 128
@@ -51,6 +51,11 @@ WORKLOADS = {
     "cross_ragged": Workload("cross_ragged", 2, 24, 8192, 512, seed=4, k_lens=[512, 300]),
     "cross_ragged_mxfp4": Workload("cross_ragged_mxfp4", 2, 24, 8192, 512, seed=4, fmt=1,
                                    k_lens=[512, 300]),
+    # FP8 E4M3 Q/K (the pages' FP8 QK^T / FP8 PV format) on the image and video shapes
+    "image_dit_fp8": Workload("image_dit_fp8", 1, 24, 4608, 4608, seed=1, fmt=2,
+                              structure="k_channels_x8"),
+    "video_dit_fp8": Workload("video_dit_fp8", 1, 40, 14040, 14040, seed=2, fmt=2,
+                              structure="k_mean"),
 }
 
 

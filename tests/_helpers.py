@@ -22,6 +22,9 @@ def oracle_quantize(fmt, q, k, v, k_lens=None):
     if fmt == 0:
         qz = oracle.quantize_int8(qb)
         kz = oracle.quantize_int8(kb, lens=k_lens)
+    elif fmt == 2:
+        qz = oracle.quantize_fp8_qk(qb)
+        kz = oracle.quantize_fp8_qk(kb, lens=k_lens)
     else:
         qz = oracle.quantize_mxfp4(qb)
         kz = oracle.quantize_mxfp4(kb, lens=k_lens)
@@ -39,7 +42,7 @@ def gpu_codes(fmt, x_q):
 def assert_qk_equal(fmt, gpu_q, gpu_s, ref_q, ref_s):
     np.testing.assert_array_equal(gpu_codes(fmt, gpu_q), ref_q)
     gs = gpu_s.cpu().numpy()
-    if fmt == 0:
+    if fmt in (0, 2):  # float block scales, compared bit for bit
         np.testing.assert_array_equal(gs.view(np.uint32), ref_s.view(np.uint32))
     else:
         np.testing.assert_array_equal(gs, ref_s)

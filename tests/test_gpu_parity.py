@@ -346,3 +346,77 @@ def test_full_size_workload_mxfp4(name, heads):
     rows = _sample_rows(w.Nq)
     ro, rl = _oracle_attention(1, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
     assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+
+
+# ------------------------------------------------------------------ FP8 E4M3 Q/K attention
+@pytest.mark.parametrize("N,lens", [(256, None), (1, None), (129, None), (300, [211])])
+def test_quantize_fp8_qk_bitexact(N, lens):
+    w, q, k, v = _small(1, 3, N, N, seed=60 + N)
+    gq, gs = binding.sage_quantize_qk(k, 2, lens=lens)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_fp8_qk(bf16_bits(k), lens=lens)
+    assert_qk_equal(2, gq, gs, rq, rs)
+
+
+def test_quantize_fp8_qk_near_ties_bitexact():
+    """Values whose quotient x/s lands next to an E4M3 rounding boundary:
+    the fast product path must defer to the exact division there."""
+    g = torch.Generator().manual_seed(61)
+    x = torch.randn(1, 128, 1, 128, generator=g)
+    x[0, 0, 0, 0] = 448.0 / 64                       # amax: s = 7/448 = 2^-6
+    mids = torch.tensor([1.0625, 1.1875, 1.3125, 2.125, 3.375, 0.015625 * 1.5, 20.0, 208.0])
+    x[0, 1, 0, :8] = mids * 2.0 ** -6                 # exact midpoints between E4M3 values
+    x[0, 2, 0, :8] = mids * 2.0 ** -6 * (1 + 2.0 ** -7)  # just above (BF16 step)
+    x = x.to(torch.bfloat16)
+    gq, gs = binding.sage_quantize_qk(x.cuda(), 2)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_fp8_qk(bf16_bits(x))
+    assert_qk_equal(2, gq, gs, rq, rs)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (127, 127), (129, 300), (256, 384), (513, 77),
+                                   (128, 1000)])
+def test_attention_fp8_ragged_tails(Nq, Nk):
+    w, q, k, v = _small(1, 2, Nq, Nk, seed=Nq * 3 + Nk, structure="k_offset_std2")
+    (qq, qs), (kq, ks), _, o, lse = _run_gpu(2, q, k, v)
+    qz, kz, vz = oracle_quantize(2, q, k, v)
+    assert_qk_equal(2, qq, qs, *qz)
+    assert_qk_equal(2, kq, ks, *kz)
+    ro, rl = _oracle_attention(2, qz, kz, vz, Nq, Nk)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_fp8_cross_ragged_and_splits():
+    w, q, k, v = _small(2, 2, 300, 512, seed=62)
+    lens = [512, 300]
+    qz, kz, vz = oracle_quantize(2, q, k, v, k_lens=lens)
+    ro, rl = _oracle_attention(2, qz, kz, vz, 300, 512, k_lens=lens)
+    for splits in (1, 3):
+        _, _, _, o, lse = _run_gpu(2, q, k, v, k_lens=lens, num_splits=splits)
+        assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_fp8_deterministic():
+    w = WORKLOADS["image_dit_fp8"]
+    q, k, v = make_qkv(w, device="cuda")
+    o1, l1 = binding.sage_attention(q, k, v, fmt=2)
+    for _ in range(2):
+        o2, l2 = binding.sage_attention(q, k, v, fmt=2)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+
+
+@pytest.mark.parametrize("name,heads", [("image_dit_fp8", [0, 5, 23]), ("video_dit_fp8", [0, 39])])
+def test_full_size_workload_fp8(name, heads):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(2, q, k, v, k_lens=w.k_lens)
+    sub = lambda t: t[:, :, heads]  # noqa: E731  head slice of [B, N, H, D]
+    qz, kz, vz = oracle_quantize(2, sub(q), sub(k), sub(v), k_lens=w.k_lens)
+    assert_qk_equal(2, qq[:, heads], qs[:, heads], *qz)
+    assert_qk_equal(2, kq[:, heads], ks[:, heads], *kz)
+    assert_v_equal(vq[:, heads], vs[:, heads], *vz)
+    rows = _sample_rows(w.Nq)
+    ro, rl = _oracle_attention(2, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
+    assert_attention_close(o[:, :, heads], lse[:, heads], ro, rl, rows=rows)
