@@ -64,9 +64,11 @@ def _L():
         lib.oracle_bf16_from_double.argtypes = [D]
         q_args = [P, I64, I64, I64, I64, I64, I64, I64, P, P, P]
         for name in ("oracle_quantize_int8", "oracle_quantize_v_fp8", "oracle_quantize_mxfp4",
-                     "oracle_quantize_fp8_qk"):
+                     "oracle_quantize_fp8_qk", "oracle_quantize_mxfp4_hadamard"):
             getattr(lib, name).restype = None
             getattr(lib, name).argtypes = q_args
+        lib.oracle_fwht128.restype = None
+        lib.oracle_fwht128.argtypes = [P, P, I64]
         lib.oracle_attention.restype = None
         lib.oracle_attention.argtypes = [I32, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, D,
                                          P, I64, P, P, P, I32]
@@ -148,6 +150,27 @@ def quantize_v_fp8(v: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
     ln = _lens(lens)
     _L().oracle_quantize_v_fp8(_ptr(v), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(v8), _ptr(sv))
     return v8, sv
+
+
+def fwht128(x: np.ndarray) -> np.ndarray:
+    """Binary32 fast Walsh-Hadamard transform of the last axis (length 128)."""
+    xin = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(xin)
+    _L().oracle_fwht128(_ptr(xin), _ptr(out), xin.size // 128)
+    return out
+
+
+def quantize_mxfp4_hadamard(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
+    """MXFP4 codes [B,H,Npad,D/2] and E8M0 scales [B,H,Npad,D/32] of the
+    Hadamard-rotated rows; pair with softmax_scale / 128 in attention()."""
+    B, N, H, D, sb, sn, sh = _bnhd(x)
+    Np = pad128(N)
+    c = np.zeros((B, H, Np, D // 2), np.uint8)
+    e = np.zeros((B, H, Np, D // 32), np.uint8)
+    ln = _lens(lens)
+    _L().oracle_quantize_mxfp4_hadamard(_ptr(x), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(c),
+                                        _ptr(e))
+    return c, e
 
 
 def quantize_fp8_qk(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:

@@ -30,6 +30,12 @@
 //  - MXFP4: OCP Microscaling shared exponent floor(log2 amax) - 2 per 32
 //    channels (E8M0, clamped to [0, 254]); E2M1 elements with round to
 //    nearest even and saturation at 6.
+//  - Hadamard-rotated MXFP4 ("new MHA v4 entrypoint ...", Q/K rotation before
+//    MXFP4 quantization): each 128-channel row times the unnormalized
+//    Sylvester Hadamard matrix, computed as the fast Walsh-Hadamard transform
+//    in binary32 with the butterfly spans 1, 2, 4, ..., 64 in that order, then
+//    the MXFP4 rule on the rotated values; (QH)(KH)^T = 128 QK^T, so the
+//    logit multiplier carries a factor 1/128.
 //  - FP8 Q/K ("new MHA v4 entrypoint ...", "Test Result": the FP8 QK^T / FP8
 //    PV row): one FP32 absmax/448 scale per 128-token block per (b,h), codes
 //    E4M3 (rne, saturating) of the FP32 quotient x/s, as for V but with the
@@ -199,6 +205,60 @@ void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
           }
       }
     }
+  }
+}
+
+void oracle_fwht128(const float* in, float* out, int64_t rows) {
+  for (int64_t r = 0; r < rows; ++r) {
+    float x[128];
+    for (int i = 0; i < 128; ++i) x[i] = in[r * 128 + i];
+    for (int h = 1; h < 128; h *= 2)
+      for (int i = 0; i < 128; ++i)
+        if ((i & h) == 0) {
+          const float a = x[i], b = x[i + h];
+          x[i] = a + b;  // binary32, round to nearest even
+          x[i + h] = a - b;
+        }
+    for (int i = 0; i < 128; ++i) out[r * 128 + i] = x[i];
+  }
+}
+
+void oracle_quantize_mxfp4_hadamard(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
+                                    int64_t B, int64_t N, int64_t H, int64_t D,
+                                    const int32_t* lens, uint8_t* codes, uint8_t* e8m0) {
+  const int64_t Np = pad128(N), G = D / 32;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t nv = valid_len(lens, b, N);
+    for (int64_t h = 0; h < H; ++h)
+      for (int64_t n = 0; n < Np; ++n) {
+        uint8_t* crow = codes + ((b * H + h) * Np + n) * (D / 2);
+        uint8_t* srow = e8m0 + ((b * H + h) * Np + n) * G;
+        if (n >= nv) {
+          std::fill(crow, crow + D / 2, 0);
+          std::fill(srow, srow + G, 0);
+          continue;
+        }
+        float row[128], rot[128];
+        for (int64_t d = 0; d < D; ++d) row[d] = bf16_to_float(x[b * sb + n * sn + h * sh + d]);
+        oracle_fwht128(row, rot, 1);
+        for (int64_t g = 0; g < G; ++g) {
+          float amax = 0.0f;
+          for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(rot[g * 32 + i]));
+          int byte = 0;
+          if (amax > 0.0f) {
+            int k;
+            std::frexp(static_cast<double>(amax), &k);  // floor(log2 amax) = k - 1
+            byte = std::min(254, std::max(0, (k - 1) - 2 + 127));
+          }
+          srow[g] = static_cast<uint8_t>(byte);
+          const double X = std::ldexp(1.0, byte - 127);
+          for (int i = 0; i < 32; i += 2) {
+            const uint8_t lo = oracle_e2m1_encode(static_cast<double>(rot[g * 32 + i]) / X);
+            const uint8_t hi = oracle_e2m1_encode(static_cast<double>(rot[g * 32 + i + 1]) / X);
+            crow[g * 16 + i / 2] = static_cast<uint8_t>(lo | (hi << 4));
+          }
+        }
+      }
   }
 }
 

@@ -45,6 +45,17 @@ void oracle_quantize_mxfp4(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh
                            int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* codes,
                            uint8_t* e8m0);
 
+/* Fast Walsh-Hadamard transform of `rows` rows of 128 binary32 values (the
+ * unnormalized Sylvester Hadamard product x H), butterflies (a, b) -> (a + b,
+ * a - b) in binary32 with spans 1, 2, 4, ..., 64 in that order. */
+void oracle_fwht128(const float* in, float* out, int64_t rows);
+/* MXFP4 quantization (as oracle_quantize_mxfp4) of the Hadamard-rotated rows:
+ * each token's 128 channels (BF16 widened to binary32) through oracle_fwht128,
+ * then per 32 channels the E8M0 exponent and E2M1 codes of the rotated values.
+ * Same output layout as oracle_quantize_mxfp4. */
+void oracle_quantize_mxfp4_hadamard(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
+                                    int64_t B, int64_t N, int64_t H, int64_t D,
+                                    const int32_t* lens, uint8_t* codes, uint8_t* e8m0);
 /* FP8 E4M3 Q/K per-(b,h,128-token block) absmax: scale absmax/448 (binary32),
  * codes E4M3 (RNE, saturating) of the binary32 quotient x/s.
  * q: uint8 [B][H][Npad][D], padding rows 0; scale: float [B][H][Npad/128]. */

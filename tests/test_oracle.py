@@ -247,6 +247,92 @@ def test_quantize_mxfp4(lens):
                         assert c == (mag | (0x8 if y < 0 or (y == 0 and math.copysign(1, y) < 0) else 0))
 
 
+# ------------------------------------------------------------------ Hadamard-rotated MXFP4
+def test_fwht128_is_the_sylvester_hadamard_product():
+    """On small-integer rows every binary32 sum is exact, so the transform must
+    equal x @ H with scipy's Sylvester Hadamard matrix, and applying it twice
+    must give 128 x (H H = 128 I)."""
+    import scipy.linalg
+    rng = np.random.RandomState(3)
+    x = rng.randint(-64, 65, size=(9, 128)).astype(np.float32)
+    y = oracle.fwht128(x)
+    np.testing.assert_array_equal(y, (x.astype(np.float64) @ scipy.linalg.hadamard(128)))
+    np.testing.assert_array_equal(oracle.fwht128(y), 128.0 * x)
+
+
+def test_fwht128_rounding_bound():
+    """General BF16 rows: within the rounding of seven binary32 butterfly
+    stages of the exact product (each stage adds at most 2^-24 of the row's
+    absolute sum)."""
+    import scipy.linalg
+    w, q, k, v = _tiny()
+    x = _f32(bf16_bits(k))[0, :64, 0, :]
+    y = oracle.fwht128(x).astype(np.float64)
+    exact = x.astype(np.float64) @ scipy.linalg.hadamard(128)
+    bound = 7 * 2.0 ** -24 * np.abs(x).astype(np.float64).sum(axis=1, keepdims=True)
+    assert np.all(np.abs(y - exact) <= bound)
+    assert np.any(y != exact)                       # rounding does occur on these rows
+
+
+@pytest.mark.parametrize("lens", [None, [100]])
+def test_quantize_mxfp4_hadamard(lens):
+    """Codes and E8M0 bytes equal the MXFP4 rule applied (independently, in
+    numpy) to the rotated rows."""
+    w, q, k, v = _tiny()
+    x = bf16_bits(k)
+    codes, e8 = oracle.quantize_mxfp4_hadamard(x, lens=lens)
+    xf = _f32(x)
+    B, N, H, D = xf.shape
+    nv = lens[0] if lens else N
+    codes_tab = np.arange(8, dtype=np.uint8)
+    vals_tab = np.array(E2M1)
+    for b in range(B):
+        for h in range(H):
+            rot = oracle.fwht128(xf[b, :, h, :]).astype(np.float64)  # [N, 128]
+            for n in range(0, oracle.pad128(N), 11 if lens is None else 1):
+                if n >= nv:
+                    assert np.all(codes[b, h, n] == 0) and np.all(e8[b, h, n] == 0)
+                    continue
+                for g in range(D // 32):
+                    grp = rot[n, g * 32:(g + 1) * 32]
+                    e = int(np.floor(np.log2(np.abs(grp).max()))) - 2
+                    assert e8[b, h, n, g] == e + 127
+                    for i in range(32):
+                        c = (codes[b, h, n, g * 16 + i // 2] >> (4 * (i % 2))) & 0xF
+                        y = grp[i] / 2.0 ** e
+                        mag = _nearest_even(y, codes_tab, vals_tab, 6.0)
+                        assert c == (mag | (0x8 if y < 0 or (y == 0 and math.copysign(1, y) < 0) else 0))
+
+
+def test_hadamard_rotation_scales_logits_by_128():
+    """(QH)(KH)^T = 128 QK^T: exact on integer rows."""
+    rng = np.random.RandomState(4)
+    qi = rng.randint(-20, 21, size=(5, 128)).astype(np.float32)
+    ki = rng.randint(-20, 21, size=(7, 128)).astype(np.float32)
+    lhs = oracle.fwht128(qi).astype(np.float64) @ oracle.fwht128(ki).astype(np.float64).T
+    np.testing.assert_array_equal(lhs, 128.0 * (qi.astype(np.float64) @ ki.astype(np.float64).T))
+
+
+def test_hadamard_improves_mxfp4_accuracy():
+    """With outlier K channels (4 of 128 scaled x8, the image workload's
+    structure) the rotated MXFP4 attention (logit multiplier / 128) is closer
+    to unquantized attention than plain MXFP4: the rotation spreads each
+    outlier over all channels, so the 32-channel blocks lose less precision."""
+    w = Workload("outliers", 1, 2, 256, 256, seed=7, structure="k_channels_x8")
+    q, k, v = make_qkv(w)
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    vz = oracle.quantize_v_fp8(vb)
+    c = 1.0 / math.sqrt(128)
+    oe, _ = oracle.attention_exact(qb, kb, vb)
+    o1, _, _ = oracle.attention(1, *oracle.quantize_mxfp4(qb), *oracle.quantize_mxfp4(kb), *vz,
+                                Nq=w.Nq, Nk=w.Nk)
+    oh, _, _ = oracle.attention(1, *oracle.quantize_mxfp4_hadamard(qb),
+                                *oracle.quantize_mxfp4_hadamard(kb), *vz, Nq=w.Nq, Nk=w.Nk,
+                                softmax_scale=c / 128)
+    cos = lambda a: float((a * oe).sum() / math.sqrt((a * a).sum() * (oe * oe).sum()))  # noqa: E731
+    assert cos(oh) > cos(o1) + 0.02
+
+
 def test_mxfp4_nibble_order_and_scale_closed_form():
     x = np.zeros((1, 1, 1, 128), np.float32)
     x[0, 0, 0, 0] = 6.0 * 2.0 ** 5     # element 0 -> +6 at scale 2^5
