@@ -53,7 +53,7 @@ def _roofline_peak(p16: float, fmt: int) -> float:
     pipe (INT8 codes held as FP16), the FP4 pipe (MXFP4) or the FP8 pipe (FP8
     Q/K), half (P V) on the FP8 pipe; the two halves run back to back, so the
     rates combine harmonically."""
-    p_qk = p16 * {0: 1.0, 1: _FP4_RATIO, 2: _FP8_RATIO}[fmt]
+    p_qk = p16 * {0: 1.0, 1: _FP4_RATIO, 2: _FP8_RATIO, 3: _FP4_RATIO}[fmt]
     p_pv = p16 * _FP8_RATIO
     return 2.0 / (1.0 / p_qk + 1.0 / p_pv)
 
@@ -103,7 +103,7 @@ def _quant_bytes(w, Nqp: int, Nkp: int) -> float:
     as codes (FP16-held INT8, or packed E2M1 plus one E8M0 byte per 32), V read
     by both passes (channel maxima, then encoding) and written as FP8."""
     B, H, D = w.B, w.H, w.D
-    code = {0: 2.0, 1: 0.5 + 1.0 / 32, 2: 1.0}[w.fmt]
+    code = {0: 2.0, 1: 0.5 + 1.0 / 32, 2: 1.0, 3: 0.5 + 1.0 / 32}[w.fmt]
     qk = (B * w.Nq * H * D * 2 + B * H * Nqp * D * code + B * w.Nk * H * D * 2
           + B * H * Nkp * D * code)
     return qk + B * w.Nk * H * D * 2 * 2 + B * H * D * Nkp
@@ -175,12 +175,15 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64, nthreads: int = 0
     def run(nh, rows):
         qb, kb, vb = (bf16_bits(t[:, :, :nh]) for t in (q, k, v))
         t0 = time.perf_counter()
-        quant_qk = {0: oracle.quantize_int8, 1: oracle.quantize_mxfp4, 2: oracle.quantize_fp8_qk}[w.fmt]
+        quant_qk = {0: oracle.quantize_int8, 1: oracle.quantize_mxfp4, 2: oracle.quantize_fp8_qk,
+                    3: oracle.quantize_mxfp4_hadamard}[w.fmt]
         qz = quant_qk(qb)
         kz = quant_qk(kb, lens=lens)
         vz = oracle.quantize_v_fp8(vb, lens=lens)
-        oracle.attention(w.fmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows,
-                         nthreads=nthreads)
+        # rotated MXFP4: MXFP4 codes of QH and KH, logits (QH)(KH)^T / 128
+        afmt, c = (1, 1.0 / math.sqrt(w.D) / 128) if w.fmt == 3 else (w.fmt, None)
+        oracle.attention(afmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows,
+                         softmax_scale=c, nthreads=nthreads)
         return time.perf_counter() - t0
 
     def rows_of(n):
@@ -453,9 +456,11 @@ def main():
     mhz = (clk or {}).get("sm_mhz") or 2070.0
     exp2_ms = exp2_count / (_EX2_PER_CLK_SM * 152 * mhz * 1e6) * 1e3
     nqt = 2 if Nqp >= 256 else 1
-    kernel = f"sage_attn_kernel<{fmt},{nqt},{(2 if nqt == 2 else 3) if fmt == 0 else 4}>"
+    kfmt = 1 if fmt == 3 else fmt   # the rotated MXFP4 format runs the MXFP4 kernel
+    kernel = f"sage_attn_kernel<{kfmt},{nqt},{(2 if nqt == 2 else 3) if kfmt == 0 else 4}>"
     fmt_names = {0: ("int8+fp8e4m3", "int8_qk_fp8_v"), 1: ("mxfp4+fp8e4m3", "mxfp4_qk_fp8_v"),
-                 2: ("fp8e4m3", "fp8_qk_fp8_v")}
+                 2: ("fp8e4m3", "fp8_qk_fp8_v"),
+                 3: ("mxfp4+fp8e4m3", "hadamard_mxfp4_qk_fp8_v")}
     traffic = _profiled_traffic(kernel, w.name) if args.heads == 0 else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -486,7 +491,7 @@ def main():
                      "traffic": None if traffic is None else traffic,
                      "algorithmic_flops_per_launch": flops,
                      "peak_basis": (f"{peak_kind} bf16 {p16} TFLOP/s x nominal ratios: Q K^T "
-                                    f"{ {0: 'fp16 x1', 1: 'fp4 x6', 2: 'fp8 x2'}[fmt] }, P V fp8 x2, "
+                                    f"{ {0: 'fp16 x1', 1: 'fp4 x6', 2: 'fp8 x2', 3: 'fp4 x6'}[fmt] }, P V fp8 x2, "
                                     f"harmonic combination"),
                      "kernel": kernel},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

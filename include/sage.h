@@ -63,8 +63,11 @@ typedef enum {
 typedef enum {
   SAGE_FMT_QK_INT8_V_FP8 = 0,  /* Q/K INT8 per-128-token-block scales, V FP8 E4M3 */
   SAGE_FMT_QK_MXFP4_V_FP8 = 1, /* Q/K MXFP4 E2M1 + E8M0 per 32 channels, V FP8 E4M3 */
-  SAGE_FMT_QK_FP8_V_FP8 = 2    /* Q/K FP8 E4M3 per-128-token-block scales, V FP8 E4M3
+  SAGE_FMT_QK_FP8_V_FP8 = 2,   /* Q/K FP8 E4M3 per-128-token-block scales, V FP8 E4M3
                                   ("Test Result": the FP8 QK^T / FP8 PV row) */
+  SAGE_FMT_QK_MXFP4H_V_FP8 = 3 /* Q/K rotated by the 128-point Hadamard transform, then
+                                  MXFP4 as format 1; V FP8 E4M3 (Q/K rotation before
+                                  MXFP4 quantization) */
 } sage_format_t;
 
 typedef struct {
@@ -87,6 +90,12 @@ typedef struct {
  *   data  : [B][H][Npad][D/2] bytes, two E2M1 codes per byte, element 2i in
  *           the low nibble.
  *   scale : [B][H][Npad][D/32] E8M0 bytes (2^(byte-127)).
+ * SAGE_FMT_QK_MXFP4H_V_FP8, Q or K: the layout of SAGE_FMT_QK_MXFP4_V_FP8,
+ *   holding the codes of x H: each token's 128 channels (BF16 widened to
+ *   binary32) times the unnormalized Sylvester Hadamard matrix, computed as
+ *   the fast Walsh-Hadamard transform with binary32 butterflies
+ *   (a, b) -> (a + b, a - b), spans 1, 2, 4, ..., 64 in that order. Since
+ *   (QH)(KH)^T = 128 QK^T, sage_attn_fwd divides the logit multiplier by 128.
  * SAGE_FMT_QK_FP8_V_FP8, Q or K:
  *   data  : [B][H][Npad][D] FP8 E4M3 codes (one byte each).
  *   scale : [B][H][Npad/128] float, absmax/448 of each 128-token block.

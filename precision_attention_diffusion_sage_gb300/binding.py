@@ -23,6 +23,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "sage.h")
 FMT_INT8 = 0   # SAGE_FMT_QK_INT8_V_FP8
 FMT_MXFP4 = 1  # SAGE_FMT_QK_MXFP4_V_FP8
 FMT_FP8 = 2    # SAGE_FMT_QK_FP8_V_FP8
+FMT_MXFP4H = 3  # SAGE_FMT_QK_MXFP4H_V_FP8 (Hadamard-rotated MXFP4)
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libsage.so is not built ({LIB_PATH}); run __graft_entry__.build()")
@@ -133,8 +134,8 @@ def sage_quantize_qk(x: torch.Tensor, fmt: int = FMT_INT8, lens=None,
 
     INT8: returns (codes held as float16 ``[B, H, Npad, D]``, float32 scales
     ``[B, H, Npad/128]``). MXFP4: (uint8 ``[B, H, Npad, D/2]``, uint8 E8M0
-    ``[B, H, Npad, D/32]``). FP8: (uint8 E4M3 ``[B, H, Npad, D]``, float32
-    scales ``[B, H, Npad/128]``).
+    ``[B, H, Npad, D/32]``; the rotated MXFP4 format has the same layout).
+    FP8: (uint8 E4M3 ``[B, H, Npad, D]``, float32 scales ``[B, H, Npad/128]``).
     """
     B, N, H, D = x.shape
     Np = pad128(N)
@@ -147,7 +148,7 @@ def sage_quantize_qk(x: torch.Tensor, fmt: int = FMT_INT8, lens=None,
             out = torch.empty((B, H, Np, D // 2), dtype=torch.uint8, device=x.device)
     if scale is None:
         scale = (torch.empty((B, H, Np, D // 32), dtype=torch.uint8, device=x.device)
-                 if fmt == FMT_MXFP4
+                 if fmt in (FMT_MXFP4, FMT_MXFP4H)
                  else torch.empty((B, H, Np // 128), dtype=torch.float32, device=x.device))
     ln = _lens_tensor(lens, x.device)
     _check(_lib.sage_quantize_qk(fmt, _ptr(x), _bnhd_strides(x), B, N, H, D, _ptr(ln), _ptr(out),

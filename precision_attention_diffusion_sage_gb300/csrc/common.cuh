@@ -53,7 +53,8 @@ struct QuantQKArgs {
   int* status;
 };
 cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s);
-cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s);
+// rotate: Hadamard-transform each token row before quantizing.
+cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s, bool rotate);
 cudaError_t launch_quantize_qk_fp8(const QuantQKArgs& a, cudaStream_t s);
 
 struct QuantVArgs {

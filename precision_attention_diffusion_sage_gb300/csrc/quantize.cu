@@ -254,6 +254,37 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&x)[8], float scale) {
 
 // MXFP4: 256 threads = 16 token rows per pass, 16 lanes per row, each lane 8
 // channels; 4 lanes share one 32-channel group. 64 rows per CTA.
+// One step of the binary32 fast Walsh-Hadamard transform across the 16 lanes
+// of a token row (lane L holds channels 8L .. 8L+7): the butterfly partner of
+// channel c is c ^ (8 m), in lane L ^ m; the lane holding the lower channel
+// keeps a + b, the other a - b.
+__device__ __forceinline__ void fwht_lanes(float (&f)[8], int lane16, int m) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float o = __shfl_xor_sync(0xffffffffu, f[i], m);
+    f[i] = (lane16 & m) ? __fsub_rn(o, f[i]) : __fadd_rn(f[i], o);
+  }
+}
+
+// The unnormalized 128-point Walsh-Hadamard transform of one token row, in
+// binary32 with the butterfly spans 1, 2, 4 (inside a thread's 8 channels)
+// then 8, 16, 32, 64 (across lanes), in that order.
+__device__ __forceinline__ void fwht128_row(float (&f)[8], int lane16) {
+#pragma unroll
+  for (int h = 1; h < 8; h *= 2)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & h) == 0) {
+        const float a = f[i], b = f[i + h];
+        f[i] = __fadd_rn(a, b);
+        f[i + h] = __fsub_rn(a, b);
+      }
+#pragma unroll
+  for (int m = 1; m < 16; m *= 2) fwht_lanes(f, lane16, m);
+}
+
+// ROT: rotate each token row by the Hadamard transform before quantizing.
+template <bool ROT>
 __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
   const int64_t h = blockIdx.x, b = blockIdx.z;
   const int64_t Np = pad128(a.N);
@@ -268,6 +299,7 @@ __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
     const int64_t n = blockIdx.y * 64 + pass * 16 + (threadIdx.x >> 4);  // < Np by the grid
     float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (n < nv) unpack8(ldg_v4(a.x + b * a.sb + n * a.sn + h * a.sh + col), f);
+    if constexpr (ROT) fwht128_row(f, static_cast<int>(threadIdx.x & 15));  // whole row per 16 lanes
     float amax = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
@@ -735,10 +767,13 @@ cudaError_t launch_quantize_qk_fp8(const QuantQKArgs& a, cudaStream_t s) {
   return launch_quantize_qk_block<1>(a, s);
 }
 
-cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s) {
+cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s, bool rotate) {
   dim3 grid(static_cast<unsigned>(a.H), static_cast<unsigned>(pad128(a.N) / 64),
             static_cast<unsigned>(a.B));
-  quantize_qk_mxfp4_kernel<<<grid, 256, 0, s>>>(a);
+  if (rotate)
+    quantize_qk_mxfp4_kernel<true><<<grid, 256, 0, s>>>(a);
+  else
+    quantize_qk_mxfp4_kernel<false><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

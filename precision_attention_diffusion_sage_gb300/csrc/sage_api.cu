@@ -61,7 +61,7 @@ sage_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAG
 
 bool known_format(sage_format_t fmt) {
   return fmt == SAGE_FMT_QK_INT8_V_FP8 || fmt == SAGE_FMT_QK_MXFP4_V_FP8 ||
-         fmt == SAGE_FMT_QK_FP8_V_FP8;
+         fmt == SAGE_FMT_QK_FP8_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
 }
 
 int64_t resolve_splits(int num_splits, int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
@@ -81,7 +81,7 @@ size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, 
   if (check_shape(B, N, H, D) != SAGE_OK) return 0;
   if (!known_format(fmt)) return 0;
   const int64_t Np = pad128(N);
-  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8;
+  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
   switch (which) {
     case 0:  // FP16-held INT8 codes: 2 B, E4M3: 1 B, packed E2M1: 1/2 B per element
       return static_cast<size_t>(mx ? B * H * Np * D / 2
@@ -134,7 +134,8 @@ sage_status_t sage_quantize_qk(sage_format_t fmt, const void* x, sage_strides_t 
   switch (fmt) {
     case SAGE_FMT_QK_INT8_V_FP8: return from_cuda(launch_quantize_qk_int8(a, s));
     case SAGE_FMT_QK_FP8_V_FP8: return from_cuda(launch_quantize_qk_fp8(a, s));
-    default: return from_cuda(launch_quantize_qk_mxfp4(a, s));
+    case SAGE_FMT_QK_MXFP4H_V_FP8: return from_cuda(launch_quantize_qk_mxfp4(a, s, true));
+    default: return from_cuda(launch_quantize_qk_mxfp4(a, s, false));
   }
 }
 
@@ -182,7 +183,7 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   int* status = nullptr;
   if ((st = device_state(&status)) != SAGE_OK) return st;
   const float c = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8;
+  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
   AttnLaunch a;
   a.fmt = mx ? 1 : (fmt == SAGE_FMT_QK_FP8_V_FP8 ? 2 : 0);
   a.q = q_q;
@@ -202,6 +203,8 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   p.nbq = pad128(Nq) / 128;
   p.nbk = pad128(Nk) / 128;
   p.scale_log2 = static_cast<float>(static_cast<double>(c) * 1.4426950408889634);
+  // Hadamard-rotated Q/K: (QH)(KH)^T = 128 QK^T (an exact power of two).
+  if (fmt == SAGE_FMT_QK_MXFP4H_V_FP8) p.scale_log2 *= 0.0078125f;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.osb = os.b;
   p.osn = os.n;

@@ -25,11 +25,24 @@ def oracle_quantize(fmt, q, k, v, k_lens=None):
     elif fmt == 2:
         qz = oracle.quantize_fp8_qk(qb)
         kz = oracle.quantize_fp8_qk(kb, lens=k_lens)
+    elif fmt == 3:
+        qz = oracle.quantize_mxfp4_hadamard(qb)
+        kz = oracle.quantize_mxfp4_hadamard(kb, lens=k_lens)
     else:
         qz = oracle.quantize_mxfp4(qb)
         kz = oracle.quantize_mxfp4(kb, lens=k_lens)
     vz = oracle.quantize_v_fp8(vb, lens=k_lens)
     return qz, kz, vz
+
+
+def oracle_attention_format(fmt, softmax_scale=None, D=128):
+    """The oracle attention call for a library format: the rotated MXFP4
+    format holds MXFP4 codes of QH and KH, whose logits (QH)(KH)^T are 128
+    times QK^T, so it is MXFP4 attention with the multiplier divided by 128."""
+    if fmt != 3:
+        return fmt, softmax_scale
+    c = 1.0 / math.sqrt(D) if softmax_scale is None or softmax_scale <= 0 else softmax_scale
+    return 1, c / 128.0
 
 
 def gpu_codes(fmt, x_q):

@@ -16,7 +16,7 @@ import oracle
 from precision_attention_diffusion_sage_gb300.inputs import WORKLOADS, Workload, bf16_bits, make_qkv
 
 from _helpers import (assert_attention_close, assert_qk_equal, assert_v_equal, gpu_codes,
-                      oracle_quantize)
+                      oracle_attention_format, oracle_quantize)
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,7 @@ def _run_gpu(fmt, q, k, v, k_lens=None, num_splits=0, softmax_scale=None):
 
 
 def _oracle_attention(fmt, qz, kz, vz, Nq, Nk, k_lens=None, rows=None, softmax_scale=None):
+    fmt, softmax_scale = oracle_attention_format(fmt, softmax_scale)
     o, lse, _ = oracle.attention(fmt, qz[0], qz[1], kz[0], kz[1], vz[0], vz[1], Nq=Nq, Nk=Nk,
                                  k_lens=k_lens, rows=rows, softmax_scale=softmax_scale)
     return o, lse
@@ -420,3 +421,75 @@ def test_full_size_workload_fp8(name, heads):
     rows = _sample_rows(w.Nq)
     ro, rl = _oracle_attention(2, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
     assert_attention_close(o[:, :, heads], lse[:, heads], ro, rl, rows=rows)
+
+
+# ------------------------------------------------------------------ Hadamard-rotated MXFP4 Q/K
+@pytest.mark.parametrize("N,lens", [(256, None), (1, None), (129, None), (300, [100])])
+def test_quantize_mxfp4h_bitexact(N, lens):
+    w, q, k, v = _small(1, 2, N, N, seed=70 + N, structure="k_channels_x8")
+    for x in (q, k):
+        xq, xs = binding.sage_quantize_qk(x, 3, lens=lens)
+        rq, rs = oracle.quantize_mxfp4_hadamard(bf16_bits(x), lens=lens)
+        assert_qk_equal(3, xq, xs, rq, rs)
+
+
+def test_quantize_mxfp4h_rounding_order_bitexact():
+    """Rows mixing magnitudes 2^12 and 2^-12: every binary32 butterfly rounds,
+    so only the same butterfly order (spans 1, 2, 4, ..., 64) and the same
+    rounding give the same codes and block exponents."""
+    g = torch.Generator().manual_seed(71)
+    N = 256
+    mag = torch.where(torch.rand(1, N, 2, 128, generator=g) < 0.5, 4096.0, 1.0 / 4096.0)
+    x = (torch.randn(1, N, 2, 128, generator=g) * mag).to(torch.bfloat16)
+    # a few rows whose transform has a block of exact cancellations (all-equal rows)
+    x[0, :8] = 3.0
+    xq, xs = binding.sage_quantize_qk(x.cuda(), 3)
+    rq, rs = oracle.quantize_mxfp4_hadamard(bf16_bits(x))
+    assert_qk_equal(3, xq, xs, rq, rs)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (129, 65), (300, 300), (513, 77), (256, 384)])
+def test_attention_mxfp4h_ragged_tails(Nq, Nk):
+    w, q, k, v = _small(1, 2, Nq, Nk, seed=Nq * 7 + Nk, structure="k_channels_x8")
+    (qq, qs), (kq, ks), _, o, lse = _run_gpu(3, q, k, v)
+    qz, kz, vz = oracle_quantize(3, q, k, v)
+    assert_qk_equal(3, qq, qs, *qz)
+    assert_qk_equal(3, kq, ks, *kz)
+    ro, rl = _oracle_attention(3, qz, kz, vz, Nq, Nk)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_mxfp4h_cross_ragged_splits_and_scale():
+    w, q, k, v = _small(2, 2, 300, 1000, seed=72, structure="k_offset_std2")
+    lens = [1000, 333]
+    for splits, c in ((1, None), (3, None), (2, 0.05)):
+        _, _, _, o, lse = _run_gpu(3, q, k, v, k_lens=lens, num_splits=splits, softmax_scale=c)
+        qz, kz, vz = oracle_quantize(3, q, k, v, k_lens=lens)
+        ro, rl = _oracle_attention(3, qz, kz, vz, 300, 1000, k_lens=lens, softmax_scale=c)
+        assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_mxfp4h_deterministic():
+    w = WORKLOADS["mxfp4h_self"]
+    q, k, v = make_qkv(w, device="cuda")
+    o1, l1 = binding.sage_attention(q, k, v, fmt=3)
+    for _ in range(2):
+        o2, l2 = binding.sage_attention(q, k, v, fmt=3)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+
+
+def test_full_size_workload_mxfp4h():
+    w = WORKLOADS["mxfp4h_self"]
+    q, k, v = make_qkv(w, device="cuda")
+    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(3, q, k, v)
+    hs = [0, 11, 23]
+    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
+    qz, kz, vz = oracle_quantize(3, sub(q), sub(k), sub(v))
+    assert_qk_equal(3, qq[:, hs], qs[:, hs], *qz)
+    assert_qk_equal(3, kq[:, hs], ks[:, hs], *kz)
+    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
+    rows = _sample_rows(w.Nq)
+    ro, rl = _oracle_attention(3, qz, kz, vz, w.Nq, w.Nk, rows=rows)
+    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)

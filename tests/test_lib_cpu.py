@@ -37,6 +37,10 @@ def test_quantized_bytes():
     assert binding.sage_quantized_bytes(0, 2, B, N, H, D) == B * H * D * Np
     assert binding.sage_quantized_bytes(0, 3, B, N, H, D) == B * H * D * 4
     assert binding.sage_quantized_bytes(0, 0, B, N, H, 64) == 0      # D must be 128
+    assert binding.sage_quantized_bytes(2, 0, B, N, H, D) == B * H * Np * D       # FP8 codes
+    assert binding.sage_quantized_bytes(2, 1, B, N, H, D) == B * H * 3 * 4        # FP8 block scales
+    assert binding.sage_quantized_bytes(3, 0, B, N, H, D) == B * H * Np * 64      # rotated MXFP4
+    assert binding.sage_quantized_bytes(3, 1, B, N, H, D) == B * H * Np * 4
     assert binding.sage_quantized_bytes(7, 0, B, N, H, D) == 0       # unknown format
 
 
