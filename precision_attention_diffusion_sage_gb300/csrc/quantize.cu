@@ -252,17 +252,42 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&x)[8], float scale) {
   return r;
 }
 
-// MXFP4: 256 threads = 16 token rows per pass, 16 lanes per row, each lane 8
-// channels; 4 lanes share one 32-channel group. 64 rows per CTA.
 // One step of the binary32 fast Walsh-Hadamard transform across the 16 lanes
 // of a token row (lane L holds channels 8L .. 8L+7): the butterfly partner of
 // channel c is c ^ (8 m), in lane L ^ m; the lane holding the lower channel
-// keeps a + b, the other a - b.
+// keeps a + b, the other a - b. Both are written as fma(own, +-1, partner):
+// the product is exact, so the single rounding gives the same binary32 value
+// (and the same signed zero) as the plain sum or difference.
 __device__ __forceinline__ void fwht_lanes(float (&f)[8], int lane16, int m) {
+  const float sg = (lane16 & m) ? -1.0f : 1.0f;
+  const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float o = __shfl_xor_sync(0xffffffffu, f[i], m);
-    f[i] = (lane16 & m) ? __fsub_rn(o, f[i]) : __fadd_rn(f[i], o);
+  for (int i = 0; i < 8; i += 2) {
+    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, f[i], m),
+                                 __shfl_xor_sync(0xffffffffu, f[i + 1], m));
+    const float2 r = __ffma2_rn(make_float2(f[i], f[i + 1]), sg2, o);
+    f[i] = r.x;
+    f[i + 1] = r.y;
+  }
+}
+
+// In-thread butterflies of span h (1, 2 or 4) on a thread's 8 channels, two
+// butterflies per packed instruction: sums a + b and differences
+// fma(b, -1, a) = a - b.
+template <int H>
+__device__ __forceinline__ void fwht_local(float (&f)[8]) {
+  constexpr int i0 = 0, i1 = (H == 1) ? 2 : 1;          // first two lower indices
+  constexpr int i2 = (H == 4) ? 2 : 4, i3 = (H == 4) ? 3 : (H == 2 ? 5 : 6);
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+  {
+    const float2 a = make_float2(f[i0], f[i1]), b = make_float2(f[i0 + H], f[i1 + H]);
+    const float2 s = __fadd2_rn(a, b), d = __ffma2_rn(b, m1, a);
+    f[i0] = s.x; f[i1] = s.y; f[i0 + H] = d.x; f[i1 + H] = d.y;
+  }
+  {
+    const float2 a = make_float2(f[i2], f[i3]), b = make_float2(f[i2 + H], f[i3 + H]);
+    const float2 s = __fadd2_rn(a, b), d = __ffma2_rn(b, m1, a);
+    f[i2] = s.x; f[i3] = s.y; f[i2 + H] = d.x; f[i3 + H] = d.y;
   }
 }
 
@@ -270,20 +295,17 @@ __device__ __forceinline__ void fwht_lanes(float (&f)[8], int lane16, int m) {
 // binary32 with the butterfly spans 1, 2, 4 (inside a thread's 8 channels)
 // then 8, 16, 32, 64 (across lanes), in that order.
 __device__ __forceinline__ void fwht128_row(float (&f)[8], int lane16) {
-#pragma unroll
-  for (int h = 1; h < 8; h *= 2)
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((i & h) == 0) {
-        const float a = f[i], b = f[i + h];
-        f[i] = __fadd_rn(a, b);
-        f[i + h] = __fsub_rn(a, b);
-      }
+  fwht_local<1>(f);
+  fwht_local<2>(f);
+  fwht_local<4>(f);
 #pragma unroll
   for (int m = 1; m < 16; m *= 2) fwht_lanes(f, lane16, m);
 }
 
-// ROT: rotate each token row by the Hadamard transform before quantizing.
+// MXFP4: 256 threads = 16 token rows per pass, 16 lanes per row, each lane 8
+// channels; 4 lanes share one 32-channel group. 64 rows per CTA, the four
+// passes' loads issued before any arithmetic. ROT: rotate each token row by
+// the Hadamard transform before quantizing.
 template <bool ROT>
 __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
   const int64_t h = blockIdx.x, b = blockIdx.z;
@@ -294,11 +316,18 @@ __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
   const int group = col / 32;
   uint8_t* codes = static_cast<uint8_t*>(a.out);
   uint8_t* e8 = static_cast<uint8_t*>(a.scale);
-#pragma unroll 1
+  const int64_t n0 = blockIdx.y * 64 + (threadIdx.x >> 4);  // pass p: row n0 + 16 p < Np
+  uint4 raw[4];
+#pragma unroll
   for (int pass = 0; pass < 4; ++pass) {
-    const int64_t n = blockIdx.y * 64 + pass * 16 + (threadIdx.x >> 4);  // < Np by the grid
-    float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (n < nv) unpack8(ldg_v4(a.x + b * a.sb + n * a.sn + h * a.sh + col), f);
+    const int64_t n = n0 + pass * 16;
+    raw[pass] = n < nv ? ldg_v4(a.x + b * a.sb + n * a.sn + h * a.sh + col) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const int64_t n = n0 + pass * 16;
+    float f[8];
+    unpack8(raw[pass], f);
     if constexpr (ROT) fwht128_row(f, static_cast<int>(threadIdx.x & 15));  // whole row per 16 lanes
     float amax = 0.0f;
 #pragma unroll
