@@ -67,6 +67,13 @@ def _L():
                      "oracle_quantize_fp8_qk", "oracle_quantize_mxfp4_hadamard"):
             getattr(lib, name).restype = None
             getattr(lib, name).argtypes = q_args
+        lib.oracle_k_mean.restype = None
+        lib.oracle_k_mean.argtypes = [P, I64, I64, I64, I64, I64, I64, I64, P, P]
+        lib.oracle_quantize_int8_smooth.restype = None
+        lib.oracle_quantize_int8_smooth.argtypes = [P, I64, I64, I64, I64, I64, I64, I64, P, P, P,
+                                                    P]
+        lib.oracle_k_mean_lse_term.restype = None
+        lib.oracle_k_mean_lse_term.argtypes = [P, P, P, I64, I64, I64, I64, D, P, I64, P]
         lib.oracle_fwht128.restype = None
         lib.oracle_fwht128.argtypes = [P, P, I64]
         lib.oracle_attention.restype = None
@@ -173,6 +180,45 @@ def quantize_mxfp4_hadamard(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.nd
     return c, e
 
 
+def k_mean(x: np.ndarray, lens=None) -> np.ndarray:
+    """Per-(b,h,channel) K mean over the valid tokens, float32 [B,H,D], from the
+    exact fixed-point sum (grid 2^(E-40), E the exponent of the channel maximum)."""
+    B, N, H, D, sb, sn, sh = _bnhd(x)
+    mu = np.zeros((B, H, D), np.float32)
+    ln = _lens(lens)
+    _L().oracle_k_mean(_ptr(x), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(mu))
+    return mu
+
+
+def quantize_int8_smooth(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """K smoothing then INT8: (codes [B,H,Npad,D], block scales [B,H,Npad/128],
+    channel means [B,H,D]) with codes/scales those of (float)k - mean."""
+    B, N, H, D, sb, sn, sh = _bnhd(x)
+    Np = pad128(N)
+    mu = k_mean(x, lens=lens)
+    q = np.zeros((B, H, Np, D), np.int8)
+    s = np.zeros((B, H, Np // 128), np.float32)
+    ln = _lens(lens)
+    _L().oracle_quantize_int8_smooth(_ptr(x), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(mu), _ptr(q),
+                                     _ptr(s))
+    return q, s, mu
+
+
+def k_mean_lse_term(q: np.ndarray, q_scale: np.ndarray, mu: np.ndarray, *, Nq: int,
+                    softmax_scale: Optional[float] = None, rows=None) -> np.ndarray:
+    """softmax_scale * (s_q q8_i) . mu for every (b, h, evaluated row): the
+    per-row logit offset that K smoothing removes, [B,H,nrows] float64."""
+    B, H, _, D = q.shape
+    c = 1.0 / math.sqrt(D) if softmax_scale is None or softmax_scale <= 0 else float(softmax_scale)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nr = Nq if r is None else len(r)
+    out = np.zeros((B, H, nr), np.float64)
+    qa, sa, ma = (np.ascontiguousarray(a) for a in (q, q_scale, mu))
+    _L().oracle_k_mean_lse_term(_ptr(qa), _ptr(sa), _ptr(ma), B, H, Nq, D, c, _ptr(r), nr,
+                                _ptr(out))
+    return out
+
+
 def quantize_fp8_qk(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
     """E4M3 codes [B,H,Npad,D] and FP32 block scales [B,H,Npad/128] (absmax/448)."""
     B, N, H, D, sb, sn, sh = _bnhd(x)
@@ -198,8 +244,12 @@ def quantize_mxfp4(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
 # ------------------------------------------------------------------ attention
 def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: int = 128,
               softmax_scale: Optional[float] = None, k_lens=None, rows=None,
-              want_weights: bool = False, nthreads: int = 0):
+              want_weights: bool = False, nthreads: int = 0, k_mean=None):
     """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K; fmt 2: E4M3 Q/K. V is E4M3.
+
+    k_mean (fmt 0 only): the channel means that K smoothing subtracted before
+    quantizing K; O is that of the smoothed logits and LSE adds back the
+    per-row term softmax_scale * q^ . mean (k_mean_lse_term).
 
     Returns (o [B,H,nrows,D] float64, lse [B,H,nrows] float64, w or None).
     """
@@ -214,6 +264,9 @@ def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: 
     ln = _lens(k_lens)
     _L().oracle_attention(fmt, *(_ptr(a) for a in arrs), _ptr(ln), B, H, Nq, Nk, D, c, _ptr(r),
                           nr, _ptr(o), _ptr(lse), _ptr(w), nthreads)
+    if k_mean is not None:
+        assert fmt == 0, "K smoothing is defined for the INT8 Q/K format"
+        lse = lse + k_mean_lse_term(q, q_scale, k_mean, Nq=Nq, softmax_scale=c, rows=r)
     return o, lse, w
 
 

@@ -208,6 +208,98 @@ void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
   }
 }
 
+// K smoothing: the per-(b,h,channel) mean of K over the valid tokens.
+// Reading (the pages name a smoothing kernel but print no formula): the mean
+// is made independent of summation order by summing exactly in integers on a
+// fixed-point grid. E = the binary32 exponent of the channel's absolute
+// maximum (exponent field at least 1, minus 127); a BF16 value m * 2^x (m the
+// integer significand) contributes m * 2^(x + 40 - E), truncated toward zero;
+// the integer sum S then gives mu = (float)(((double)S * 2^(E - 40)) / n),
+// binary64 rounded to nearest at each step, then binary32. No valid token, or
+// a zero maximum, gives mu = 0.
+void oracle_k_mean(const uint16_t* k, int64_t sb, int64_t sn, int64_t sh, int64_t B, int64_t N,
+                   int64_t H, int64_t D, const int32_t* lens, float* mu) {
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t nv = valid_len(lens, b, N);
+    for (int64_t h = 0; h < H; ++h)
+      for (int64_t d = 0; d < D; ++d) {
+        float amax = 0.0f;
+        for (int64_t n = 0; n < nv; ++n)
+          amax = std::max(amax, std::fabs(bf16_to_float(k[b * sb + n * sn + h * sh + d])));
+        float& out = mu[(b * H + h) * D + d];
+        if (nv <= 0 || amax == 0.0f) {
+          out = 0.0f;
+          continue;
+        }
+        uint32_t abits;
+        std::memcpy(&abits, &amax, 4);
+        const int E = std::max<int>(1, (abits >> 23) & 0xFF) - 127;
+        int64_t S = 0;
+        for (int64_t n = 0; n < nv; ++n) {
+          const uint16_t v = k[b * sb + n * sn + h * sh + d];
+          const int ef = (v >> 7) & 0xFF;
+          const int64_t m = (v & 0x7F) | (ef ? 0x80 : 0);     // integer significand
+          const int x = std::max(ef, 1) - 127 - 7;              // value = m * 2^x
+          const int shift = x + 40 - E;                          // <= 33 since |v| <= amax
+          int64_t c = shift >= 0 ? (m << shift) : (-shift >= 63 ? 0 : (m >> -shift));
+          S += (v & 0x8000) ? -c : c;
+        }
+        const double mean = std::ldexp(static_cast<double>(S), E - 40) / static_cast<double>(nv);
+        out = static_cast<float>(mean);
+      }
+  }
+}
+
+// INT8 quantization of smoothed K: y = (float)k - mu[b,h,d] in binary32, then
+// the INT8 rule of oracle_quantize_int8 (absmax/127 per 128-token block) on y.
+void oracle_quantize_int8_smooth(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
+                                 int64_t B, int64_t N, int64_t H, int64_t D, const int32_t* lens,
+                                 const float* mu, int8_t* q, float* scale) {
+  const int64_t Np = pad128(N), nb = Np / 128;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t nv = valid_len(lens, b, N);
+    for (int64_t h = 0; h < H; ++h) {
+      const float* m = mu + (b * H + h) * D;
+      for (int64_t blk = 0; blk < nb; ++blk) {
+        const int64_t n0 = blk * 128, n1 = std::min(n0 + 128, nv);
+        float amax = 0.0f;
+        for (int64_t n = n0; n < n1; ++n)
+          for (int64_t d = 0; d < D; ++d)
+            amax = std::max(amax, std::fabs(bf16_to_float(x[b * sb + n * sn + h * sh + d]) - m[d]));
+        const float s = amax / 127.0f;
+        scale[(b * H + h) * nb + blk] = s;
+        for (int64_t n = n0; n < n0 + 128; ++n)
+          for (int64_t d = 0; d < D; ++d) {
+            int v = 0;
+            if (n < n1 && s > 0.0f)
+              v = oracle_int8_quantize_value(bf16_to_float(x[b * sb + n * sn + h * sh + d]) - m[d],
+                                             s);
+            q[((b * H + h) * Np + n) * D + d] = static_cast<int8_t>(v);
+          }
+      }
+    }
+  }
+}
+
+// The logit term that K smoothing removes, per query row: softmax_scale *
+// sum_d q^_id mu_d with q^ = s_q * q8 the dequantized INT8 query (FP64). Every
+// logit of row i carries it, so O is unchanged and LSE_i gains it.
+void oracle_k_mean_lse_term(const int8_t* q, const float* q_scale, const float* mu, int64_t B,
+                            int64_t H, int64_t Nq, int64_t D, double softmax_scale,
+                            const int64_t* rows, int64_t nrows, double* term) {
+  const int64_t Nqp = pad128(Nq);
+  if (!rows) nrows = Nq;
+  for (int64_t bh = 0; bh < B * H; ++bh)
+    for (int64_t r = 0; r < nrows; ++r) {
+      const int64_t i = rows ? rows[r] : r;
+      const double sq = q_scale[bh * (Nqp / 128) + i / 128];
+      double acc = 0.0;
+      for (int64_t d = 0; d < D; ++d)
+        acc += static_cast<double>(q[(bh * Nqp + i) * D + d]) * sq * static_cast<double>(mu[bh * D + d]);
+      term[bh * nrows + r] = softmax_scale * acc;
+    }
+}
+
 void oracle_fwht128(const float* in, float* out, int64_t rows) {
   for (int64_t r = 0; r < rows; ++r) {
     float x[128];

@@ -63,6 +63,23 @@ void oracle_quantize_fp8_qk(const uint16_t* x, int64_t sb, int64_t sn, int64_t s
                             int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* q,
                             float* scale);
 
+/* K smoothing (mean subtraction before INT8 quantization).
+ * mu: float [B][H][D], the mean of each channel over the valid tokens, summed
+ * exactly on the fixed-point grid 2^(E-40) (E = exponent of the channel's
+ * absolute maximum, values truncated toward zero), then (double)S * 2^(E-40)
+ * / n rounded to binary64 and to binary32; 0 for an empty or all-zero channel. */
+void oracle_k_mean(const uint16_t* k, int64_t sb, int64_t sn, int64_t sh, int64_t B, int64_t N,
+                   int64_t H, int64_t D, const int32_t* lens, float* mu);
+/* INT8 block quantization (as oracle_quantize_int8) of y = (float)k - mu. */
+void oracle_quantize_int8_smooth(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
+                                 int64_t B, int64_t N, int64_t H, int64_t D, const int32_t* lens,
+                                 const float* mu, int8_t* q, float* scale);
+/* term[bh][r] = softmax_scale * sum_d (s_q q8_id) mu_d for the evaluated rows
+ * (rows NULL: all Nq): what smoothing removed from every logit of row i. */
+void oracle_k_mean_lse_term(const int8_t* q, const float* q_scale, const float* mu, int64_t B,
+                            int64_t H, int64_t Nq, int64_t D, double softmax_scale,
+                            const int64_t* rows, int64_t nrows, double* term);
+
 /* ---- attention ---- */
 /* fmt 0: q_data/k_data are int8 [B][H][Npad][D] with float block scales
  *        [B][H][Npad/128];

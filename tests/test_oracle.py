@@ -517,3 +517,117 @@ def test_p8_online_equals_final_encoding():
         normal = np.exp2(t - M) * 256.0 >= 2.0 ** -6
         np.testing.assert_array_equal(a[normal], b[normal])
         assert np.all(np.abs(a - b) <= 2.0 ** -17)
+
+
+# ------------------------------------------------------------------ K smoothing
+def _bits(x):
+    """float array [B,N,H,D] -> BF16 bit patterns (the values must be BF16-exact)."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    assert np.array_equal(t.float().numpy(), np.asarray(x, dtype=np.float32)), "not BF16-exact"
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("N", [256, 300])
+def test_k_mean_exact_on_dyadic_data(N):
+    """On multiples of 1/8 the fixed-point sum loses nothing, so the mean is
+    the correctly rounded quotient of the exact sum by the token count."""
+    rng = np.random.RandomState(11)
+    x = rng.randint(-64, 65, size=(1, N, 2, 128)).astype(np.float32) / 8 + rng.randint(
+        -4, 5, size=(1, 1, 2, 128))
+    mu = oracle.k_mean(_bits(x))
+    want = (x.astype(np.float64).sum(1) / N).astype(np.float32)   # exact sum, one division
+    np.testing.assert_array_equal(mu, want)
+
+
+def test_k_mean_truncation_rule():
+    """Contributions are truncated toward zero on the grid 2^(E-40), E the
+    exponent of the channel maximum (here E = 10, grid 2^-30)."""
+    x = np.zeros((1, 3, 1, 128), np.float32)
+    x[0, 0, 0, :] = 2.0 ** 10
+    x[0, 1, 0, :] = -(2.0 ** 10)
+    x[0, 2, 0, 0] = 3 * 2.0 ** -32      # 0.75 grid steps: truncated to 0
+    x[0, 2, 0, 1] = -3 * 2.0 ** -32     # -0.75: toward zero gives 0 (floor would give -1)
+    x[0, 2, 0, 2] = 2.0 ** -29          # 2 grid steps: kept
+    x[0, 2, 0, 3] = -5 * 2.0 ** -31     # -2.5 steps: -2
+    mu = oracle.k_mean(_bits(x))[0, 0]
+    assert mu[0] == 0.0 and mu[1] == 0.0 and not np.signbit(mu[1])
+    assert mu[2] == np.float32(2.0 * 2.0 ** -30 / 3)
+    assert mu[3] == np.float32(-2.0 * 2.0 ** -30 / 3)
+    assert np.all(mu[4:] == 0.0)
+
+
+def test_k_mean_ragged_empty_and_zero():
+    rng = np.random.RandomState(12)
+    x = rng.randint(-64, 65, size=(3, 200, 1, 128)).astype(np.float32) / 8
+    x[:, 150:] = 1000.0                      # past the valid length of batch 0
+    x[2, :, :, :5] = 0.0                     # all-zero channels
+    mu = oracle.k_mean(_bits(x), lens=[150, 0, 200])
+    np.testing.assert_array_equal(mu[0], (x[0, :150].astype(np.float64).sum(0) / 150).astype(np.float32))
+    assert np.all(mu[1] == 0.0)              # no valid token
+    assert np.all(mu[2, :, :5] == 0.0)
+
+
+def test_k_mean_error_bound_on_gaussian_data():
+    """Truncation moves each term by less than one grid step 2^(E-40) <=
+    amax 2^-40, and the two final roundings add at most one binary32 ulp."""
+    w, q, k, v = _tiny(N=300)
+    kb = bf16_bits(k)
+    mu = oracle.k_mean(kb).astype(np.float64)
+    kf = _f32(kb).astype(np.float64)
+    mean = kf.mean(1)
+    amax = np.abs(kf).max(1)
+    assert np.all(np.abs(mu - mean) <= amax * 2.0 ** -40 + np.abs(mean) * 2.0 ** -23)
+
+
+def test_smoothing_is_translation_invariant():
+    """Adding a constant to every token of a channel changes the mean by that
+    constant and leaves the smoothed codes and scales unchanged (all values
+    dyadic, so every step is exact)."""
+    rng = np.random.RandomState(13)
+    x = rng.randint(-64, 65, size=(1, 256, 2, 128)).astype(np.float32) / 8
+    c = rng.randint(-4, 5, size=(1, 1, 2, 128)).astype(np.float32)
+    q0, s0, m0 = oracle.quantize_int8_smooth(_bits(x))
+    q1, s1, m1 = oracle.quantize_int8_smooth(_bits(x + c))
+    np.testing.assert_array_equal(m1, m0 + c[0].transpose(1, 0, 2)[:, 0][None])
+    np.testing.assert_array_equal(q1, q0)
+    np.testing.assert_array_equal(s1.view(np.uint32), s0.view(np.uint32))
+    # without smoothing the offset changes the codes
+    assert not np.array_equal(oracle.quantize_int8(_bits(x + c))[0], q0)
+
+
+def test_smoothing_zero_mean_reduces_to_plain_int8():
+    """Channels whose tokens come in +-pairs have mean exactly 0: the smoothed
+    quantizer then equals the plain INT8 quantizer."""
+    w, q, k, v = _tiny(N=128)
+    kf = _f32(bf16_bits(k))
+    x = np.concatenate([kf, -kf], axis=1)
+    q0, s0 = oracle.quantize_int8(_bits(x))
+    q1, s1, m1 = oracle.quantize_int8_smooth(_bits(x))
+    assert np.all(m1 == 0.0)
+    np.testing.assert_array_equal(q1, q0)
+    np.testing.assert_array_equal(s1.view(np.uint32), s0.view(np.uint32))
+
+
+def test_smoothed_attention_lse_and_accuracy():
+    """K with large per-channel offsets (mean ~ N(0, 3^2)): attention over the
+    smoothed K, with the per-row term c q^.mean added back to the LSE, matches
+    unquantized attention; the term is O(1), so dropping it would fail; and
+    smoothing lowers the output error of plain INT8 quantization."""
+    w = Workload("offsets", 1, 2, 256, 256, seed=14)
+    q, k, v = make_qkv(w)
+    k = (k.float() + 3.0 * torch.randn(1, 1, 2, 128, generator=torch.Generator().manual_seed(15))
+         ).to(torch.bfloat16)
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    oe, le = oracle.attention_exact(qb, kb, vb)
+    qz = oracle.quantize_int8(qb)
+    vz = oracle.quantize_v_fp8(vb)
+    kq, ks, mu = oracle.quantize_int8_smooth(kb)
+    os_, ls, _ = oracle.attention(0, *qz, kq, ks, *vz, Nq=256, Nk=256, k_mean=mu)
+    op, lp, _ = oracle.attention(0, *qz, *oracle.quantize_int8(kb), *vz, Nq=256, Nk=256)
+    term = oracle.k_mean_lse_term(*qz, mu, Nq=256)
+    assert np.abs(term).max() > 1.0
+    # the LSE error is that of INT8 Q (the same in both quantized runs)
+    assert np.abs(ls - lp).max() < 0.05
+    assert np.abs(ls - le).max() < 0.15
+    err = lambda o: float(np.abs(o - oe).max())  # noqa: E731
+    assert err(os_) < err(op)
