@@ -106,6 +106,8 @@ def _quant_bytes(w, Nqp: int, Nkp: int) -> float:
     code = {0: 2.0, 1: 0.5 + 1.0 / 32, 2: 1.0, 3: 0.5 + 1.0 / 32}[w.fmt]
     qk = (B * w.Nq * H * D * 2 + B * H * Nqp * D * code + B * w.Nk * H * D * 2
           + B * H * Nkp * D * code)
+    if w.smooth_k:  # K also read by the channel-maximum and the fixed-point-sum passes
+        qk += 2 * B * w.Nk * H * D * 2
     return qk + B * w.Nk * H * D * 2 * 2 + B * H * D * Nkp
 
 
@@ -178,12 +180,16 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64, nthreads: int = 0
         quant_qk = {0: oracle.quantize_int8, 1: oracle.quantize_mxfp4, 2: oracle.quantize_fp8_qk,
                     3: oracle.quantize_mxfp4_hadamard}[w.fmt]
         qz = quant_qk(qb)
-        kz = quant_qk(kb, lens=lens)
+        km = None
+        if w.smooth_k:
+            *kz, km = oracle.quantize_int8_smooth(kb, lens=lens)
+        else:
+            kz = quant_qk(kb, lens=lens)
         vz = oracle.quantize_v_fp8(vb, lens=lens)
         # rotated MXFP4: MXFP4 codes of QH and KH, logits (QH)(KH)^T / 128
         afmt, c = (1, 1.0 / math.sqrt(w.D) / 128) if w.fmt == 3 else (w.fmt, None)
         oracle.attention(afmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows,
-                         softmax_scale=c, nthreads=nthreads)
+                         softmax_scale=c, nthreads=nthreads, k_mean=km)
         return time.perf_counter() - t0
 
     def rows_of(n):
@@ -314,15 +320,23 @@ def main():
     def quant_q():
         binding.sage_quantize_qk(q, fmt, out=qq, scale=qs)
 
+    km = torch.empty((B, H, D), dtype=torch.float32, device=dev) if w.smooth_k else None
+    kws = (torch.empty(binding.sage_workspace_bytes(3, fmt, B, H, Nk, Nk), dtype=torch.uint8,
+                       device=dev) if w.smooth_k else None)
+
     def quant_k():
-        binding.sage_quantize_qk(k, fmt, lens=k_lens, out=kq, scale=ks)
+        if w.smooth_k:
+            binding.sage_quantize_k_smooth(k, lens=k_lens, out=kq, scale=ks, k_mean=km,
+                                           workspace=kws)
+        else:
+            binding.sage_quantize_qk(k, fmt, lens=k_lens, out=kq, scale=ks)
 
     def quant_v():
         binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
 
     def attn():
         binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens, out=o,
-                              lse=lse, num_splits=args.splits, workspace=aws)
+                              lse=lse, num_splits=args.splits, workspace=aws, k_mean=km)
 
     calls = (quant_q, quant_k, quant_v, attn)
     for _ in range(args.warmup):
@@ -412,7 +426,7 @@ def main():
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
             oo, ll = binding.sage_attention(qd, kd, vd, fmt=fmt, k_lens=k_lens,
-                                            num_splits=args.splits)
+                                            num_splits=args.splits, smooth_k=w.smooth_k)
             oh.copy_(oo, non_blocking=True)
             lh.copy_(ll, non_blocking=True)
 
@@ -447,7 +461,9 @@ def main():
                "kind": "oracle", "sample": desc, "seconds": dt,
                "value_1core": f1 / dt1 / 1e12, "sample_1core": desc1, "seconds_1core": dt1}
 
-    launches_per_step = 2 + 2 + 1 + (1 if nsplit > 1 else 0)
+    # Q and K quantize, V maxima + encode, attention (+ merge); K smoothing
+    # runs four K kernels (maxima, sums, means, encode) instead of one
+    launches_per_step = 2 + 2 + 1 + (1 if nsplit > 1 else 0) + (3 if w.smooth_k else 0)
     quant_bytes = _quant_bytes(w, Nqp, Nkp)
     # Secondary bound: one exp2 per logit on the MUFU pipe (no FMA-polynomial
     # exponentials are used), at the SM clock sampled during the run.
@@ -471,6 +487,7 @@ def main():
                    "k_lens": w.k_lens,
                    "heads_override": args.heads > 0,
                    "format": fmt_names[fmt][1],
+                   "k_smoothing": w.smooth_k,
                    "splits": nsplit,
                    "l2": "flushed between steps (256 MiB read outside the timed events)",
                    "launch": "one CUDA graph per library call (quantize Q, K, V; attention)",

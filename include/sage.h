@@ -111,7 +111,8 @@ size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, 
 
 /* Workspace bytes. op: 0 = sage_quantize_qk (always 0), 1 = sage_quantize_v
  * (per-(b,h,channel) maxima, B*H*128*4 bytes), 2 = sage_attn_fwd with
- * `num_splits` KV splits (0 = the split count the library would choose). */
+ * `num_splits` KV splits (0 = the split count the library would choose),
+ * 3 = sage_quantize_k_smooth (B*H*128*12 bytes; INT8 format only, else 0). */
 size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int64_t Nq,
                             int64_t Nk, int64_t D, int num_splits);
 
@@ -167,9 +168,44 @@ sage_status_t sage_quantize_v_noalloc(const void* v, sage_strides_t vs, int64_t 
                                       int64_t H, int64_t D, const int32_t* lens, void* v_q,
                                       float* v_scale, sage_stream_t stream);
 
+/* K smoothing for the INT8 Q/K format (the "_q_smooth_int8_kernel" /
+ * smoothing kernels named on "new MHA v4 entrypoint ..."; the pages give no
+ * formula, so the reading is): subtract each channel's mean of K over the
+ * valid tokens, then quantize as sage_quantize_qk does for
+ * SAGE_FMT_QK_INT8_V_FP8. Softmax is invariant to the per-row logit shift
+ * this causes, so O is that of the smoothed logits; pass k_mean to
+ * sage_attn_fwd (sage_attn_options_t) to have LSE include the shift.
+ *   mean   : the channel mean made independent of summation order: E =
+ *            binary32 exponent of the channel's absolute maximum (exponent
+ *            field at least 1, minus 127); each BF16 value m * 2^x (m its
+ *            integer significand) contributes m * 2^(x + 40 - E) truncated
+ *            toward zero; S = the exact integer sum; mean = (float)
+ *            (((double)S * 2^(E-40)) / n), binary64 rounded at each step, then
+ *            to binary32; 0 when n = 0 or the maximum is 0.
+ *   codes  : INT8 block quantization (as sage_quantize_qk) of the binary32
+ *            differences (float)k - mean.
+ *            K must be finite; a NaN or infinity leaves its channel's mean
+ *            unspecified.
+ *   fmt    : must be SAGE_FMT_QK_INT8_V_FP8 (else SAGE_ERR_UNSUPPORTED).
+ *   k, ks, B, N, H, D, lens, k_q, k_scale : as sage_quantize_qk.
+ *   k_mean : output float [B][H][D], 16-byte aligned.
+ *   workspace : sage_workspace_bytes(3, ...) bytes, 16-byte aligned; cleared
+ *            by the call (contents on entry ignored).
+ * Four stream-ordered steps: a clear of the workspace, the channel maxima,
+ * the fixed-point sums, and the finalize + encode. */
+sage_status_t sage_quantize_k_smooth(sage_format_t fmt, const void* k, sage_strides_t ks,
+                                     int64_t B, int64_t N, int64_t H, int64_t D,
+                                     const int32_t* lens, void* k_q, void* k_scale,
+                                     float* k_mean, void* workspace, size_t ws_bytes,
+                                     sage_stream_t stream);
+
 typedef struct {
-  int32_t num_splits; /* KV splits: 0 = library choice, 1 = no split, >1 = forced */
-  int32_t cta_mode;   /* reserved: 0 = library choice */
+  int32_t num_splits;   /* KV splits: 0 = library choice, 1 = no split, >1 = forced */
+  int32_t cta_mode;     /* reserved: 0 = library choice */
+  const float* k_mean;  /* nullable: the k_mean written by sage_quantize_k_smooth when K
+                           was smoothed (SAGE_FMT_QK_INT8_V_FP8 only; 16-byte aligned);
+                           LSE_i then adds softmax_scale * (s_q q8_i) . k_mean, the
+                           per-row logit term smoothing removed (O is unchanged by it) */
 } sage_attn_options_t;
 
 /* Attention forward ("[ROCm] Add aiter_sage_attn ...", Changes; "new MHA v4

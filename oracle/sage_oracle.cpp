@@ -216,7 +216,8 @@ void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
 // integer significand) contributes m * 2^(x + 40 - E), truncated toward zero;
 // the integer sum S then gives mu = (float)(((double)S * 2^(E - 40)) / n),
 // binary64 rounded to nearest at each step, then binary32. No valid token, or
-// a zero maximum, gives mu = 0.
+// a zero maximum, gives mu = 0. The definition is for finite K (a NaN or an
+// infinity makes the library's mean unspecified).
 void oracle_k_mean(const uint16_t* k, int64_t sb, int64_t sn, int64_t sh, int64_t B, int64_t N,
                    int64_t H, int64_t D, const int32_t* lens, float* mu) {
   for (int64_t b = 0; b < B; ++b) {
@@ -240,7 +241,9 @@ void oracle_k_mean(const uint16_t* k, int64_t sb, int64_t sn, int64_t sh, int64_
           const int ef = (v >> 7) & 0xFF;
           const int64_t m = (v & 0x7F) | (ef ? 0x80 : 0);     // integer significand
           const int x = std::max(ef, 1) - 127 - 7;              // value = m * 2^x
-          const int shift = x + 40 - E;                          // <= 33 since |v| <= amax
+          // <= 33 since |v| <= amax; capped at 40 so a NaN (which the maximum
+          // passes over) still gives a defined shift
+          const int shift = std::min(x + 40 - E, 40);
           int64_t c = shift >= 0 ? (m << shift) : (-shift >= 63 ? 0 : (m >> -shift));
           S += (v & 0x8000) ? -c : c;
         }

@@ -36,7 +36,8 @@ class Strides(ctypes.Structure):
 
 
 class AttnOptions(ctypes.Structure):
-    _fields_ = [("num_splits", ctypes.c_int32), ("cta_mode", ctypes.c_int32)]
+    _fields_ = [("num_splits", ctypes.c_int32), ("cta_mode", ctypes.c_int32),
+                ("k_mean", ctypes.c_void_p)]
 
 
 _P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
@@ -49,6 +50,9 @@ _lib.sage_quantize_qk.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P,
 _lib.sage_quantize_v.restype = _I32
 _lib.sage_quantize_v.argtypes = [_P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
                                  ctypes.c_size_t, _P]
+_lib.sage_quantize_k_smooth.restype = _I32
+_lib.sage_quantize_k_smooth.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
+                                        _P, ctypes.c_size_t, _P]
 _lib.sage_attn_fwd.restype = _I32
 _lib.sage_attn_fwd.argtypes = [_I32, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
                                ctypes.c_float, _I32, _P, Strides, _P, _P, ctypes.c_size_t,
@@ -176,12 +180,39 @@ def sage_quantize_v(v: torch.Tensor, lens=None, out: Optional[torch.Tensor] = No
     return out, scale
 
 
+def sage_quantize_k_smooth(k: torch.Tensor, lens=None, out: Optional[torch.Tensor] = None,
+                           scale: Optional[torch.Tensor] = None,
+                           k_mean: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None):
+    """K smoothing + INT8 quantization of BF16 K ``[B, N, H, D]``: returns (codes
+    held as float16 ``[B, H, Npad, D]``, float32 block scales ``[B, H, Npad/128]``,
+    float32 channel means ``[B, H, D]``); pass the means to sage_attn_fwd(k_mean=)."""
+    B, N, H, D = k.shape
+    Np = pad128(N)
+    dev = k.device
+    if out is None:
+        out = torch.empty((B, H, Np, D), dtype=torch.float16, device=dev)
+    if scale is None:
+        scale = torch.empty((B, H, Np // 128), dtype=torch.float32, device=dev)
+    if k_mean is None:
+        k_mean = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    need = sage_workspace_bytes(3, FMT_INT8, B, H, N, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    ln = _lens_tensor(lens, dev)
+    _check(_lib.sage_quantize_k_smooth(FMT_INT8, _ptr(k), _bnhd_strides(k), B, N, H, D, _ptr(ln),
+                                       _ptr(out), _ptr(scale), _ptr(k_mean), _ptr(workspace),
+                                       workspace.numel(), _stream()), "sage_quantize_k_smooth")
+    return out, scale, k_mean
+
+
 def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int, Nk: int,
                   k_lens=None, softmax_scale: Optional[float] = None, causal: int = 0,
                   out: Optional[torch.Tensor] = None, return_lse: bool = True,
                   lse: Optional[torch.Tensor] = None, num_splits: int = 0,
-                  workspace: Optional[torch.Tensor] = None):
-    """Attention forward on quantized operands. Returns (O ``[B, Nq, H, D]`` bf16, LSE or None)."""
+                  workspace: Optional[torch.Tensor] = None, k_mean: Optional[torch.Tensor] = None):
+    """Attention forward on quantized operands. Returns (O ``[B, Nq, H, D]`` bf16, LSE or None).
+    k_mean: the channel means from sage_quantize_k_smooth when K was smoothed."""
     B, H = q_q.shape[0], q_q.shape[1]
     D = 128
     dev = q_q.device
@@ -193,7 +224,7 @@ def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int
     if need > 0 and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ln = _lens_tensor(k_lens, dev)
-    opts = AttnOptions(num_splits, 0)
+    opts = AttnOptions(num_splits, 0, None if k_mean is None else k_mean.data_ptr())
     sc = -1.0 if softmax_scale is None else float(softmax_scale)
     _check(_lib.sage_attn_fwd(fmt, _ptr(q_q), _ptr(q_scale), _ptr(k_q), _ptr(k_scale), _ptr(v_q),
                               _ptr(v_scale), _ptr(ln), B, H, Nq, Nk, D, sc, causal, _ptr(out),
@@ -210,16 +241,22 @@ def sage_last_device_status() -> int:
 
 def sage_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: int = FMT_INT8,
                    k_lens=None, softmax_scale: Optional[float] = None, num_splits: int = 0,
-                   return_lse: bool = True):
-    """Quantize Q/K/V and attend: the four library calls in order."""
+                   return_lse: bool = True, smooth_k: bool = False):
+    """Quantize Q/K/V and attend: the four library calls in order. smooth_k
+    (INT8 only) quantizes K with sage_quantize_k_smooth and passes its channel
+    means to the attention call."""
     B, Nq, H, D = q.shape
     Nk = k.shape[1]
     qq, qs = sage_quantize_qk(q, fmt)
-    kq, ks = sage_quantize_qk(k, fmt, lens=k_lens)
+    km = None
+    if smooth_k:
+        kq, ks, km = sage_quantize_k_smooth(k, lens=k_lens)
+    else:
+        kq, ks = sage_quantize_qk(k, fmt, lens=k_lens)
     vq, vs = sage_quantize_v(v, lens=k_lens)
     return sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
                          softmax_scale=softmax_scale, num_splits=num_splits,
-                         return_lse=return_lse)
+                         return_lse=return_lse, k_mean=km)
 
 
 def int8_codes(x_q: torch.Tensor) -> torch.Tensor:

@@ -204,6 +204,33 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Dot product of row r of an INT8 Q tile (FP16-held codes, two 64-channel
+// halves of 128 rows x 128 B at +0 and +16 KB, 16-byte chunks swizzled by
+// r & 7) with 128 channel values in global memory.
+__device__ __forceinline__ float q_dot_kmean(uint32_t tile, int r, const float* mu) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int hlf = 0; hlf < 2; ++hlf)
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint32_t addr = tile + hlf * 16384 + r * 128 + (((g ^ r) & 7) << 4);
+      uint32_t w[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(addr));
+      const float4 m0 = __ldg(reinterpret_cast<const float4*>(mu + hlf * 64 + g * 8));
+      const float4 m1 = __ldg(reinterpret_cast<const float4*>(mu + hlf * 64 + g * 8 + 4));
+      const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+        acc = fmaf(c.x, mv[2 * q], acc);
+        acc = fmaf(c.y, mv[2 * q + 1], acc);
+      }
+    }
+  return acc;
+}
+
 // Threads per CTA: 7 warps for one query tile; 12 (three full warpgroups)
 // for two, so that registers can be moved to the softmax warpgroups with
 // setmaxnreg (each SM sub-partition holds one warp of every warpgroup).
@@ -728,7 +755,15 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const float lse = (m + log2f(l) - 8.0f + kHeadroom) * kLn2;
+      // K smoothing took the per-row constant softmax_scale * q^ . mean_k out
+      // of every logit (O is unchanged by it); the LSE adds it back, in log2
+      // units alpha_q * (q8 . mean_k), from this row's codes in the Q tile.
+      float lse_add = 0.0f;
+      if constexpr (FMT == 0) {
+        if (p.k_mean && (ok = warp_wait(q_full, 0, abort, p.status)))
+          lse_add = alpha_q * q_dot_kmean(smem_u32(sQ + t * 32768), r, p.k_mean + bh * 128);
+      }
+      const float lse = (m + log2f(l) - 8.0f + kHeadroom + lse_add) * kLn2;
       const bool store = row < p.Nq;
       if (p.num_splits > 1) {
         float* op = p.o_part + ((static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row) * 128;

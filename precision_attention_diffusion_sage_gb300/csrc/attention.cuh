@@ -20,6 +20,7 @@ struct AttnParams {
   __nv_bfloat16* o;
   int64_t osb, osn, osh;
   float* lse;            // nullable [B][H][Nq]
+  const float* k_mean;   // nullable [B][H][128], INT8 only: channel means removed by K smoothing
   int num_splits;
   int o_tma;             // 1: O stored through the tensor map (set by the launcher)
   float* o_part;         // [splits][B][H][Nq][128] when num_splits > 1

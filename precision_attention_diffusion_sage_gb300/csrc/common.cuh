@@ -71,4 +71,11 @@ struct QuantVArgs {
 inline int64_t v_workspace_bytes(int64_t B, int64_t H) { return B * H * 128 * 4; }
 cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s);
 
+// K smoothing workspace: an int64 sum and a binary32 maximum per (b, h, channel).
+inline int64_t k_smooth_workspace_bytes(int64_t B, int64_t H) { return B * H * 128 * 12; }
+// Smoothed INT8 K: channel means of K over the valid tokens (k_mean, float
+// [B][H][128]) subtracted before the INT8 block quantization into q.out/q.scale.
+cudaError_t launch_quantize_k_smooth(const QuantQKArgs& q, float* k_mean, void* workspace,
+                                     cudaStream_t s);
+
 }  // namespace sage

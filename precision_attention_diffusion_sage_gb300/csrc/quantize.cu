@@ -96,9 +96,7 @@ __device__ __forceinline__ float bf16x2_hmax(uint32_t m) { return fmaxf(bf16_lo(
 // comes within 2^-14 of 1/2, x / s (within 1.2e-5 of the product) may round
 // the other way and the caller redoes the chunk with the division. |n| <=
 // 127 needs no clamp: x / s never exceeds amax / s = 127 (1 + 2^-23).
-__device__ __forceinline__ uint4 int8_codes8(const uint4& raw, float inv, float& dmax) {
-  float f[8];
-  unpack8(raw, f);
+__device__ __forceinline__ uint4 int8_codes8f(const float (&f)[8], float inv, float& dmax) {
   const float2 inv2 = make_float2(inv, inv);
   const float2 mag = make_float2(12582912.0f, 12582912.0f), nmag = make_float2(-12582912.0f, -12582912.0f);
   uint32_t w[4];
@@ -113,6 +111,11 @@ __device__ __forceinline__ uint4 int8_codes8(const uint4& raw, float inv, float&
     w[q] = *reinterpret_cast<const uint32_t*>(&h2);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint4 int8_codes8(const uint4& raw, float inv, float& dmax) {
+  float f[8];
+  unpack8(raw, f);
+  return int8_codes8f(f, inv, dmax);
 }
 
 // One CTA per (128-token block, h, b); 256 threads, each owning 8 channels of
@@ -434,6 +437,182 @@ __global__ void __launch_bounds__(256) v_quantize_kernel(QuantVArgs a) {
 
 
 // ----------------------------------------------------------------------------
+// K smoothing (INT8 Q/K): the per-(b,h,channel) mean of K over the valid
+// tokens is subtracted before the INT8 block quantization. The mean is made
+// independent of summation order by an exact integer sum on the fixed-point
+// grid 2^(E-40), E the binary32 exponent of the channel's absolute maximum
+// (exponent field at least 1, minus 127): each BF16 value m * 2^x (m its
+// integer significand) contributes m * 2^(x + 40 - E) truncated toward zero;
+// then mean = (float)((double)S * 2^(E-40) / n) with binary64 rounding at
+// each step. Pass 1 is the V channel-maximum kernel run on K; pass 2 sums the
+// terms (int64 atomics per channel); pass 3 finalizes the means and encodes.
+
+// E of a channel maximum given as its binary32 bit pattern.
+__device__ __forceinline__ int k_grid_exp(int amax_bits) {
+  return max((amax_bits >> 23) & 0xFF, 1) - 127;
+}
+
+// Fixed-point terms of eight BF16 values (one row chunk, channels c..c+7),
+// added with their signs into per-channel (hi, lo) float accumulators, where
+// trunc(|v| 2^(40-E)) = hi 2^20 + lo. With a = |v| 2^(20-E) (two exact
+// power-of-two products c1 c2; a < 2^21 since |v| < 2^(E+1)): hi = floor(a)
+// and lo = floor(frac(a) 2^20), each read from a round-toward-zero addition
+// of 2^23 (whose unit in the last place is 1 there). Every accumulated value
+// is an integer below 2^24, so eight rows sum exactly in binary32. A value
+// whose a falls below the binary32 normal range contributes 0 on both
+// counts, as its truncated term is 0. (Defined for finite inputs.)
+__device__ __forceinline__ void k_fixed_terms8(const uint4& u, const float2 (&c1)[4],
+                                               const float2 (&c2)[4], float2 (&hi)[4],
+                                               float2 (&lo)[4]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  const float2 M = make_float2(8388608.0f, 8388608.0f), nM = make_float2(-8388608.0f, -8388608.0f);
+  const float2 m1 = make_float2(-1.0f, -1.0f), s20 = make_float2(1048576.0f, 1048576.0f);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t wa = w[q] & 0x7FFF7FFFu;
+    const float2 av = make_float2(__uint_as_float(wa << 16), __uint_as_float(wa & 0xFFFF0000u));
+    const float2 sg = make_float2(__uint_as_float(((w[q] << 16) & 0x80000000u) | 0x3F800000u),
+                                  __uint_as_float((w[q] & 0x80000000u) | 0x3F800000u));
+    const float2 a = __fmul2_rn(__fmul2_rn(av, c1[q]), c2[q]);
+    const float2 hf = __fadd2_rn(__fadd2_rz(a, M), nM);       // floor(a)
+    const float2 fr = __ffma2_rn(hf, m1, a);                  // frac(a), exact
+    const float2 lf = __fadd2_rn(__ffma2_rz(fr, s20, M), nM); // floor(frac(a) 2^20)
+    hi[q] = __ffma2_rn(hf, sg, hi[q]);
+    lo[q] = __ffma2_rn(lf, sg, lo[q]);
+  }
+}
+
+// Scale factors c1, c2 (c1 c2 = 2^(20-E), each step exact) of a channel whose
+// maximum has the binary32 bit pattern amax_bits.
+__device__ __forceinline__ void k_term_scales(int amax_bits, float& c1, float& c2) {
+  const int E = k_grid_exp(amax_bits);
+  c1 = E > 0 ? 1.0f : 0x1p64f;
+  c2 = exp2_int(E > 0 ? 20 - E : -44 - E);
+}
+
+// The exact integer term sum of one channel from its (hi, lo) accumulators.
+__device__ __forceinline__ long long k_term_sum(float hi, float lo) {
+  return __float2ll_rn(hi) * 1048576ll + __float2ll_rn(lo);
+}
+
+struct KSmoothArgs {
+  QuantQKArgs q;
+  float* k_mean;             // out [B][H][128]
+  unsigned long long* sum;   // workspace [B][H][128], int64 two's complement
+  int* amax;                 // workspace [B][H][128], binary32 bit patterns
+};
+
+// Pass 2: one CTA per (h, 128-token block, b); 16 row groups x 16 channel
+// groups of 8; per-thread int64 sums, reduced in shared memory, one atomic
+// per channel.
+__global__ void __launch_bounds__(256) k_sum_kernel(KSmoothArgs a) {
+  __shared__ long long red[16][128];
+  const int64_t h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
+  const int64_t nv = valid_tokens(a.q.lens, b, a.q.N, a.q.status);
+  const int64_t bh = b * a.q.H + h;
+  const int col = (threadIdx.x & 15) * 8;
+  const int rg = threadIdx.x >> 4;
+  float2 c1[4], c2[4], hi[4], lo[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    k_term_scales(a.amax[bh * 128 + col + 2 * q], c1[q].x, c2[q].x);
+    k_term_scales(a.amax[bh * 128 + col + 2 * q + 1], c1[q].y, c2[q].y);
+    hi[q] = lo[q] = make_float2(0.0f, 0.0f);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t n = blk * 128 + rg + 16 * i;
+    if (n < nv)
+      k_fixed_terms8(ldg_v4(a.q.x + b * a.q.sb + n * a.q.sn + h * a.q.sh + col), c1, c2, hi, lo);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    red[rg][col + 2 * q] = k_term_sum(hi[q].x, lo[q].x);
+    red[rg][col + 2 * q + 1] = k_term_sum(hi[q].y, lo[q].y);
+  }
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    long long t = 0;
+#pragma unroll
+    for (int g = 0; g < 16; ++g) t += red[g][threadIdx.x];
+    if (t != 0) atomicAdd(&a.sum[bh * 128 + threadIdx.x], static_cast<unsigned long long>(t));
+  }
+}
+
+// Channel means from the sums: one thread per (b, h, channel).
+__global__ void __launch_bounds__(128) k_mean_kernel(KSmoothArgs a) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 128 + threadIdx.x;  // (b*H + h)*128 + d
+  const int64_t b = i / (a.q.H * 128);
+  const int64_t nv = valid_tokens(a.q.lens, b, a.q.N, a.q.status);
+  const int ab = a.amax[i];
+  float mu = 0.0f;
+  if (nv > 0 && ab != 0) {
+    const int E = k_grid_exp(ab);
+    const double grid = __longlong_as_double(static_cast<long long>(E - 40 + 1023) << 52);
+    const long long S = static_cast<long long>(a.sum[i]);
+    mu = __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(S), grid), static_cast<double>(nv)));
+  }
+  a.k_mean[i] = mu;
+}
+
+// Pass 3 (direct loads): y = k - mean in binary32, then the INT8 rule of
+// quantize_qk_block_kernel on y.
+__global__ void __launch_bounds__(256) quantize_k_smooth_kernel(KSmoothArgs a) {
+  __shared__ float red[8];
+  __shared__ float smu[128];
+  const int64_t h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
+  const int64_t Np = pad128(a.q.N), nb = Np / 128;
+  const int64_t nv = valid_tokens(a.q.lens, b, a.q.N, a.q.status);
+  const int64_t bh = b * a.q.H + h;
+  if (threadIdx.x < 128) smu[threadIdx.x] = a.k_mean[bh * 128 + threadIdx.x];
+  __syncthreads();
+  const int col = (threadIdx.x & 15) * 8;
+  const int r0 = threadIdx.x >> 4;
+  float mu8[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mu8[k] = smu[col + k];
+  float y[8][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t n = blk * 128 + r0 + i * 16;
+    if (n < nv) {
+      float f[8];
+      unpack8(ldg_v4(a.q.x + b * a.q.sb + n * a.q.sn + h * a.q.sh + col), f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        y[i][k] = __fsub_rn(f[k], mu8[k]);
+        amax = fmaxf(amax, fabsf(y[i][k]));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) y[i][k] = 0.0f;
+    }
+  }
+  amax = block_max_256(amax, red);
+  const float s = __fdiv_rn(amax, 127.0f);
+  const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
+  if (threadIdx.x == 0) static_cast<float*>(a.q.scale)[bh * nb + blk] = s;
+  __half* out = static_cast<__half*>(a.q.out);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t n = blk * 128 + r0 + i * 16;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float c0 = 0.0f, c1 = 0.0f;
+      if (n < nv && s > 0.0f) {
+        c0 = int8_code(y[i][2 * k], s, inv);
+        c1 = int8_code(y[i][2 * k + 1], s, inv);
+      }
+      const __half2 h2 = __floats2half2_rn(c0, c1);  // exact: |c| <= 127
+      w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(out + (bh * Np + n) * 128 + col) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// ----------------------------------------------------------------------------
 // TMA-fed persistent variants. A grid of about two CTAs per SM walks the
 // 128-token blocks (head index fastest, so concurrent CTAs read contiguous
 // token rows); each block's 128 x 128 BF16 tile arrives by one 4-D TMA box
@@ -724,6 +903,143 @@ __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
   ring.drain(k, a.status);
 }
 
+// K smoothing pass 2, TMA-fed: fixed-point channel sums of each 128-token
+// block; the two row groups of a warp combine by a shuffle, the eight warps
+// through shared memory, then one int64 atomic per channel.
+__global__ void __launch_bounds__(256, 2) k_sum_tma_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                           KSmoothArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ long long red[8][128];
+  __shared__ int abort_flag;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  BlockRing<kQStages> ring;
+  ring.init(base, &abort_flag);
+  const int64_t nb = pad128(a.q.N) / 128, total = a.q.B * a.q.H * nb;
+  const int col = (threadIdx.x & 15) * 8;
+  const int rg = threadIdx.x >> 4;
+  for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmK, k, total, a.q.H, nb);
+  int64_t k = 0;
+  for (;; ++k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (i >= total) break;
+    ring.load(&tmK, k + kQStages - 1, total, a.q.H, nb);
+    const BlockCoord c = block_coord(i, a.q.H, nb);
+    const int64_t bh = c.b * a.q.H + c.h;
+    const int4 a0 = *reinterpret_cast<const int4*>(a.amax + bh * 128 + col);
+    const int4 a1 = *reinterpret_cast<const int4*>(a.amax + bh * 128 + col + 4);
+    const int ab[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    float2 c1[4], c2[4], hi[4], lo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      k_term_scales(ab[2 * q], c1[q].x, c2[q].x);
+      k_term_scales(ab[2 * q + 1], c1[q].y, c2[q].y);
+      hi[q] = lo[q] = make_float2(0.0f, 0.0f);
+    }
+    if (!ring.wait(k, &abort_flag, a.q.status)) break;
+    const int64_t nv = valid_tokens(a.q.lens, c.b, a.q.N, a.q.status);
+    const uint8_t* tile = ring.stage(k);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int rr = rg + 16 * j;
+      if (c.blk * 128 + rr < nv)
+        k_fixed_terms8(*reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2), c1, c2, hi, lo);
+    }
+    long long acc[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[2 * q] = k_term_sum(hi[q].x, lo[q].x);
+      acc[2 * q + 1] = k_term_sum(hi[q].y, lo[q].y);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], 16);
+    if ((threadIdx.x & 16) == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) red[threadIdx.x >> 5][col + q] = acc[q];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      long long t = 0;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) t += red[g][threadIdx.x];
+      if (t != 0) atomicAdd(&a.sum[bh * 128 + threadIdx.x], static_cast<unsigned long long>(t));
+    }
+    __syncthreads();  // stage and red[] free again
+  }
+  ring.drain(k, a.q.status);
+}
+
+// K smoothing pass 3, TMA-fed: y = k - mean (binary32), block maximum of |y|
+// over the valid rows, INT8 codes of y (as quantize_qk_tma_kernel<0>).
+__global__ void __launch_bounds__(256, 2) quantize_k_smooth_tma_kernel(
+    const __grid_constant__ CUtensorMap tmK, KSmoothArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float red[8];
+  __shared__ int abort_flag;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  BlockRing<kQStages> ring;
+  ring.init(base, &abort_flag);
+  const int64_t Np = pad128(a.q.N), nb = Np / 128, total = a.q.B * a.q.H * nb;
+  const int col = (threadIdx.x & 15) * 8;
+  const int r0 = threadIdx.x >> 4;
+  __half* out = static_cast<__half*>(a.q.out);
+  float* scale = static_cast<float*>(a.q.scale);
+  for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmK, k, total, a.q.H, nb);
+  int64_t k = 0;
+  for (;; ++k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (i >= total) break;
+    ring.load(&tmK, k + kQStages - 1, total, a.q.H, nb);
+    const BlockCoord c = block_coord(i, a.q.H, nb);
+    const int64_t bh = c.b * a.q.H + c.h;
+    const float4 m0 = *reinterpret_cast<const float4*>(a.k_mean + bh * 128 + col);
+    const float4 m1 = *reinterpret_cast<const float4*>(a.k_mean + bh * 128 + col + 4);
+    const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    if (!ring.wait(k, &abort_flag, a.q.status)) break;
+    const int64_t nv = valid_tokens(a.q.lens, c.b, a.q.N, a.q.status);
+    const uint8_t* tile = ring.stage(k);
+    float y[8][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int rr = r0 + 16 * j;
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2), f);
+      const bool valid = c.blk * 128 + rr < nv;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        y[j][q] = valid ? __fsub_rn(f[q], mu[q]) : 0.0f;
+        amax = fmaxf(amax, fabsf(y[j][q]));
+      }
+    }
+    amax = block_max_256(amax, red);
+    const float s = __fdiv_rn(amax, 127.0f);
+    const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
+    if (threadIdx.x == 0) scale[bh * nb + c.blk] = s;
+    __half* orow0 = out + (bh * Np + c.blk * 128 + r0) * 128 + col;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float dmax = 0.0f;
+      uint4 cw = int8_codes8f(y[j], inv, dmax);
+      if (!(dmax <= 0.5f - 0x1p-14f) && s > 0.0f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float n0 = fminf(fmaxf(round_rne(__fdiv_rn(y[j][2 * q], s)), -127.0f), 127.0f);
+          const float n1 = fminf(fmaxf(round_rne(__fdiv_rn(y[j][2 * q + 1], s)), -127.0f), 127.0f);
+          const __half2 h2 = __floats2half2_rn(n0, n1);
+          w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        cw = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
+    }
+    __syncthreads();  // stage k % kQStages (and red[]) free again
+  }
+  ring.drain(k, a.q.status);
+}
+
 }  // namespace
 
 namespace {
@@ -826,6 +1142,45 @@ cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s) {
   v_amax_kernel<<<grid, 256, 0, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   v_quantize_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_k_smooth(const QuantQKArgs& q, float* k_mean, void* workspace,
+                                     cudaStream_t s) {
+  KSmoothArgs a{q, k_mean, static_cast<unsigned long long*>(workspace), nullptr};
+  a.amax = reinterpret_cast<int*>(a.sum + q.B * q.H * 128);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, static_cast<size_t>(k_smooth_workspace_bytes(q.B, q.H)), s);
+  if (e != cudaSuccess) return e;
+  // pass 1: channel maxima of K (the V maxima kernels on the K tensor)
+  QuantVArgs va{q.x, q.sb, q.sn, q.sh, q.B, q.N, q.H, q.lens, nullptr, nullptr, a.amax, q.status};
+  const int64_t nb = pad128(q.N) / 128, blocks = q.B * q.H * nb;
+  const dim3 grid(static_cast<unsigned>(q.H), static_cast<unsigned>(nb), static_cast<unsigned>(q.B));
+  CUtensorMap m;
+  const bool tma = bnhd_map(&m, q.x, q.sb, q.sn, q.sh, q.B, q.N, q.H);
+  const int smem = kQStages * kBlockBytes + kQStages * 8 + 128;
+  if (tma) {
+    if ((e = set_smem<v_amax_tma_kernel>(smem)) != cudaSuccess) return e;
+    if ((e = set_smem<k_sum_tma_kernel>(smem)) != cudaSuccess) return e;
+    if ((e = set_smem<quantize_k_smooth_tma_kernel>(smem)) != cudaSuccess) return e;
+    v_amax_tma_kernel<<<persistent_grid(blocks), 256, smem, s>>>(m, va);
+  } else {
+    v_amax_kernel<<<grid, 256, 0, s>>>(va);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // pass 2: fixed-point channel sums
+  if (tma)
+    k_sum_tma_kernel<<<persistent_grid(blocks), 256, smem, s>>>(m, a);
+  else
+    k_sum_kernel<<<grid, 256, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // channel means (B * H * 128 threads)
+  k_mean_kernel<<<static_cast<unsigned>(q.B * q.H), 128, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // pass 3: subtract and encode
+  if (tma)
+    quantize_k_smooth_tma_kernel<<<persistent_grid(blocks), 256, smem, s>>>(m, a);
+  else
+    quantize_k_smooth_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

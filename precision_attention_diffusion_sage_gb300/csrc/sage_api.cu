@@ -106,6 +106,9 @@ size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int
     case 1:
       if (check_shape(B, Nk, H, D) != SAGE_OK) return 0;
       return static_cast<size_t>(v_workspace_bytes(B, H));
+    case 3:
+      if (fmt != SAGE_FMT_QK_INT8_V_FP8 || check_shape(B, Nk, H, D) != SAGE_OK) return 0;
+      return static_cast<size_t>(k_smooth_workspace_bytes(B, H));
     case 2: {
       if (check_shape(B, Nq, H, D) != SAGE_OK || check_shape(B, Nk, H, D) != SAGE_OK) return 0;
       const int64_t s = resolve_splits(num_splits, B, H, Nq, Nk);
@@ -156,6 +159,28 @@ sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64
   return from_cuda(launch_quantize_v(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+sage_status_t sage_quantize_k_smooth(sage_format_t fmt, const void* k, sage_strides_t ks,
+                                     int64_t B, int64_t N, int64_t H, int64_t D,
+                                     const int32_t* lens, void* k_q, void* k_scale,
+                                     float* k_mean, void* workspace, size_t ws_bytes,
+                                     sage_stream_t stream) {
+  if (fmt != SAGE_FMT_QK_INT8_V_FP8) return SAGE_ERR_UNSUPPORTED;
+  sage_status_t st = check_shape(B, N, H, D);
+  if (st != SAGE_OK) return st;
+  if (!k || !k_q || !k_scale || !k_mean || !aligned(k, 16) || !aligned(k_q, 16) ||
+      !aligned(k_scale, 4) || !aligned(k_mean, 16) || !strides_ok(ks) ||
+      (lens && !aligned(lens, 4)))
+    return SAGE_ERR_INVALID_ARG;
+  const size_t need = sage_workspace_bytes(3, fmt, B, H, N, N, D, 0);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return SAGE_ERR_WORKSPACE;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != SAGE_OK) return st;
+  QuantQKArgs a{static_cast<const uint16_t*>(k), ks.b, ks.n, ks.h, B, N, H, lens, k_q, k_scale,
+                status};
+  return from_cuda(launch_quantize_k_smooth(a, k_mean, workspace,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_scale,
                             const void* k_q, const void* k_scale, const void* v_q,
                             const float* v_scale, const int32_t* k_lens, int64_t B, int64_t H,
@@ -174,6 +199,10 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
       (lse && !aligned(lse, 4)) || (k_lens && !aligned(k_lens, 4)) || !strides_ok(os))
     return SAGE_ERR_INVALID_ARG;
   if (!(softmax_scale <= 0.0f) && !std::isfinite(softmax_scale)) return SAGE_ERR_INVALID_ARG;
+  const float* k_mean = opts ? opts->k_mean : nullptr;
+  if (k_mean && (fmt != SAGE_FMT_QK_INT8_V_FP8 || !aligned(k_mean, 16))) {
+    return fmt != SAGE_FMT_QK_INT8_V_FP8 ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_INVALID_ARG;
+  }
   const int req = opts ? opts->num_splits : 0;
   if (req < 0 || req > 64) return SAGE_ERR_INVALID_ARG;
   const int64_t splits = resolve_splits(req, B, H, Nq, Nk);
@@ -210,6 +239,7 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   p.osn = os.n;
   p.osh = os.h;
   p.lse = lse;
+  p.k_mean = k_mean;
   p.num_splits = static_cast<int>(splits);
   p.o_part = splits > 1 ? static_cast<float*>(workspace) : nullptr;
   p.lse_part = splits > 1 ? static_cast<float*>(workspace) + splits * B * H * Nq * D : nullptr;

@@ -25,6 +25,7 @@ class Workload:
     seed: int
     fmt: int = 0                      # 0: INT8, 1: MXFP4, 2: FP8, 3: rotated MXFP4 Q/K (V FP8)
     structure: str = "plain"
+    smooth_k: bool = False            # K smoothing (INT8 only): channel means removed from K
     k_lens: Optional[List[int]] = field(default=None)
     D: int = 128
 
@@ -56,6 +57,10 @@ WORKLOADS = {
                               structure="k_channels_x8"),
     "video_dit_fp8": Workload("video_dit_fp8", 1, 40, 14040, 14040, seed=2, fmt=2,
                               structure="k_mean"),
+    # video DiT with K smoothing: the per-channel K means (the workload's
+    # structure) taken out of K before INT8 quantization
+    "video_dit_ksmooth": Workload("video_dit_ksmooth", 1, 40, 14040, 14040, seed=2,
+                                  structure="k_mean", smooth_k=True),
     # Hadamard-rotated MXFP4 Q/K on the 8K shape, with the outlier-channel K
     # structure the rotation is meant to spread
     "mxfp4h_self": Workload("mxfp4h_self", 2, 24, 8192, 8192, seed=4, fmt=3,

@@ -493,3 +493,113 @@ def test_full_size_workload_mxfp4h():
     rows = _sample_rows(w.Nq)
     ro, rl = _oracle_attention(3, qz, kz, vz, w.Nq, w.Nk, rows=rows)
     assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+
+
+# ------------------------------------------------------------------ K smoothing (INT8)
+def _run_gpu_smooth(q, k, v, k_lens=None, num_splits=0, softmax_scale=None):
+    Nq, Nk = q.shape[1], k.shape[1]
+    qq, qs = binding.sage_quantize_qk(q, 0)
+    kq, ks, km = binding.sage_quantize_k_smooth(k, lens=k_lens)
+    vq, vs = binding.sage_quantize_v(v, lens=k_lens)
+    o, lse = binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
+                                   num_splits=num_splits, softmax_scale=softmax_scale, k_mean=km)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    return (qq, qs), (kq, ks, km), (vq, vs), o, lse
+
+
+def _assert_smooth_equal(kq, ks, km, rq, rs, rm):
+    assert_qk_equal(0, kq, ks, rq, rs)
+    np.testing.assert_array_equal(km.cpu().numpy().view(np.uint32), rm.view(np.uint32))
+
+
+@pytest.mark.parametrize("B,N,lens", [(1, 256, None), (1, 1, None), (1, 129, None),
+                                      (1, 300, [173]), (2, 512, [512, 0]), (2, 1000, [999, 64])])
+def test_quantize_k_smooth_bitexact(B, N, lens):
+    w = Workload("case", B, 2, N, N, seed=80 + N, structure="k_mean")
+    _, k, _ = make_qkv(w)
+    kq, ks, km = binding.sage_quantize_k_smooth(k.cuda(), lens=lens)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    _assert_smooth_equal(kq, ks, km, *oracle.quantize_int8_smooth(bf16_bits(k), lens=lens))
+
+
+def test_quantize_k_smooth_fixed_point_edges():
+    """Channel maxima 2^10 with terms below the 2^-30 grid (truncated toward
+    zero), cancelling pairs, all-zero channels, subnormal BF16 values and
+    huge values: the means and codes are bit-exact."""
+    x = np.zeros((1, 256, 1, 128), np.float32)
+    x[0, 0::2, 0, :] = 2.0 ** 10
+    x[0, 1::2, 0, :] = -(2.0 ** 10)
+    x[0, 5, 0, 0] = 3 * 2.0 ** -32
+    x[0, 7, 0, 1] = -3 * 2.0 ** -32
+    x[0, 9, 0, 2] = 2.0 ** -29
+    x[0, 11, 0, 3] = -5 * 2.0 ** -31
+    x[0, :, 0, 8:16] = 0.0
+    x[0, :, 0, 16] = 2.0 ** -130                      # subnormal BF16
+    x[0, 3, 0, 17] = -(2.0 ** -128)
+    x[0, :, 0, 18] = np.linspace(-3e38, 3e38, 256)    # near the BF16 maximum
+    g = torch.Generator().manual_seed(81)
+    x[0, :, 0, 32:] = (torch.randn(256, 96, generator=g) * 7 + 3).numpy()
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    kq, ks, km = binding.sage_quantize_k_smooth(t.cuda())
+    torch.cuda.synchronize()
+    _assert_smooth_equal(kq, ks, km, *oracle.quantize_int8_smooth(bf16_bits(t)))
+
+
+@pytest.mark.parametrize("Nq,Nk,splits", [(256, 256, 0), (300, 333, 0), (129, 1000, 3),
+                                          (513, 77, 0)])
+def test_attention_k_smooth(Nq, Nk, splits):
+    w = Workload("case", 1, 2, Nq, Nk, seed=Nq + 3 * Nk, structure="k_mean")
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    (qq, qs), (kq, ks, km), _, o, lse = _run_gpu_smooth(q, k, v, num_splits=splits)
+    qz = oracle.quantize_int8(bf16_bits(q))
+    rq, rs, rm = oracle.quantize_int8_smooth(bf16_bits(k))
+    vz = oracle.quantize_v_fp8(bf16_bits(v))
+    _assert_smooth_equal(kq, ks, km, rq, rs, rm)
+    ro, rl, _ = oracle.attention(0, *qz, rq, rs, *vz, Nq=Nq, Nk=Nk, k_mean=rm)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_k_smooth_cross_ragged_and_scale():
+    w = Workload("case", 2, 2, 300, 512, seed=82, structure="k_mean")
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    lens = [512, 300]
+    _, (kq, ks, km), _, o, lse = _run_gpu_smooth(q, k, v, k_lens=lens, softmax_scale=0.2)
+    qz = oracle.quantize_int8(bf16_bits(q))
+    rq, rs, rm = oracle.quantize_int8_smooth(bf16_bits(k), lens=lens)
+    vz = oracle.quantize_v_fp8(bf16_bits(v), lens=lens)
+    ro, rl, _ = oracle.attention(0, *qz, rq, rs, *vz, Nq=300, Nk=512, k_lens=lens,
+                                 softmax_scale=0.2, k_mean=rm)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_full_size_video_k_smooth():
+    w = WORKLOADS["video_dit"]
+    q, k, v = make_qkv(w, device="cuda")
+    (qq, qs), (kq, ks, km), (vq, vs), o, lse = _run_gpu_smooth(q, k, v)
+    hs = [0, 17, 39]
+    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
+    qz = oracle.quantize_int8(bf16_bits(sub(q)))
+    rq, rs, rm = oracle.quantize_int8_smooth(bf16_bits(sub(k)))
+    vz = oracle.quantize_v_fp8(bf16_bits(sub(v)))
+    assert_qk_equal(0, qq[:, hs], qs[:, hs], *qz)
+    _assert_smooth_equal(kq[:, hs], ks[:, hs], km[:, hs], rq, rs, rm)
+    rows = _sample_rows(w.Nq)
+    ro, rl, _ = oracle.attention(0, *qz, rq, rs, *vz, Nq=w.Nq, Nk=w.Nk, rows=rows, k_mean=rm)
+    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+
+
+def test_quantize_k_smooth_direct_load_path():
+    """A batch-broadcast K (batch stride 0) cannot be described by a tensor
+    map, so the direct-load kernels run; results equal the oracle's."""
+    w = Workload("case", 1, 3, 300, 300, seed=83, structure="k_mean")
+    _, k, _ = make_qkv(w)
+    kb = k.cuda().expand(2, -1, -1, -1)
+    assert kb.stride(0) == 0
+    lens = [300, 211]
+    kq, ks, km = binding.sage_quantize_k_smooth(kb, lens=lens)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    ref = oracle.quantize_int8_smooth(bf16_bits(k.expand(2, -1, -1, -1).contiguous()), lens=lens)
+    _assert_smooth_equal(kq, ks, km, *ref)

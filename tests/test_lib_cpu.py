@@ -52,6 +52,9 @@ def test_workspace_bytes():
     assert binding.sage_workspace_bytes(2, 0, 1, 2, 256, 1024, 128, 1) == 0
     # large grids need no split
     assert binding.sage_workspace_bytes(2, 0, 1, 40, 14040, 14040) == 0
+    # K smoothing: an int64 sum and a binary32 maximum per channel; INT8 only
+    assert binding.sage_workspace_bytes(3, 0, 2, 3, 300, 300) == 2 * 3 * 128 * 12
+    assert binding.sage_workspace_bytes(3, 1, 2, 3, 300, 300) == 0
 
 
 def _status(name):
@@ -83,6 +86,21 @@ def test_host_validation_rejects_before_launch():
     opts = binding.AttnOptions(4, 0)
     assert lib.sage_attn_fwd(0, fake, fake, fake, fake, fake, fake, None, 1, 1, 128, 1024, 128,
                              -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None) == -3
+    # K smoothing: INT8 only, needs its workspace and an aligned mean output
+    ws = ctypes.c_void_p(1 << 24)
+    assert lib.sage_quantize_k_smooth(1, fake, S, 1, 128, 1, 128, None, fake, fake, fake, ws,
+                                      1 << 20, None) == -2
+    assert lib.sage_quantize_k_smooth(0, fake, S, 1, 128, 1, 128, None, fake, fake, fake, None,
+                                      0, None) == -3
+    assert lib.sage_quantize_k_smooth(0, fake, S, 1, 128, 1, 128, None, fake, fake,
+                                      ctypes.c_void_p((1 << 20) + 4), ws, 1 << 20, None) == -1
+    # the channel means only go with the INT8 format, 16-byte aligned
+    opts = binding.AttnOptions(1, 0, 1 << 20)
+    assert lib.sage_attn_fwd(1, fake, fake, fake, fake, fake, fake, None, 1, 1, 128, 128, 128,
+                             -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None) == -2
+    opts = binding.AttnOptions(1, 0, (1 << 20) + 4)
+    assert lib.sage_attn_fwd(0, fake, fake, fake, fake, fake, fake, None, 1, 1, 128, 128, 128,
+                             -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None) == -1
 
 
 def test_status_strings():
