@@ -168,6 +168,24 @@ sage_status_t sage_quantize_v_noalloc(const void* v, sage_strides_t vs, int64_t 
                                       int64_t H, int64_t D, const int32_t* lens, void* v_q,
                                       float* v_scale, sage_stream_t stream);
 
+/* The pages this library restates have no counterpart to this entry point
+ * (they quantize Q, K and V with separate kernels).
+ * Q, K and V quantization in one call: the same results, bit for bit, as
+ *   sage_quantize_qk(fmt, q, qs, B, Nq, H, D, NULL, q_q, q_scale, stream);
+ *   sage_quantize_qk(fmt, k, ks, B, Nk, H, D, k_lens, k_q, k_scale, stream);
+ *   sage_quantize_v(v, vs, B, Nk, H, D, k_lens, v_q, v_scale, workspace, ws_bytes, stream);
+ * with the same argument rules, layouts and workspace (sage_workspace_bytes(1, ...)).
+ * For the INT8 and FP8 formats the Q and K quantization and V's channel maxima
+ * run as one persistent launch (fewer launches and no idle tail between the
+ * three), followed by the V encode; other formats, or inputs whose strides no
+ * TMA tensor map can describe, run the separate kernels. */
+sage_status_t sage_quantize_qkv(sage_format_t fmt, const void* q, sage_strides_t qs,
+                                const void* k, sage_strides_t ks, const void* v,
+                                sage_strides_t vs, int64_t B, int64_t Nq, int64_t Nk, int64_t H,
+                                int64_t D, const int32_t* k_lens, void* q_q, void* q_scale,
+                                void* k_q, void* k_scale, void* v_q, float* v_scale,
+                                void* workspace, size_t ws_bytes, sage_stream_t stream);
+
 /* K smoothing for the INT8 Q/K format (the "_q_smooth_int8_kernel" /
  * smoothing kernels named on "new MHA v4 entrypoint ..."; the pages give no
  * formula, so the reading is): subtract each channel's mean of K over the

@@ -50,6 +50,10 @@ _lib.sage_quantize_qk.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P,
 _lib.sage_quantize_v.restype = _I32
 _lib.sage_quantize_v.argtypes = [_P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
                                  ctypes.c_size_t, _P]
+_lib.sage_quantize_qkv.restype = _I32
+_lib.sage_quantize_qkv.argtypes = [_I32, _P, Strides, _P, Strides, _P, Strides, _I64, _I64, _I64,
+                                   _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                   _P]
 _lib.sage_quantize_k_smooth.restype = _I32
 _lib.sage_quantize_k_smooth.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
                                         _P, ctypes.c_size_t, _P]
@@ -180,6 +184,44 @@ def sage_quantize_v(v: torch.Tensor, lens=None, out: Optional[torch.Tensor] = No
     return out, scale
 
 
+def _qk_outputs(fmt: int, B: int, N: int, H: int, D: int, dev):
+    Np = pad128(N)
+    if fmt == FMT_INT8:
+        return (torch.empty((B, H, Np, D), dtype=torch.float16, device=dev),
+                torch.empty((B, H, Np // 128), dtype=torch.float32, device=dev))
+    if fmt == FMT_FP8:
+        return (torch.empty((B, H, Np, D), dtype=torch.uint8, device=dev),
+                torch.empty((B, H, Np // 128), dtype=torch.float32, device=dev))
+    return (torch.empty((B, H, Np, D // 2), dtype=torch.uint8, device=dev),
+            torch.empty((B, H, Np, D // 32), dtype=torch.uint8, device=dev))
+
+
+def sage_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: int = FMT_INT8,
+                      k_lens=None, outs=None, workspace: Optional[torch.Tensor] = None):
+    """Quantize Q, K, V in one library call (bit-identical to the three separate
+    calls). Returns ((q_q, q_scale), (k_q, k_scale), (v_q, v_scale)); `outs` may
+    supply those six tensors."""
+    B, Nq, H, D = q.shape
+    Nk = k.shape[1]
+    dev = q.device
+    if outs is None:
+        (qq, qs), (kq, ks) = _qk_outputs(fmt, B, Nq, H, D, dev), _qk_outputs(fmt, B, Nk, H, D, dev)
+        vq = torch.empty((B, H, D, pad128(Nk)), dtype=torch.uint8, device=dev)
+        vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    else:
+        (qq, qs), (kq, ks), (vq, vs) = outs
+    need = sage_workspace_bytes(1, fmt, B, H, Nk, Nk, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    ln = _lens_tensor(k_lens, dev)
+    _check(_lib.sage_quantize_qkv(fmt, _ptr(q), _bnhd_strides(q), _ptr(k), _bnhd_strides(k),
+                                  _ptr(v), _bnhd_strides(v), B, Nq, Nk, H, D, _ptr(ln), _ptr(qq),
+                                  _ptr(qs), _ptr(kq), _ptr(ks), _ptr(vq), _ptr(vs),
+                                  _ptr(workspace), workspace.numel(), _stream()),
+           "sage_quantize_qkv")
+    return (qq, qs), (kq, ks), (vq, vs)
+
+
 def sage_quantize_k_smooth(k: torch.Tensor, lens=None, out: Optional[torch.Tensor] = None,
                            scale: Optional[torch.Tensor] = None,
                            k_mean: Optional[torch.Tensor] = None,
@@ -242,18 +284,18 @@ def sage_last_device_status() -> int:
 def sage_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: int = FMT_INT8,
                    k_lens=None, softmax_scale: Optional[float] = None, num_splits: int = 0,
                    return_lse: bool = True, smooth_k: bool = False):
-    """Quantize Q/K/V and attend: the four library calls in order. smooth_k
+    """Quantize Q/K/V (one sage_quantize_qkv call) and attend. smooth_k
     (INT8 only) quantizes K with sage_quantize_k_smooth and passes its channel
     means to the attention call."""
     B, Nq, H, D = q.shape
     Nk = k.shape[1]
-    qq, qs = sage_quantize_qk(q, fmt)
     km = None
     if smooth_k:
+        qq, qs = sage_quantize_qk(q, fmt)
         kq, ks, km = sage_quantize_k_smooth(k, lens=k_lens)
+        vq, vs = sage_quantize_v(v, lens=k_lens)
     else:
-        kq, ks = sage_quantize_qk(k, fmt, lens=k_lens)
-    vq, vs = sage_quantize_v(v, lens=k_lens)
+        (qq, qs), (kq, ks), (vq, vs) = sage_quantize_qkv(q, k, v, fmt, k_lens=k_lens)
     return sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
                          softmax_scale=softmax_scale, num_splits=num_splits,
                          return_lse=return_lse, k_mean=km)

@@ -42,40 +42,4 @@ cudaError_t once_per_device(Setup setup) {
   return e;
 }
 
-// ---- launchers (defined in quantize.cu / attention.cu, called from sage_api.cu)
-struct QuantQKArgs {
-  const uint16_t* x;  // bf16 bits
-  int64_t sb, sn, sh;
-  int64_t B, N, H;
-  const int32_t* lens;
-  void* out;      // fp16-held int8 codes, e4m3 codes or packed e2m1
-  void* scale;    // float block scales or e8m0 bytes
-  int* status;
-};
-cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s);
-// rotate: Hadamard-transform each token row before quantizing.
-cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s, bool rotate);
-cudaError_t launch_quantize_qk_fp8(const QuantQKArgs& a, cudaStream_t s);
-
-struct QuantVArgs {
-  const uint16_t* v;
-  int64_t sb, sn, sh;
-  int64_t B, N, H;
-  const int32_t* lens;
-  uint8_t* out;   // [B][H][D][Npad]
-  float* scale;   // [B][H][D]
-  int* amax;      // [B][H][D] channel maxima as binary32 bit patterns (workspace)
-  int* status;
-};
-// Workspace of the V quantization: one int per (b, h, channel).
-inline int64_t v_workspace_bytes(int64_t B, int64_t H) { return B * H * 128 * 4; }
-cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s);
-
-// K smoothing workspace: an int64 sum and a binary32 maximum per (b, h, channel).
-inline int64_t k_smooth_workspace_bytes(int64_t B, int64_t H) { return B * H * 128 * 12; }
-// Smoothed INT8 K: channel means of K over the valid tokens (k_mean, float
-// [B][H][128]) subtracted before the INT8 block quantization into q.out/q.scale.
-cudaError_t launch_quantize_k_smooth(const QuantQKArgs& q, float* k_mean, void* workspace,
-                                     cudaStream_t s);
-
 }  // namespace sage

@@ -18,7 +18,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "common.cuh"
+#include "quantize.cuh"
 #include "sm103_ptx.cuh"
 
 namespace sage {
@@ -694,6 +694,96 @@ struct BlockRing {
   }
 };
 
+// One 128-token block of Q or K (CODE as quantize_qk_block_kernel) from its
+// staged 128 x 128 BF16 tile: block maximum, scale, codes. Every thread of
+// the CTA calls it; red[] is free again after the caller's next barrier.
+template <int CODE>
+__device__ __forceinline__ void qk_block_from_tile(const uint8_t* tile, const BlockCoord& c,
+                                                   int64_t nv, const QuantQKArgs& a, float* red) {
+  const int64_t Np = pad128(a.N), nb = Np / 128;
+  const int col = (threadIdx.x & 15) * 8;
+  const int r0 = threadIdx.x >> 4;
+  uint4 raw[8];
+  uint32_t am2 = 0;  // packed BF16 |x| maximum
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int rr = r0 + 16 * j;
+    raw[j] = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
+    if (c.blk * 128 + rr >= nv) raw[j] = make_uint4(0, 0, 0, 0);
+    am2 = bf16x2_absmax(am2, raw[j].x);
+    am2 = bf16x2_absmax(am2, raw[j].y);
+    am2 = bf16x2_absmax(am2, raw[j].z);
+    am2 = bf16x2_absmax(am2, raw[j].w);
+  }
+  const float amax = block_max_256(bf16x2_hmax(am2), red);
+  const float s = __fdiv_rn(amax, CODE == 0 ? 127.0f : 448.0f);
+  const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
+  const int64_t bh = c.b * a.H + c.h;
+  if (threadIdx.x == 0) static_cast<float*>(a.scale)[bh * nb + c.blk] = s;
+  if constexpr (CODE == 0) {
+    __half* orow0 = static_cast<__half*>(a.out) + (bh * Np + c.blk * 128 + r0) * 128 + col;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float dmax = 0.0f;
+      uint4 cw = int8_codes8(raw[j], inv, dmax);
+      if (!(dmax <= 0.5f - 0x1p-14f) && s > 0.0f) {
+        float f[8];
+        unpack8(raw[j], f);
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float n0 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q], s)), -127.0f), 127.0f);
+          const float n1 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q + 1], s)), -127.0f), 127.0f);
+          const __half2 h2 = __floats2half2_rn(n0, n1);
+          w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        cw = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
+    }
+  } else {
+    uint8_t* orow0 = static_cast<uint8_t*>(a.out) + (bh * Np + c.blk * 128 + r0) * 128 + col;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint2 cw = s > 0.0f ? fp8_codes8(raw[j], s, inv) : make_uint2(0, 0);
+      *reinterpret_cast<uint2*>(orow0 + j * 16 * 128) = cw;
+    }
+  }
+}
+
+// Channel maxima of one 128-token block of V from its staged tile, folded
+// into the per-(b,h) words. red16 is free again after the caller's next
+// barrier.
+__device__ __forceinline__ void v_amax_from_tile(const uint8_t* tile, const BlockCoord& c,
+                                                 int64_t nv, const QuantVArgs& a,
+                                                 float (*red16)[128]) {
+  const int col = (threadIdx.x & 15) * 8;
+  const int rg = threadIdx.x >> 4;
+  uint4 m2 = make_uint4(0, 0, 0, 0);  // packed BF16 |x| maxima of 8 channels
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int rr = rg + 16 * j;
+    if (c.blk * 128 + rr < nv) {
+      const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
+      m2.x = bf16x2_absmax(m2.x, w.x);
+      m2.y = bf16x2_absmax(m2.y, w.y);
+      m2.z = bf16x2_absmax(m2.z, w.z);
+      m2.w = bf16x2_absmax(m2.w, w.w);
+    }
+  }
+  float m[8];
+  unpack8(m2, m);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) red16[rg][col + q] = m[q];
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    float r = red16[0][threadIdx.x];
+#pragma unroll
+    for (int g = 1; g < 16; ++g) r = fmaxf(r, red16[g][threadIdx.x]);
+    if (r > 0.0f) atomicMax(&a.amax[(c.b * a.H + c.h) * 128 + threadIdx.x], __float_as_int(r));
+  }
+}
+
 template <int CODE>  // as quantize_qk_block_kernel
 __global__ void __launch_bounds__(256, 2) quantize_qk_tma_kernel(
     const __grid_constant__ CUtensorMap tmX, QuantQKArgs a) {
@@ -704,11 +794,7 @@ __global__ void __launch_bounds__(256, 2) quantize_qk_tma_kernel(
                                              ~static_cast<uintptr_t>(127));
   BlockRing<kQStages> ring;
   ring.init(base, &abort_flag);
-  const int64_t Np = pad128(a.N), nb = Np / 128, total = a.B * a.H * nb;
-  const int col = (threadIdx.x & 15) * 8;
-  const int r0 = threadIdx.x >> 4;
-  __half* out = static_cast<__half*>(a.out);  // CODE 0
-  float* scale = static_cast<float*>(a.scale);
+  const int64_t nb = pad128(a.N) / 128, total = a.B * a.H * nb;
   for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmX, k, total, a.H, nb);
   int64_t k = 0;
   for (;; ++k) {
@@ -717,54 +803,7 @@ __global__ void __launch_bounds__(256, 2) quantize_qk_tma_kernel(
     ring.load(&tmX, k + kQStages - 1, total, a.H, nb);
     if (!ring.wait(k, &abort_flag, a.status)) break;
     const BlockCoord c = block_coord(i, a.H, nb);
-    const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
-    const uint8_t* tile = ring.stage(k);
-    uint4 raw[8];
-    uint32_t am2 = 0;  // packed BF16 |x| maximum
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int rr = r0 + 16 * j;
-      raw[j] = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
-      if (c.blk * 128 + rr >= nv) raw[j] = make_uint4(0, 0, 0, 0);
-      am2 = bf16x2_absmax(am2, raw[j].x);
-      am2 = bf16x2_absmax(am2, raw[j].y);
-      am2 = bf16x2_absmax(am2, raw[j].z);
-      am2 = bf16x2_absmax(am2, raw[j].w);
-    }
-    const float amax = block_max_256(bf16x2_hmax(am2), red);
-    const float s = __fdiv_rn(amax, CODE == 0 ? 127.0f : 448.0f);
-    const float inv = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    const int64_t bh = c.b * a.H + c.h;
-    if (threadIdx.x == 0) scale[bh * nb + c.blk] = s;
-    if constexpr (CODE == 0) {
-      __half* orow0 = out + (bh * Np + c.blk * 128 + r0) * 128 + col;
-  #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float dmax = 0.0f;
-        uint4 cw = int8_codes8(raw[j], inv, dmax);
-        if (!(dmax <= 0.5f - 0x1p-14f) && s > 0.0f) {
-          float f[8];
-          unpack8(raw[j], f);
-          uint32_t w[4];
-  #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float n0 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q], s)), -127.0f), 127.0f);
-            const float n1 = fminf(fmaxf(round_rne(__fdiv_rn(f[2 * q + 1], s)), -127.0f), 127.0f);
-            const __half2 h2 = __floats2half2_rn(n0, n1);
-            w[q] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          cw = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
-      }
-    } else {
-      uint8_t* orow0 = static_cast<uint8_t*>(a.out) + (bh * Np + c.blk * 128 + r0) * 128 + col;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint2 cw = s > 0.0f ? fp8_codes8(raw[j], s, inv) : make_uint2(0, 0);
-        *reinterpret_cast<uint2*>(orow0 + j * 16 * 128) = cw;
-      }
-    }
+    qk_block_from_tile<CODE>(ring.stage(k), c, valid_tokens(a.lens, c.b, a.N, a.status), a, red);
     __syncthreads();  // stage k % kQStages (and red[]) free again
   }
   ring.drain(k, a.status);
@@ -780,8 +819,6 @@ __global__ void __launch_bounds__(256, 2) v_amax_tma_kernel(const __grid_constan
   BlockRing<kQStages> ring;
   ring.init(base, &abort_flag);
   const int64_t nb = pad128(a.N) / 128, total = a.B * a.H * nb;
-  const int col = (threadIdx.x & 15) * 8;
-  const int rg = threadIdx.x >> 4;
   for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmV, k, total, a.H, nb);
   int64_t k = 0;
   for (;; ++k) {
@@ -790,38 +827,84 @@ __global__ void __launch_bounds__(256, 2) v_amax_tma_kernel(const __grid_constan
     ring.load(&tmV, k + kQStages - 1, total, a.H, nb);
     if (!ring.wait(k, &abort_flag, a.status)) break;
     const BlockCoord c = block_coord(i, a.H, nb);
-    const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
-    const uint8_t* tile = ring.stage(k);
-    uint4 m2 = make_uint4(0, 0, 0, 0);  // packed BF16 |x| maxima of 8 channels
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int rr = rg + 16 * j;
-      if (c.blk * 128 + rr < nv) {
-        const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
-        m2.x = bf16x2_absmax(m2.x, w.x);
-        m2.y = bf16x2_absmax(m2.y, w.y);
-        m2.z = bf16x2_absmax(m2.z, w.z);
-        m2.w = bf16x2_absmax(m2.w, w.w);
-      }
-    }
-    float m[8];
-    unpack8(m2, m);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) red[rg][col + q] = m[q];
-    __syncthreads();
-    if (threadIdx.x < 128) {
-      float r = red[0][threadIdx.x];
-#pragma unroll
-      for (int g = 1; g < 16; ++g) r = fmaxf(r, red[g][threadIdx.x]);
-      if (r > 0.0f) atomicMax(&a.amax[(c.b * a.H + c.h) * 128 + threadIdx.x], __float_as_int(r));
-    }
+    v_amax_from_tile(ring.stage(k), c, valid_tokens(a.lens, c.b, a.N, a.status), a, red);
     __syncthreads();
   }
   ring.drain(k, a.status);
 }
 
+// One pass over Q, K and V (INT8 or FP8 Q/K codes, V channel maxima): the
+// items are Q's 128-token blocks, then K's, then V's, each staged by TMA from
+// its own tensor map into the one ring; the V encode runs after it.
+struct FusedQuantArgs {
+  QuantQKArgs q, k;
+  QuantVArgs v;
+};
+
+template <int CODE>
+__global__ void __launch_bounds__(256, 2) quantize_qkv_tma_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmV, FusedQuantArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float red[16][128];
+  __shared__ int abort_flag;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  BlockRing<kQStages> ring;
+  ring.init(base, &abort_flag);
+  const int64_t nbq = pad128(a.q.N) / 128, nbk = pad128(a.k.N) / 128;
+  const int64_t nQ = a.q.B * a.q.H * nbq, nK = a.k.B * a.k.H * nbk, total = nQ + 2 * nK;
+  // Thread 0: stage this CTA's k-th item (if it exists).
+  auto load = [&](int64_t k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (threadIdx.x != 0 || i >= total) return;
+    const CUtensorMap* map;
+    BlockCoord c;
+    if (i < nQ) {
+      map = &tmQ;
+      c = block_coord(i, a.q.H, nbq);
+    } else {
+      map = i < nQ + nK ? &tmK : &tmV;
+      c = block_coord((i - nQ) % nK, a.k.H, nbk);
+    }
+    const int st = static_cast<int>(k % kQStages);
+    mbar_arrive_expect_tx(&ring.full[st], kBlockBytes);
+    tma_load_4d(ring.stage(k), map, &ring.full[st], 0, static_cast<int32_t>(c.h),
+                static_cast<int32_t>(c.blk * 128), static_cast<int32_t>(c.b));
+    ++ring.issued;
+  };
+  for (int k = 0; k < kQStages - 1; ++k) load(k);
+  int64_t k = 0;
+  for (;; ++k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    if (i >= total) break;
+    load(k + kQStages - 1);
+    if (!ring.wait(k, &abort_flag, a.q.status)) break;
+    const uint8_t* tile = ring.stage(k);
+    if (i < nQ) {
+      const BlockCoord c = block_coord(i, a.q.H, nbq);
+      qk_block_from_tile<CODE>(tile, c, valid_tokens(a.q.lens, c.b, a.q.N, a.q.status), a.q,
+                               &red[0][0]);
+    } else if (i < nQ + nK) {
+      const BlockCoord c = block_coord(i - nQ, a.k.H, nbk);
+      qk_block_from_tile<CODE>(tile, c, valid_tokens(a.k.lens, c.b, a.k.N, a.k.status), a.k,
+                               &red[0][0]);
+    } else {
+      const BlockCoord c = block_coord(i - nQ - nK, a.v.H, nbk);
+      v_amax_from_tile(tile, c, valid_tokens(a.v.lens, c.b, a.v.N, a.v.status), a.v, red);
+    }
+    __syncthreads();  // stage k % kQStages and red[] free again
+  }
+  ring.drain(k, a.q.status);
+}
+
 constexpr int kVStages = 2;
 
+// V encode, TMA-fed: thread t owns channels d = 2 (t % 64), d + 1 and tokens
+// 32 (t / 64) .. + 31 of the staged block. Its 4-byte shared loads (one token,
+// both channels) are conflict-free across a warp; each channel's 32 codes
+// (E4M3 of the binary32 quotient v / s_d, exact as in e4m3x2_fast) go out as
+// two 16-byte stores into that channel's token-contiguous row.
 __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
     const __grid_constant__ CUtensorMap tmV, QuantVArgs a) {
   constexpr int kPitchWords = 33;
@@ -1102,6 +1185,40 @@ cudaError_t launch_quantize_qk_block(const QuantQKArgs& a, cudaStream_t s) {
             static_cast<unsigned>(a.B));
   quantize_qk_block_kernel<CODE><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+// Q, K and V in two launches (after the clear of V's channel maxima): the
+// fused Q/K quantize + V maxima pass, then the V encode. Inputs a tensor map
+// cannot describe take the separate launches.
+template <int CODE>
+cudaError_t launch_quantize_qkv_code(const QuantQKArgs& q, const QuantQKArgs& k,
+                                     const QuantVArgs& v, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  if (!bnhd_map(&mq, q.x, q.sb, q.sn, q.sh, q.B, q.N, q.H) ||
+      !bnhd_map(&mk, k.x, k.sb, k.sn, k.sh, k.B, k.N, k.H) ||
+      !bnhd_map(&mv, v.v, v.sb, v.sn, v.sh, v.B, v.N, v.H)) {
+    cudaError_t e = launch_quantize_qk_block<CODE>(q, s);
+    if (e == cudaSuccess) e = launch_quantize_qk_block<CODE>(k, s);
+    if (e == cudaSuccess) e = launch_quantize_v(v, s);
+    return e;
+  }
+  cudaError_t e = cudaMemsetAsync(v.amax, 0, static_cast<size_t>(v_workspace_bytes(v.B, v.H)), s);
+  if (e != cudaSuccess) return e;
+  const int smem1 = kQStages * kBlockBytes + kQStages * 8 + 128;
+  const int smem2 = kVStages * kBlockBytes + kVStages * 8 + 128;
+  if ((e = set_smem<quantize_qkv_tma_kernel<CODE>>(smem1)) != cudaSuccess) return e;
+  if ((e = set_smem<v_quantize_tma_kernel>(smem2)) != cudaSuccess) return e;
+  const int64_t nQ = q.B * q.H * (pad128(q.N) / 128), nV = v.B * v.H * (pad128(v.N) / 128);
+  quantize_qkv_tma_kernel<CODE><<<persistent_grid(nQ + 2 * nV), 256, smem1, s>>>(
+      mq, mk, mv, FusedQuantArgs{q, k, v});
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  v_quantize_tma_kernel<<<persistent_grid(nV), 256, smem2, s>>>(mv, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_qkv(bool fp8, const QuantQKArgs& q, const QuantQKArgs& k,
+                                const QuantVArgs& v, cudaStream_t s) {
+  return fp8 ? launch_quantize_qkv_code<1>(q, k, v, s) : launch_quantize_qkv_code<0>(q, k, v, s);
 }
 
 cudaError_t launch_quantize_qk_int8(const QuantQKArgs& a, cudaStream_t s) {

@@ -7,7 +7,7 @@
 
 #include "../../include/sage.h"
 #include "attention.cuh"
-#include "common.cuh"
+#include "quantize.cuh"
 
 namespace sage {
 namespace {
@@ -157,6 +157,42 @@ sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64
   QuantVArgs a{static_cast<const uint16_t*>(v), vs.b, vs.n, vs.h, B, N, H, lens,
                static_cast<uint8_t*>(v_q), v_scale, static_cast<int*>(workspace), status};
   return from_cuda(launch_quantize_v(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sage_status_t sage_quantize_qkv(sage_format_t fmt, const void* q, sage_strides_t qs,
+                                const void* k, sage_strides_t ks, const void* v,
+                                sage_strides_t vs, int64_t B, int64_t Nq, int64_t Nk, int64_t H,
+                                int64_t D, const int32_t* k_lens, void* q_q, void* q_scale,
+                                void* k_q, void* k_scale, void* v_q, float* v_scale,
+                                void* workspace, size_t ws_bytes, sage_stream_t stream) {
+  if (!known_format(fmt)) return SAGE_ERR_UNSUPPORTED;
+  sage_status_t st = check_shape(B, Nq, H, D);
+  if (st != SAGE_OK) return st;
+  if ((st = check_shape(B, Nk, H, D)) != SAGE_OK) return st;
+  if (!q || !k || !v || !q_q || !q_scale || !k_q || !k_scale || !v_q || !v_scale ||
+      !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_q, 16) ||
+      !aligned(k_q, 16) || !aligned(v_q, 16) || !aligned(q_scale, 4) || !aligned(k_scale, 4) ||
+      !aligned(v_scale, 4) || !strides_ok(qs) || !strides_ok(ks) || !strides_ok(vs) ||
+      (k_lens && !aligned(k_lens, 4)))
+    return SAGE_ERR_INVALID_ARG;
+  const size_t need = sage_workspace_bytes(1, fmt, B, H, Nk, Nk, D, 0);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return SAGE_ERR_WORKSPACE;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != SAGE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  QuantQKArgs aq{static_cast<const uint16_t*>(q), qs.b, qs.n, qs.h, B, Nq, H, nullptr, q_q,
+                 q_scale, status};
+  QuantQKArgs ak{static_cast<const uint16_t*>(k), ks.b, ks.n, ks.h, B, Nk, H, k_lens, k_q,
+                 k_scale, status};
+  QuantVArgs av{static_cast<const uint16_t*>(v), vs.b, vs.n, vs.h, B, Nk, H, k_lens,
+                static_cast<uint8_t*>(v_q), v_scale, static_cast<int*>(workspace), status};
+  if (fmt == SAGE_FMT_QK_INT8_V_FP8 || fmt == SAGE_FMT_QK_FP8_V_FP8)
+    return from_cuda(launch_quantize_qkv(fmt == SAGE_FMT_QK_FP8_V_FP8, aq, ak, av, s));
+  const bool rot = fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
+  cudaError_t e = launch_quantize_qk_mxfp4(aq, s, rot);
+  if (e == cudaSuccess) e = launch_quantize_qk_mxfp4(ak, s, rot);
+  if (e == cudaSuccess) e = launch_quantize_v(av, s);
+  return from_cuda(e);
 }
 
 sage_status_t sage_quantize_k_smooth(sage_format_t fmt, const void* k, sage_strides_t ks,

@@ -603,3 +603,41 @@ def test_quantize_k_smooth_direct_load_path():
     assert binding.sage_last_device_status() == 0
     ref = oracle.quantize_int8_smooth(bf16_bits(k.expand(2, -1, -1, -1).contiguous()), lens=lens)
     _assert_smooth_equal(kq, ks, km, *ref)
+
+
+# ------------------------------------------------------------------ one-call Q/K/V quantization
+@pytest.mark.parametrize("fmt", [0, 2, 1, 3])
+@pytest.mark.parametrize("B,Nq,Nk,lens", [(1, 300, 300, None), (2, 257, 512, [512, 300]),
+                                          (2, 129, 1000, [0, 999])])
+def test_quantize_qkv_equals_separate_calls_and_oracle(fmt, B, Nq, Nk, lens):
+    w = Workload("case", B, 3, Nq, Nk, seed=90 + Nq + fmt, structure="k_channels_x8")
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    (qq, qs), (kq, ks), (vq, vs) = binding.sage_quantize_qkv(q, k, v, fmt, k_lens=lens)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    sq = binding.sage_quantize_qk(q, fmt)
+    sk = binding.sage_quantize_qk(k, fmt, lens=lens)
+    sv = binding.sage_quantize_v(v, lens=lens)
+    for a, b in zip((qq, qs, kq, ks, vq, vs), (*sq, *sk, *sv)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    qz, kz, vz = oracle_quantize(fmt, q, k, v, k_lens=lens)
+    assert_qk_equal(fmt, qq, qs, *qz)
+    assert_qk_equal(fmt, kq, ks, *kz)
+    assert_v_equal(vq, vs, *vz)
+
+
+def test_quantize_qkv_packed_and_broadcast_layouts():
+    """Q/K/V as views of one packed [B, N, 3, H, D] tensor (tensor maps apply)
+    and a batch-broadcast V (stride 0: the separate kernels run)."""
+    g = torch.Generator(device="cuda").manual_seed(91)
+    qkv = torch.randn(2, 384, 3, 4, 128, generator=g, device="cuda").to(torch.bfloat16)
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    vb = v[:1].expand(2, -1, -1, -1)
+    for vv in (v, vb):
+        outs = binding.sage_quantize_qkv(q, k, vv, 0, k_lens=[384, 200])
+        torch.cuda.synchronize()
+        assert binding.sage_last_device_status() == 0
+        qz, kz, vz = oracle_quantize(0, q, k, vv, k_lens=[384, 200])
+        assert_qk_equal(0, *outs[0], *qz)
+        assert_qk_equal(0, *outs[1], *kz)
+        assert_v_equal(*outs[2], *vz)
