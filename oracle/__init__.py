@@ -64,7 +64,8 @@ def _L():
         lib.oracle_bf16_from_double.argtypes = [D]
         q_args = [P, I64, I64, I64, I64, I64, I64, I64, P, P, P]
         for name in ("oracle_quantize_int8", "oracle_quantize_v_fp8", "oracle_quantize_mxfp4",
-                     "oracle_quantize_fp8_qk", "oracle_quantize_mxfp4_hadamard"):
+                     "oracle_quantize_fp8_qk", "oracle_quantize_mxfp4_hadamard",
+                     "oracle_quantize_v_mxfp4"):
             getattr(lib, name).restype = None
             getattr(lib, name).argtypes = q_args
         lib.oracle_k_mean.restype = None
@@ -159,6 +160,18 @@ def quantize_v_fp8(v: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
     return v8, sv
 
 
+def quantize_v_mxfp4(v: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
+    """MXFP4 V along tokens: codes [B,H,D,Npad/2] (token 2i in the low nibble)
+    and E8M0 bytes [B,H,Npad/128,D,4] (32-token blocks, per 128-token tile)."""
+    B, N, H, D, sb, sn, sh = _bnhd(v)
+    Np = pad128(N)
+    c = np.zeros((B, H, D, Np // 2), np.uint8)
+    e = np.zeros((B, H, Np // 128, D, 4), np.uint8)
+    ln = _lens(lens)
+    _L().oracle_quantize_v_mxfp4(_ptr(v), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(c), _ptr(e))
+    return c, e
+
+
 def fwht128(x: np.ndarray) -> np.ndarray:
     """Binary32 fast Walsh-Hadamard transform of the last axis (length 128)."""
     xin = np.ascontiguousarray(x, dtype=np.float32)
@@ -245,7 +258,8 @@ def quantize_mxfp4(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
 def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: int = 128,
               softmax_scale: Optional[float] = None, k_lens=None, rows=None,
               want_weights: bool = False, nthreads: int = 0, k_mean=None):
-    """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K; fmt 2: E4M3 Q/K. V is E4M3.
+    """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K; fmt 2: E4M3 Q/K (V E4M3);
+    fmt 4: MXFP4 Q/K with MXFP4 V (quantize_v_mxfp4) and MXFP4 P per 32 keys.
 
     k_mean (fmt 0 only): the channel means that K smoothing subtracted before
     quantizing K; O is that of the smoothed logits and LSE adds back the

@@ -450,6 +450,46 @@ void oracle_quantize_mxfp4(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh
   }
 }
 
+// MXFP4 V along tokens (the sage_quant_v_mxfp4_colmajor preprocessing named on
+// "new MHA v4 entrypoint ..."): for each (b, h, channel) and 32 consecutive
+// tokens, the OCP MX rule of oracle_quantize_mxfp4 over the valid tokens'
+// values; tokens past the valid length are zero codes and stay out of the
+// maximum. codes: [B][H][D][Npad/2], token 2i in the low nibble; e8m0:
+// [B][H][Npad/128][D][4], per 128-token tile the four block bytes of each
+// channel.
+void oracle_quantize_v_mxfp4(const uint16_t* v, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+                             int64_t N, int64_t H, int64_t D, const int32_t* lens,
+                             uint8_t* codes, uint8_t* e8m0) {
+  const int64_t Np = pad128(N), nb = Np / 128;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t nv = valid_len(lens, b, N);
+    for (int64_t h = 0; h < H; ++h)
+      for (int64_t d = 0; d < D; ++d)
+        for (int64_t blk = 0; blk < Np / 32; ++blk) {
+          float amax = 0.0f;
+          for (int64_t n = blk * 32; n < blk * 32 + 32 && n < nv; ++n)
+            amax = std::max(amax, std::fabs(bf16_to_float(v[b * sb + n * sn + h * sh + d])));
+          int byte = 0;
+          if (amax > 0.0f) {
+            int k;
+            std::frexp(static_cast<double>(amax), &k);  // floor(log2 amax) = k - 1
+            byte = std::min(254, std::max(0, (k - 1) - 2 + 127));
+          }
+          e8m0[(((b * H + h) * nb + blk / 4) * D + d) * 4 + blk % 4] = static_cast<uint8_t>(byte);
+          const double X = std::ldexp(1.0, byte - 127);
+          uint8_t* crow = codes + ((b * H + h) * D + d) * (Np / 2);
+          for (int64_t n = blk * 32; n < blk * 32 + 32; n += 2) {
+            uint8_t c[2] = {0, 0};
+            for (int i = 0; i < 2; ++i)
+              if (n + i < nv)
+                c[i] = oracle_e2m1_encode(
+                    static_cast<double>(bf16_to_float(v[b * sb + (n + i) * sn + h * sh + d])) / X);
+            crow[n / 2] = static_cast<uint8_t>(c[0] | (c[1] << 4));
+          }
+        }
+  }
+}
+
 // ---------------------------------------------------------------- attention
 void oracle_attention(int fmt, const void* q_data, const void* q_scale, const void* k_data,
                       const void* k_scale, const uint8_t* v8, const float* sv,
@@ -517,17 +557,48 @@ void oracle_attention(int fmt, const void* q_data, const void* q_scale, const vo
     for (int64_t j = 0; j < nk; ++j) tmax = std::max(tmax, t[j]);
     const double M = std::ceil(tmax);  // integer row maximum
     double l = 0.0;
-    std::vector<double> pdq(nk);
+    std::vector<double> p(nk), pdq(nk);
     for (int64_t j = 0; j < nk; ++j) {
-      const double p = std::exp2(t[j] - M);
-      l += p;
-      pdq[j] = oracle_e4m3_decode(oracle_e4m3_encode(p * 256.0)) / 256.0;
+      p[j] = std::exp2(t[j] - M);
+      l += p[j];
     }
-    const uint8_t* vb = v8 + bh * D * Nkp;
-    for (int64_t d = 0; d < D; ++d) {
-      double acc = 0.0;
-      for (int64_t j = 0; j < nk; ++j) acc += pdq[j] * oracle_e4m3_decode(vb[d * Nkp + j]);
-      orow[d] = acc * static_cast<double>(sv[bh * D + d]) / l;
+    if (fmt != 4) {
+      for (int64_t j = 0; j < nk; ++j)
+        pdq[j] = oracle_e4m3_decode(oracle_e4m3_encode(p[j] * 256.0)) / 256.0;
+      const uint8_t* vb = v8 + bh * D * Nkp;
+      for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < nk; ++j) acc += pdq[j] * oracle_e4m3_decode(vb[d * Nkp + j]);
+        orow[d] = acc * static_cast<double>(sv[bh * D + d]) / l;
+      }
+    } else {
+      // MXFP4 P: per 32 keys of the row, the OCP MX rule on the probabilities
+      // (shared exponent floor(log2 max p) - 2, E2M1 elements).
+      for (int64_t j0 = 0; j0 < nk; j0 += 32) {
+        const int64_t j1 = std::min(j0 + 32, nk);
+        double pmax = 0.0;
+        for (int64_t j = j0; j < j1; ++j) pmax = std::max(pmax, p[j]);
+        int byte = 0;
+        if (pmax > 0.0) {
+          int k;
+          std::frexp(pmax, &k);
+          byte = std::min(254, std::max(0, (k - 1) - 2 + 127));
+        }
+        const double X = std::ldexp(1.0, byte - 127);
+        for (int64_t j = j0; j < j1; ++j) pdq[j] = oracle_e2m1_decode(oracle_e2m1_encode(p[j] / X)) * X;
+      }
+      // MXFP4 V: codes [B][H][D][Nk_pad/2], E8M0 [B][H][Nk_pad/128][D][4].
+      const uint8_t* vc = v8 + bh * D * (Nkp / 2);
+      const uint8_t* ve = reinterpret_cast<const uint8_t*>(sv) + bh * (Nkp / 128) * D * 4;
+      for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
+          const uint8_t c = (vc[d * (Nkp / 2) + j / 2] >> ((j & 1) * 4)) & 0xF;
+          const int byte = ve[((j / 128) * D + d) * 4 + (j % 128) / 32];
+          acc += pdq[j] * oracle_e2m1_decode(c) * std::ldexp(1.0, byte - 127);
+        }
+        orow[d] = acc / l;
+      }
     }
     lse[idx] = (M + std::log2(l)) * kLn2;
     if (wrow)

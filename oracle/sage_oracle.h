@@ -80,14 +80,26 @@ void oracle_k_mean_lse_term(const int8_t* q, const float* q_scale, const float* 
                             int64_t H, int64_t Nq, int64_t D, double softmax_scale,
                             const int64_t* rows, int64_t nrows, double* term);
 
+/* MXFP4 V along tokens: per (b, h, channel) and 32 consecutive tokens the
+ * MXFP4 rule over the valid tokens (others zero codes, out of the maximum).
+ * codes: uint8 [B][H][D][Npad/2] (token 2i in the low nibble);
+ * e8m0: uint8 [B][H][Npad/128][D][4]. */
+void oracle_quantize_v_mxfp4(const uint16_t* v, int64_t sb, int64_t sn, int64_t sh, int64_t B,
+                             int64_t N, int64_t H, int64_t D, const int32_t* lens,
+                             uint8_t* codes, uint8_t* e8m0);
+
 /* ---- attention ---- */
 /* fmt 0: q_data/k_data are int8 [B][H][Npad][D] with float block scales
  *        [B][H][Npad/128];
  * fmt 1: q_data/k_data are MXFP4 codes [B][H][Npad][D/2] with e8m0 scales
  *        [B][H][Npad][D/32] (passed through q_scale/k_scale as bytes);
  * fmt 2: q_data/k_data are E4M3 codes [B][H][Npad][D] with float block
- *        scales [B][H][Npad/128].
- * V: fp8 [B][H][D][Nk_pad] + sv [B][H][D].
+ *        scales [B][H][Npad/128];
+ * fmt 4: Q/K as fmt 1, and V and P in MXFP4: v8 holds the V codes
+ *        [B][H][D][Nk_pad/2] and sv points to the V E8M0 bytes
+ *        [B][H][Nk_pad/128][D][4] (oracle_quantize_v_mxfp4); P per 32 keys of
+ *        a row: E8M0 exponent floor(log2 max p) - 2, E2M1 codes of p / 2^e.
+ * V (fmt 0-2): fp8 [B][H][D][Nk_pad] + sv [B][H][D].
  * rows (nullable): the query indices to evaluate (same set for every b,h);
  * nrows = number of them (rows == NULL: all Nq).
  * Outputs, for the evaluated rows only:

@@ -631,3 +631,90 @@ def test_smoothed_attention_lse_and_accuracy():
     assert np.abs(ls - le).max() < 0.15
     err = lambda o: float(np.abs(o - oe).max())  # noqa: E731
     assert err(os_) < err(op)
+
+
+# ------------------------------------------------------------------ MXFP4 V and P
+def _e2m1_code(y):
+    """Brute-force E2M1 code (sign bit 8) of y: nearest value, ties to the even code."""
+    mag = _nearest_even(y, np.arange(8, dtype=np.uint8), np.array(E2M1), 6.0)
+    return mag | (0x8 if y < 0 or (y == 0 and math.copysign(1, y) < 0) else 0)
+
+
+def _dequant_v_mxfp4(codes, e8):
+    """[B,H,D,Np/2] codes + [B,H,Np/128,D,4] bytes -> float64 V^T [B,H,D,Np]."""
+    lo, hi = codes & 0xF, codes >> 4
+    c = np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
+    mag = np.array(E2M1)[c & 7] * np.where(c & 8, -1.0, 1.0)
+    B, H, nt, D, _ = e8.shape
+    sc = np.exp2(e8.astype(np.float64) - 127).transpose(0, 1, 3, 2, 4).reshape(B, H, D, nt * 4)
+    return mag * np.repeat(sc, 32, axis=-1)
+
+
+@pytest.mark.parametrize("lens", [None, [100]])
+def test_quantize_v_mxfp4(lens):
+    """Every 32-token block of every channel: E8M0 = floor(log2 amax) - 2
+    over the valid tokens (numpy), E2M1 codes by brute-force nearest-even
+    search, token 2i in the low nibble, scales tile-major."""
+    w, q, k, v = _tiny(N=300)
+    x = bf16_bits(v)
+    codes, e8 = oracle.quantize_v_mxfp4(x, lens=lens)
+    assert codes.shape == (1, 2, 128, 192) and e8.shape == (1, 2, 3, 128, 4)
+    vf = _f32(x).astype(np.float64)
+    nv = lens[0] if lens else 300
+    for h in range(2):
+        for d in range(0, 128, 7):
+            for blk in range(12):
+                n0 = blk * 32
+                vals = vf[0, n0:min(n0 + 32, nv), h, d] if n0 < nv else np.zeros(0)
+                amax = np.abs(vals).max() if vals.size else 0.0
+                byte = 0 if amax == 0 else int(np.floor(np.log2(amax))) - 2 + 127
+                assert e8[0, h, blk // 4, d, blk % 4] == byte
+                for i in range(32):
+                    n = n0 + i
+                    c = (codes[0, h, d, n // 2] >> (4 * (n % 2))) & 0xF
+                    want = _e2m1_code(vf[0, n, h, d] / 2.0 ** (byte - 127)) if n < nv else 0
+                    assert c == want, (h, d, n)
+
+
+def test_attention_mxfp4_pv_weights_and_output():
+    """MXFP4 Q/K, V and P (fmt 4): LSE is the logsumexp of the dequantized
+    logits; each weight is the brute-force MXFP4 encoding of p = 2^(t - M)
+    (per 32 keys: exponent floor(log2 max p) - 2, E2M1 nearest-even) over l;
+    O is the weighted sum of the dequantized MXFP4 V."""
+    w, q, k, v = _tiny(N=300)
+    Nq = Nk = 300
+    qq, qs = oracle.quantize_mxfp4(bf16_bits(q))
+    kq, ks = oracle.quantize_mxfp4(bf16_bits(k))
+    vc, ve = oracle.quantize_v_mxfp4(bf16_bits(v))
+    o, lse, wts = oracle.attention(4, qq, qs, kq, ks, vc, ve, Nq=Nq, Nk=Nk, want_weights=True)
+    qd, kd = _dequant_mxfp4(qq, qs), _dequant_mxfp4(kq, ks)
+    z = (1 / math.sqrt(128)) * np.einsum("bhid,bhjd->bhij", qd[:, :, :Nq], kd[:, :, :Nk])
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(z, axis=-1), rtol=0, atol=1e-9)
+    t = z * L2E
+    M = np.ceil(t.max(-1, keepdims=True))
+    p = np.exp2(t - M)
+    l = p.sum(-1)
+    for (b, h, i) in [(0, 0, 0), (0, 1, 77), (0, 0, 299)]:
+        for j0 in range(0, Nk, 32):
+            blk = p[b, h, i, j0:j0 + 32]
+            e = int(np.floor(np.log2(blk.max()))) - 2
+            for jj, pj in enumerate(blk):
+                c = _e2m1_code(pj / 2.0 ** e)
+                want = E2M1[c & 7] * 2.0 ** e / l[b, h, i]
+                assert wts[b, h, i, j0 + jj] == pytest.approx(want, rel=1e-12, abs=1e-300)
+    vd = _dequant_v_mxfp4(vc, ve)
+    np.testing.assert_allclose(o, np.einsum("bhij,bhdj->bhid", wts, vd[..., :Nk]),
+                               rtol=1e-10, atol=1e-12)
+    # the weights still sum to one within the E2M1 half-step (1/4 relative)
+    assert np.all(np.abs(wts.sum(-1) - 1.0) <= 0.25)
+
+
+def test_mxfp4_pv_close_to_exact():
+    w, q, k, v = _tiny()
+    qz = oracle.quantize_mxfp4(bf16_bits(q))
+    kz = oracle.quantize_mxfp4(bf16_bits(k))
+    vz = oracle.quantize_v_mxfp4(bf16_bits(v))
+    o, _, _ = oracle.attention(4, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk)
+    oe, _ = oracle.attention_exact(bf16_bits(q), bf16_bits(k), bf16_bits(v))
+    cos = (o * oe).sum() / math.sqrt((o * o).sum() * (oe * oe).sum())
+    assert cos >= 0.95
