@@ -53,8 +53,8 @@ def _roofline_peak(p16: float, fmt: int) -> float:
     pipe (INT8 codes held as FP16), the FP4 pipe (MXFP4) or the FP8 pipe (FP8
     Q/K), half (P V) on the FP8 pipe; the two halves run back to back, so the
     rates combine harmonically."""
-    p_qk = p16 * {0: 1.0, 1: _FP4_RATIO, 2: _FP8_RATIO, 3: _FP4_RATIO}[fmt]
-    p_pv = p16 * _FP8_RATIO
+    p_qk = p16 * {0: 1.0, 1: _FP4_RATIO, 2: _FP8_RATIO, 3: _FP4_RATIO, 4: _FP4_RATIO}[fmt]
+    p_pv = p16 * (_FP4_RATIO if fmt == 4 else _FP8_RATIO)
     return 2.0 / (1.0 / p_qk + 1.0 / p_pv)
 
 
@@ -103,11 +103,13 @@ def _quant_bytes(w, Nqp: int, Nkp: int) -> float:
     as codes (FP16-held INT8, or packed E2M1 plus one E8M0 byte per 32), V read
     by both passes (channel maxima, then encoding) and written as FP8."""
     B, H, D = w.B, w.H, w.D
-    code = {0: 2.0, 1: 0.5 + 1.0 / 32, 2: 1.0, 3: 0.5 + 1.0 / 32}[w.fmt]
+    code = {0: 2.0, 1: 0.5 + 1.0 / 32, 2: 1.0, 3: 0.5 + 1.0 / 32, 4: 0.5 + 1.0 / 32}[w.fmt]
     qk = (B * w.Nq * H * D * 2 + B * H * Nqp * D * code + B * w.Nk * H * D * 2
           + B * H * Nkp * D * code)
     if w.smooth_k:  # K also read by the channel-maximum and the fixed-point-sum passes
         qk += 2 * B * w.Nk * H * D * 2
+    if w.fmt == 4:  # MXFP4 V: one pass, read once, packed E2M1 + E8M0 per 32 tokens
+        return qk + B * w.Nk * H * D * 2 + B * H * D * Nkp * (0.5 + 1.0 / 32)
     return qk + B * w.Nk * H * D * 2 * 2 + B * H * D * Nkp
 
 
@@ -178,14 +180,15 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64, nthreads: int = 0
         qb, kb, vb = (bf16_bits(t[:, :, :nh]) for t in (q, k, v))
         t0 = time.perf_counter()
         quant_qk = {0: oracle.quantize_int8, 1: oracle.quantize_mxfp4, 2: oracle.quantize_fp8_qk,
-                    3: oracle.quantize_mxfp4_hadamard}[w.fmt]
+                    3: oracle.quantize_mxfp4_hadamard, 4: oracle.quantize_mxfp4}[w.fmt]
         qz = quant_qk(qb)
         km = None
         if w.smooth_k:
             *kz, km = oracle.quantize_int8_smooth(kb, lens=lens)
         else:
             kz = quant_qk(kb, lens=lens)
-        vz = oracle.quantize_v_fp8(vb, lens=lens)
+        vz = (oracle.quantize_v_mxfp4(vb, lens=lens) if w.fmt == 4
+              else oracle.quantize_v_fp8(vb, lens=lens))
         # rotated MXFP4: MXFP4 codes of QH and KH, logits (QH)(KH)^T / 128
         afmt, c = (1, 1.0 / math.sqrt(w.D) / 128) if w.fmt == 3 else (w.fmt, None)
         oracle.attention(afmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows,
@@ -303,8 +306,12 @@ def main():
         qs = torch.empty((B, H, Nqp, D // 32), dtype=torch.uint8, device=dev)
         kq = torch.empty((B, H, Nkp, D // 2), dtype=torch.uint8, device=dev)
         ks = torch.empty((B, H, Nkp, D // 32), dtype=torch.uint8, device=dev)
-    vq = torch.empty((B, H, D, Nkp), dtype=torch.uint8, device=dev)
-    vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    if fmt == binding.FMT_MXFP4_V4:
+        vq = torch.empty((B, H, D, Nkp // 2), dtype=torch.uint8, device=dev)
+        vs = torch.empty((B, H, Nkp // 128, D, 4), dtype=torch.uint8, device=dev)
+    else:
+        vq = torch.empty((B, H, D, Nkp), dtype=torch.uint8, device=dev)
+        vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
     vws = torch.empty(max(16, binding.sage_workspace_bytes(1, fmt, B, H, Nk, Nk)), dtype=torch.uint8,
                       device=dev)
     o = torch.empty((B, Nq, H, D), dtype=torch.bfloat16, device=dev)
@@ -332,7 +339,10 @@ def main():
             binding.sage_quantize_qk(k, fmt, lens=k_lens, out=kq, scale=ks)
 
     def quant_v():
-        binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
+        if fmt == binding.FMT_MXFP4_V4:
+            binding.sage_quantize_v_mxfp4(v, lens=k_lens, out=vq, scale=vs)
+        else:
+            binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
 
     def attn():
         binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens, out=o,
@@ -477,7 +487,7 @@ def main():
     elif fmt in (binding.FMT_INT8, binding.FMT_FP8):
         quant_launches = 2
     else:
-        quant_launches = 4
+        quant_launches = 3 if fmt == binding.FMT_MXFP4_V4 else 4
     launches_per_step = quant_launches + 1 + (1 if nsplit > 1 else 0)
     quant_bytes = _quant_bytes(w, Nqp, Nkp)
     # Secondary bound: one exp2 per logit on the MUFU pipe (no FMA-polynomial
@@ -490,6 +500,7 @@ def main():
     kfmt = 1 if fmt == 3 else fmt   # the rotated MXFP4 format runs the MXFP4 kernel
     kernel = f"sage_attn_kernel<{kfmt},{nqt},{(2 if nqt == 2 else 3) if kfmt == 0 else 4}>"
     fmt_names = {0: ("int8+fp8e4m3", "int8_qk_fp8_v"), 1: ("mxfp4+fp8e4m3", "mxfp4_qk_fp8_v"),
+                 4: ("mxfp4", "mxfp4_qk_mxfp4_pv"),
                  2: ("fp8e4m3", "fp8_qk_fp8_v"),
                  3: ("mxfp4+fp8e4m3", "hadamard_mxfp4_qk_fp8_v")}
     traffic = _profiled_traffic(kernel, w.name) if args.heads == 0 else None
@@ -524,7 +535,8 @@ def main():
                      "traffic": None if traffic is None else traffic,
                      "algorithmic_flops_per_launch": flops,
                      "peak_basis": (f"{peak_kind} bf16 {p16} TFLOP/s x nominal ratios: Q K^T "
-                                    f"{ {0: 'fp16 x1', 1: 'fp4 x6', 2: 'fp8 x2', 3: 'fp4 x6'}[fmt] }, P V fp8 x2, "
+                                    f"{ {0: 'fp16 x1', 1: 'fp4 x6', 2: 'fp8 x2', 3: 'fp4 x6', 4: 'fp4 x6'}[fmt] }, "
+                                    f"P V { 'fp4 x6' if fmt == 4 else 'fp8 x2' }, "
                                     f"harmonic combination"),
                      "kernel": kernel},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

@@ -65,9 +65,12 @@ typedef enum {
   SAGE_FMT_QK_MXFP4_V_FP8 = 1, /* Q/K MXFP4 E2M1 + E8M0 per 32 channels, V FP8 E4M3 */
   SAGE_FMT_QK_FP8_V_FP8 = 2,   /* Q/K FP8 E4M3 per-128-token-block scales, V FP8 E4M3
                                   ("Test Result": the FP8 QK^T / FP8 PV row) */
-  SAGE_FMT_QK_MXFP4H_V_FP8 = 3 /* Q/K rotated by the 128-point Hadamard transform, then
+  SAGE_FMT_QK_MXFP4H_V_FP8 = 3, /* Q/K rotated by the 128-point Hadamard transform, then
                                   MXFP4 as format 1; V FP8 E4M3 (Q/K rotation before
                                   MXFP4 quantization) */
+  SAGE_FMT_QK_MXFP4_V_MXFP4 = 4 /* Q/K MXFP4 as format 1; V MXFP4 along tokens and P
+                                  MXFP4 per 32 keys, P V by a block-scaled FP4 MMA
+                                  ("Test Result": the FP4 P V rows) */
 } sage_format_t;
 
 typedef struct {
@@ -99,9 +102,16 @@ typedef struct {
  * SAGE_FMT_QK_FP8_V_FP8, Q or K:
  *   data  : [B][H][Npad][D] FP8 E4M3 codes (one byte each).
  *   scale : [B][H][Npad/128] float, absmax/448 of each 128-token block.
- * V (every format):
+ * V (formats 0-3):
  *   data  : [B][H][D][Npad] FP8 E4M3 codes, token-contiguous (V transposed).
  *   scale : [B][H][D] float, absmax/448 of each channel over valid tokens.
+ * V (SAGE_FMT_QK_MXFP4_V_MXFP4, from sage_quantize_v_mxfp4):
+ *   data  : [B][H][D][Npad/2] bytes of packed E2M1 codes, token-contiguous,
+ *           token 2i in the low nibble.
+ *   scale : [B][H][Npad/128][D][4] E8M0 bytes: for each 128-token tile and
+ *           channel, the exponents of its four 32-token blocks (OCP MX rule:
+ *           floor(log2 amax) - 2 over the block's valid tokens, clamped to
+ *           [0, 254] biased; 0 for an all-zero block).
  * ------------------------------------------------------------------------- */
 
 /* Bytes needed for a quantized tensor. which: 0 = Q/K data, 1 = Q/K scale,
@@ -133,6 +143,17 @@ size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int
 sage_status_t sage_quantize_qk(sage_format_t fmt, const void* x, sage_strides_t xs, int64_t B,
                                int64_t N, int64_t H, int64_t D, const int32_t* lens, void* x_q,
                                void* x_scale, sage_stream_t stream);
+
+/* Quantize V to MXFP4 along tokens for SAGE_FMT_QK_MXFP4_V_MXFP4 ("new MHA v4
+ * entrypoint ...": sage_quant_v_mxfp4_colmajor; reading: per channel and 32
+ * consecutive tokens the OCP MX rule of the MXFP4 Q/K format, tokens >=
+ * lens[b] left out of the maximum and written as zero codes). Layouts above;
+ * one launch, no workspace.
+ *   v_q     : sage_quantized_bytes(SAGE_FMT_QK_MXFP4_V_MXFP4, 2, ...) bytes, 16-byte aligned.
+ *   v_scale : sage_quantized_bytes(SAGE_FMT_QK_MXFP4_V_MXFP4, 3, ...) bytes. */
+sage_status_t sage_quantize_v_mxfp4(const void* v, sage_strides_t vs, int64_t B, int64_t N,
+                                    int64_t H, int64_t D, const int32_t* lens, void* v_q,
+                                    void* v_scale, sage_stream_t stream);
 
 /* Quantize V to FP8 E4M3 ("new MHA v4 entrypoint": sage_quant_v_amax_partial,
  * sage_quant_v_amax_finalize and sage_quant_v kernels; reading: one FP32
@@ -174,7 +195,9 @@ sage_status_t sage_quantize_v_noalloc(const void* v, sage_strides_t vs, int64_t 
  *   sage_quantize_qk(fmt, q, qs, B, Nq, H, D, NULL, q_q, q_scale, stream);
  *   sage_quantize_qk(fmt, k, ks, B, Nk, H, D, k_lens, k_q, k_scale, stream);
  *   sage_quantize_v(v, vs, B, Nk, H, D, k_lens, v_q, v_scale, workspace, ws_bytes, stream);
- * with the same argument rules, layouts and workspace (sage_workspace_bytes(1, ...)).
+ * (sage_quantize_v_mxfp4 for SAGE_FMT_QK_MXFP4_V_MXFP4, whose workspace is 0
+ * bytes and may be NULL) with the same argument rules, layouts and workspace
+ * (sage_workspace_bytes(1, ...)).
  * For the INT8 and FP8 formats the Q and K quantization and V's channel maxima
  * run as one persistent launch (fewer launches and no idle tail between the
  * three), followed by the V encode; other formats, or inputs whose strides no
@@ -241,8 +264,14 @@ typedef struct {
  *   p_ij  = 2^(t_ij - M_i),  l_i = sum_j p_ij,  P8_ij = E4M3(p_ij * 2^8)
  *   O_id  = sum_j dq(P8_ij) 2^-8 dq(V8_dj) s_v[d] / l_i          -> BF16
  *   LSE_i = (M_i + log2 l_i) ln 2  (natural-log LSE of the logits)  -> FP32
+ *   SAGE_FMT_QK_MXFP4_V_MXFP4 replaces P8 and V8: P is MXFP4 per 32 keys of a
+ *   row (e = floor(log2 max p) - 2 over the block, codes E2M1(p / 2^e)), V is
+ *   the MXFP4 V above, and O_id = sum_j dq(P4_ij) dq(V4_dj) / l_i (the
+ *   block exponents are relative to the row maximum, so the encoding does
+ *   not depend on the order of the key tiles)
  *   q_q, q_scale, k_q, k_scale : quantized Q/K from sage_quantize_qk (fmt).
- *   v_q, v_scale : quantized V from sage_quantize_v.
+ *   v_q, v_scale : quantized V from sage_quantize_v (sage_quantize_v_mxfp4 for
+ *                SAGE_FMT_QK_MXFP4_V_MXFP4).
  *   k_lens     : nullable int32 [B] device array of valid key counts
  *                (0 <= k_lens[b] <= Nk; a 0 gives O = 0 and LSE = -inf);
  *                an entry out of range sets SAGE_ERR_DEVICE_ARG in the

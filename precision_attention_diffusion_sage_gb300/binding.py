@@ -24,6 +24,7 @@ FMT_INT8 = 0   # SAGE_FMT_QK_INT8_V_FP8
 FMT_MXFP4 = 1  # SAGE_FMT_QK_MXFP4_V_FP8
 FMT_FP8 = 2    # SAGE_FMT_QK_FP8_V_FP8
 FMT_MXFP4H = 3  # SAGE_FMT_QK_MXFP4H_V_FP8 (Hadamard-rotated MXFP4)
+FMT_MXFP4_V4 = 4  # SAGE_FMT_QK_MXFP4_V_MXFP4 (MXFP4 Q/K, V and P)
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libsage.so is not built ({LIB_PATH}); run __graft_entry__.build()")
@@ -50,6 +51,8 @@ _lib.sage_quantize_qk.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P,
 _lib.sage_quantize_v.restype = _I32
 _lib.sage_quantize_v.argtypes = [_P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
                                  ctypes.c_size_t, _P]
+_lib.sage_quantize_v_mxfp4.restype = _I32
+_lib.sage_quantize_v_mxfp4.argtypes = [_P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P]
 _lib.sage_quantize_qkv.restype = _I32
 _lib.sage_quantize_qkv.argtypes = [_I32, _P, Strides, _P, Strides, _P, Strides, _I64, _I64, _I64,
                                    _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
@@ -156,7 +159,7 @@ def sage_quantize_qk(x: torch.Tensor, fmt: int = FMT_INT8, lens=None,
             out = torch.empty((B, H, Np, D // 2), dtype=torch.uint8, device=x.device)
     if scale is None:
         scale = (torch.empty((B, H, Np, D // 32), dtype=torch.uint8, device=x.device)
-                 if fmt in (FMT_MXFP4, FMT_MXFP4H)
+                 if fmt in (FMT_MXFP4, FMT_MXFP4H, FMT_MXFP4_V4)
                  else torch.empty((B, H, Np // 128), dtype=torch.float32, device=x.device))
     ln = _lens_tensor(lens, x.device)
     _check(_lib.sage_quantize_qk(fmt, _ptr(x), _bnhd_strides(x), B, N, H, D, _ptr(ln), _ptr(out),
@@ -196,6 +199,22 @@ def _qk_outputs(fmt: int, B: int, N: int, H: int, D: int, dev):
             torch.empty((B, H, Np, D // 32), dtype=torch.uint8, device=dev))
 
 
+def sage_quantize_v_mxfp4(v: torch.Tensor, lens=None, out: Optional[torch.Tensor] = None,
+                          scale: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Quantize BF16 V ``[B, N, H, D]`` to MXFP4 along tokens: packed E2M1
+    ``[B, H, D, Npad/2]`` (uint8) + E8M0 bytes ``[B, H, Npad/128, D, 4]``."""
+    B, N, H, D = v.shape
+    Np = pad128(N)
+    if out is None:
+        out = torch.empty((B, H, D, Np // 2), dtype=torch.uint8, device=v.device)
+    if scale is None:
+        scale = torch.empty((B, H, Np // 128, D, 4), dtype=torch.uint8, device=v.device)
+    ln = _lens_tensor(lens, v.device)
+    _check(_lib.sage_quantize_v_mxfp4(_ptr(v), _bnhd_strides(v), B, N, H, D, _ptr(ln), _ptr(out),
+                                      _ptr(scale), _stream()), "sage_quantize_v_mxfp4")
+    return out, scale
+
+
 def sage_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: int = FMT_INT8,
                       k_lens=None, outs=None, workspace: Optional[torch.Tensor] = None):
     """Quantize Q, K, V in one library call (bit-identical to the three separate
@@ -206,8 +225,12 @@ def sage_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: in
     dev = q.device
     if outs is None:
         (qq, qs), (kq, ks) = _qk_outputs(fmt, B, Nq, H, D, dev), _qk_outputs(fmt, B, Nk, H, D, dev)
-        vq = torch.empty((B, H, D, pad128(Nk)), dtype=torch.uint8, device=dev)
-        vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+        if fmt == FMT_MXFP4_V4:
+            vq = torch.empty((B, H, D, pad128(Nk) // 2), dtype=torch.uint8, device=dev)
+            vs = torch.empty((B, H, pad128(Nk) // 128, D, 4), dtype=torch.uint8, device=dev)
+        else:
+            vq = torch.empty((B, H, D, pad128(Nk)), dtype=torch.uint8, device=dev)
+            vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
     else:
         (qq, qs), (kq, ks), (vq, vs) = outs
     need = sage_workspace_bytes(1, fmt, B, H, Nk, Nk, D)

@@ -87,17 +87,31 @@ struct QKFormat<2> {
   static constexpr int kStep = 128;
 };
 
+// MXFP4 Q/K as format 1, with V and P in MXFP4 too (P V by kind::mxf4).
+template <>
+struct QKFormat<4> : QKFormat<1> {};
+
+// MXFP4 Q/K (formats 1 and 4) share the S path: 64-key steps, E8M0 scales.
+template <int FMT>
+__host__ __device__ constexpr bool is_mx() { return FMT == 1 || FMT == 4; }
+
 template <int FMT, int NQT, int STAGES>
 struct SmemLayout {
   using F = QKFormat<FMT>;
   static constexpr int kPSlots = 2 * (128 / F::kStep);  // P slots per query tile
   static constexpr int kQ = 0;                             // NQT Q tiles
   static constexpr int kK = kQ + NQT * F::kTileBytes;      // STAGES K tiles
-  static constexpr int kV = kK + STAGES * F::kTileBytes;   // STAGES x 16 KB (FP8 V^T 128x128)
-  static constexpr int kP = kV + STAGES * 16384;           // NQT x 2 x 16 KB (FP8 P, double buffer)
+  static constexpr int kVTile = FMT == 4 ? 8192 : 16384;  // V^T 128x128: E2M1 or E4M3
+  static constexpr int kV = kK + STAGES * F::kTileBytes;   // STAGES V tiles
+  static constexpr int kP = kV + STAGES * kVTile;          // NQT x 2 x 16 KB (P, double buffer;
+                                                           // also the O staging of the epilogue)
   static constexpr int kSf = kP + NQT * 2 * 16384;         // (NQT + STAGES) scale blocks
   static constexpr int kSv = kSf + (NQT + STAGES) * F::kSfBytes;  // 128 V channel scales
-  static constexpr int kBar = kSv + 512;
+  // MXFP4 V / P (format 4): E8M0 blocks of the V stages and of the P slots,
+  // in the line order of the TMEM copy.
+  static constexpr int kVsf = kSv + 512;
+  static constexpr int kPsf = kVsf + (FMT == 4 ? STAGES * 512 : 0);
+  static constexpr int kBar = kPsf + (FMT == 4 ? NQT * kPSlots * 512 : 0);
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
   //           s_full[T], s_free[T], p_full[T][kPSlots], o_done[T][kPSlots], mma_final
   static constexpr int kNumBars = 1 + 4 * STAGES + NQT * (2 + 2 * kPSlots) + 1;
@@ -112,16 +126,26 @@ struct SmemLayout {
 template <int FMT, int NQT>
 struct TmemLayout {
   static constexpr uint32_t kCols = NQT == 1 ? 256 : 512;
-  __host__ __device__ static constexpr uint32_t s(int t) { return FMT != 1 ? t * 256 : NQT * 128 + t * 64; }
-  __host__ __device__ static constexpr uint32_t o(int t) { return FMT != 1 ? t * 256 + 128 : t * 128; }
+  __host__ __device__ static constexpr uint32_t s(int t) { return !is_mx<FMT>() ? t * 256 : NQT * 128 + t * 64; }
+  __host__ __device__ static constexpr uint32_t o(int t) { return !is_mx<FMT>() ? t * 256 + 128 : t * 128; }
   __host__ __device__ static constexpr uint32_t sfq(int t) { return NQT * 192 + t * 4; }
   // K scales: two slots per query tile (each tile's MMA warp copies its own).
   __host__ __device__ static constexpr uint32_t sfk(int t, int slot) {
     return NQT * 196 + (t * 2 + slot) * 4;
   }
+  // Format 4: V scales in two slots per query tile (alternating V tiles) and
+  // P scales in one block per P slot.
+  __host__ __device__ static constexpr uint32_t sfv(int t, int slot) {
+    return NQT * 196 + (NQT * 2 + t * 2 + slot) * 4;
+  }
+  __host__ __device__ static constexpr uint32_t sfp(int t, int slot) {
+    return NQT * 196 + (NQT * 4 + t * 4 + slot) * 4;
+  }
 };
 static_assert(TmemLayout<1, 2>::sfk(1, 1) + 4 <= TmemLayout<1, 2>::kCols, "TMEM budget");
 static_assert(TmemLayout<1, 1>::sfk(0, 1) + 4 <= TmemLayout<1, 1>::kCols, "TMEM budget");
+static_assert(TmemLayout<4, 2>::sfp(1, 3) + 4 <= TmemLayout<4, 2>::kCols, "TMEM budget");
+static_assert(TmemLayout<4, 1>::sfp(0, 3) + 4 <= TmemLayout<4, 1>::kCols, "TMEM budget");
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -163,6 +187,32 @@ __device__ __forceinline__ float row_max(const float (&s)[N]) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], s[kTail + k]);
   return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// Maximum of s[B] .. s[B + 31].
+template <int B, int N>
+__device__ __forceinline__ float max32(const float (&s)[N]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = max3f(s[B + k], s[B + 8 + k], s[B + 16 + k]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], s[B + 24 + k]);
+  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// Eight E2M1 codes packed in a word, element i in bits 4i+3 .. 4i (round to
+// nearest even, saturating at 6).
+__device__ __forceinline__ uint32_t e2m1x8(const float (&x)[8]) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}\n"
+      : "=r"(r)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
+  return r;
 }
 
 // 2^k for an integer-valued k <= 0 (0 below the normal range).
@@ -237,7 +287,7 @@ __device__ __forceinline__ float q_dot_kmean(uint32_t tile, int r, const float* 
 template <int NQT>
 constexpr int attn_threads() { return NQT == 1 ? 7 * 32 : 12 * 32; }
 template <int FMT, int NQT>
-__host__ __device__ constexpr bool attn_split_regs() { return FMT != 1 && NQT == 2; }
+__host__ __device__ constexpr bool attn_split_regs() { return !is_mx<FMT>() && NQT == 2; }
 
 template <int FMT, int NQT, int STAGES>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
@@ -267,6 +317,9 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   uint8_t* sP = smem + L::kP;
   uint8_t* sSf = smem + L::kSf;  // MXFP4 scales: NQT query tiles, then STAGES K tiles
   float* sSv = reinterpret_cast<float*>(smem + L::kSv);
+  uint8_t* sVsf = smem + L::kVsf;  // format 4: V scale blocks per stage
+  uint8_t* sPsf = smem + L::kPsf;  // format 4: P scale blocks per query tile and slot
+  constexpr bool kMx = is_mx<FMT>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
@@ -338,7 +391,9 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   }
 
   // ---- setup
-  if (threadIdx.x < 128) sSv[threadIdx.x] = __ldg(&p.v_scale[bh * 128 + threadIdx.x]);
+  // V channel scales (MXFP4 V carries its scales inside the MMA: 1).
+  if (threadIdx.x < 128)
+    sSv[threadIdx.x] = FMT == 4 ? 1.0f : __ldg(&p.v_scale[bh * 128 + threadIdx.x]);
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
@@ -380,7 +435,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   // descriptors live in uniform registers) and one elected lane issues.
   if (warp == kTmaWarp) {
     // ================================================================ TMA producer (Q, K)
-    if constexpr (FMT == 1) {
+    if constexpr (kMx) {
       // E8M0 scales of the query tiles, written in the order the TMEM copy
       // reads: lane L stores the 16-byte line of rows L, L+32, L+64, L+96.
       for (int t = 0; t < NQT; ++t) {
@@ -414,7 +469,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     // MXFP4: the next K tile's scale words, loaded one fill ahead.
     uint32_t kw[4] = {0u, 0u, 0u, 0u};
     const uint32_t* ksf = nullptr;
-    if constexpr (FMT == 1) {
+    if constexpr (kMx) {
       ksf = p.k_sf + bh * Nk_pad + lane;
 #pragma unroll
       for (int c = 0; c < 4; ++c) kw[c] = __ldg(ksf + j0 * 128 + 32 * c);
@@ -425,7 +480,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     uint32_t rph = 0;
     for (int it = 0; it < niter; ++it) {
       if (it >= STAGES && !warp_wait(&k_empty[s], rph ^ 1u, abort, p.status)) break;
-      if constexpr (FMT == 1) {
+      if constexpr (kMx) {
         st_shared_v4(smem_u32(sSf + (NQT + s) * 512) + lane * 16, kw[0], kw[1], kw[2], kw[3]);
         fence_proxy_async_smem();
         __syncwarp();
@@ -441,7 +496,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         }
       }
       __syncwarp();
-      if constexpr (FMT == 1) {
+      if constexpr (kMx) {
         if (it + 1 < niter) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) kw[c] = __ldg(ksf + (j0 + it + 1) * 128 + 32 * c);
@@ -467,9 +522,21 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     uint32_t rph = 0;
     for (int it = 0; it < niter; ++it) {
       if (it >= STAGES && !warp_wait(&v_empty[s], rph ^ 1u, abort, p.status)) break;
+      if constexpr (FMT == 4) {
+        // The tile's E8M0 scales (128 channel rows x 4 bytes, contiguous),
+        // written in the line order of the TMEM copy (line L: rows L, L+32,
+        // L+64, L+96), visible to the async proxy before the tile's barrier.
+        const uint32_t* vsf = p.v_sf + (bh * p.nbk + j0 + it) * 128 + lane;
+        st_shared_v4(smem_u32(sVsf + s * 512) + lane * 16, __ldg(vsf), __ldg(vsf + 32),
+                     __ldg(vsf + 64), __ldg(vsf + 96));
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (elect_one()) {
-        mbar_arrive_expect_tx(&v_full[s], 16384);
-        tma_load_2d(sV + s * 16384, &tmV, &v_full[s], (j0 + it) * 128, static_cast<int>(bh * 128));
+        mbar_arrive_expect_tx(&v_full[s], L::kVTile);
+        // E4M3 V^T rows of Nk_pad bytes, or E2M1 rows of Nk_pad / 2 bytes.
+        tma_load_2d(sV + s * L::kVTile, &tmV, &v_full[s], (j0 + it) * (FMT == 4 ? 64 : 128),
+                    static_cast<int>(bh * 128));
       }
       __syncwarp();
       filled = it + 1;
@@ -544,17 +611,38 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         tmem_cp_sf512(tbase + TM::sfk(t, sf_slot), smem_u32(sSf + (NQT + stage) * 512));
       __syncwarp();
     };
-    auto issue_pv = [&](int slot, int stage, int half, bool acc) {
+    // P V of one step: P slot `slot`, V stage `stage`, 64-key half `half`;
+    // format 4 also V-scale TMEM slot `vslot` (local V tile index & 1).
+    auto issue_pv = [&](int slot, int stage, int half, int vslot, bool acc) {
       const int pbuf = slot / kSteps;
-      const uint32_t pa = p_lo + pbuf * 1024, va = v_lo + stage * 1024;
-      constexpr int kK = kStep / 32;  // K = 32 slices per step
-      if (elect_one()) {
-#pragma unroll
-        for (int k = 0; k < kK; ++k) {
-          const int kk = half * kK + k;
-          mma_f8_ss_lo(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+      if constexpr (FMT == 4) {
+        // E2M1 P (64-byte rows, keys 64h .. 64h+63 at +32 bytes) times E2M1
+        // V^T rows, one K = 64 block-scaled MMA with N = 128 channels; the
+        // scale bytes of this half are bytes 2h, 2h+1 of each row's word.
+        // The copies precede the MMA in this thread's issue order. A V slot
+        // is rewritten two V tiles later and a P slot kPSlots steps later,
+        // after the S of this tile's current step completed, which completes
+        // only after every earlier MMA of this warp (the reads of the slot).
+        const uint32_t pa = p_lo + pbuf * 1024 + half * 2;
+        const uint32_t va = v_lo + stage * (L::kVTile >> 4) + half * 2;
+        const uint32_t sfa = tbase + TM::sfp(t, slot), sfb = tbase + TM::sfv(t, vslot);
+        if (elect_one()) {
+          if (half == 0) tmem_cp_sf512(sfb, smem_u32(sVsf + stage * 512));
+          tmem_cp_sf512(sfa, smem_u32(sPsf + (t * kPSlots + slot) * 512));
+          mma_mxf4_ss_lo(d_o, pa, va, idesc_mxf4(128, 128, 2u * half), sfa, sfb, acc ? 1u : 0u);
+          mma_commit(&o_done[t * kPSlots + slot]);
         }
-        mma_commit(&o_done[t * kPSlots + slot]);
+      } else {
+        const uint32_t pa = p_lo + pbuf * 1024, va = v_lo + stage * 1024;
+        constexpr int kK = kStep / 32;  // K = 32 slices per step
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < kK; ++k) {
+            const int kk = half * kK + k;
+            mma_f8_ss_lo(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&o_done[t * kPSlots + slot]);
+        }
       }
       __syncwarp();
     };
@@ -570,7 +658,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     if (ok) ok = warp_wait(&k_full[0], 0, abort, p.status);
     tc_fence_after();
     if (ok) {
-      if constexpr (FMT == 1) {
+      if constexpr (kMx) {
         if (elect_one()) tmem_cp_sf512(tbase + TM::sfq(t), smem_u32(sSf + t * 512));
         __syncwarp();
         copy_k_scales(0, 0);
@@ -595,7 +683,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(u) & 1u, abort, p.status))) break;
         tc_fence_after();
         const int sf_slot = (v / kSteps) & 1;
-        if constexpr (FMT == 1) {
+        if constexpr (kMx) {
           if (hv == 0) copy_k_scales(ks, sf_slot);
         }
         issue_s(ks, hv, sf_slot);
@@ -614,7 +702,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
                            static_cast<uint32_t>(u >> kPSlotShift) & 1u, abort, p.status)))
         break;
       tc_fence_after();
-      issue_pv(slot, vs, hu, u > 0);
+      issue_pv(slot, vs, hu, (u / kSteps) & 1, u > 0);
       if (hu == kSteps - 1) {
         commit(&v_empty[vs]);
         if (++vs == STAGES) { vs = 0; vph ^= 1u; }
@@ -639,7 +727,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     float alpha_q = p.scale_log2;
     const float* kscale = nullptr;
     float sk_next = 1.0f;  // K block scale, loaded one tile ahead
-    if constexpr (FMT != 1) {
+    if constexpr (!kMx) {
       const float sq = qt < p.nbq ? __ldg(&p.q_scale[bh * p.nbq + qt]) : 0.0f;
       alpha_q = sq * p.scale_log2;
       kscale = p.k_scale + bh * p.nbk;
@@ -650,6 +738,11 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     bool ok = true;
     const uint32_t p_row0 = smem_u32(sP + (t * 2) * 16384) + r * 128;  // P buffer 0; buffer 1 at +16 KB
     const uint32_t swz = static_cast<uint32_t>(r & 7);
+    // Format 4: 64-byte P rows (64-byte swizzle: chunk c at c ^ ((r / 2) & 3))
+    // and this row's word in the P scale blocks (line r % 32, word r / 32).
+    const uint32_t p_row0_4 = smem_u32(sP + (t * 2) * 16384) + r * 64;
+    const uint32_t swz64 = static_cast<uint32_t>((r >> 1) & 3);
+    const uint32_t psf_row = smem_u32(sPsf + t * kPSlots * 512) + (r & 31) * 16 + (r >> 5) * 4;
 
     constexpr int kPSlotShift = kPSlots == 4 ? 2 : 1;  // log2(kPSlots)
     float sk = 1.0f;
@@ -657,7 +750,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       const int iu = u / kSteps;
       const int hu = u & (kSteps - 1);
       const int j = j0 + iu;
-      if constexpr (FMT != 1) {
+      if constexpr (!kMx) {
         sk = sk_next;
         if (iu + 1 < niter) sk_next = __ldg(&kscale[j + 1]);
       }
@@ -688,7 +781,15 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         for (int c = 0; c < kStep; ++c)
           if (c >= nvalid) s[c] = -INFINITY;
       }
-      const float mx = row_max<kStep>(s);
+      // Format 4 also keeps the maxima of the two 32-key blocks (P's scales).
+      float bm0 = 0.0f, bm1 = 0.0f, mx;
+      if constexpr (FMT == 4) {
+        bm0 = max32<0>(s);
+        bm1 = max32<32>(s);
+        mx = fmaxf(bm0, bm1);
+      } else {
+        mx = row_max<kStep>(s);
+      }
       const float cand = ceilf(mx * alpha);
       // First step: set the reference. Later: raise it only past the headroom.
       const float m_new = (u == 0) ? cand : (cand > m + kHeadroom ? cand : m);
@@ -713,37 +814,78 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         l *= f;
       }
       m = m_new;
-      const float bias = 8.0f - kHeadroom - m;
       const int slot = u & (kPSlots - 1);
-      const uint32_t p_row = p_row0 + static_cast<uint32_t>(slot / kSteps) * 16384;
-      // The P slot was last read by P V of step u - kPSlots. No wait is
-      // needed for it: the MMA warp issued that P V before the S of step u
-      // (its loop issues S of step w + 1 after P V of step w - 1, and
-      // u - kPSlots <= u - 2), and the s_full commit this warp waited for
-      // completes only after every earlier MMA of that warp.
-      // x = S * alpha + (8 - m) two at a time (packed FP32x2 FMA), p8 = 2^x,
-      // four partial row sums (packed FP32x2 adds).
-      const float2 alpha2 = make_float2(alpha, alpha), bias2 = make_float2(bias, bias);
-      float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+      if constexpr (FMT == 4) {
+        // MXFP4 P per 32 keys: x = S alpha - m, exponent e = floor(max x) - 2
+        // (clamped to the E8M0 range; an empty block gives -127), codes
+        // E2M1(2^(x - e)) into this row of the 64-byte swizzled P slot and the
+        // bytes e + 127 into byte 2h, 2h + 1 of the row's scale word. The codes
+        // depend on x - floor(max x) only, not on m; l sums the unquantized
+        // 2^x. The slot is free as argued for the FP8 P below.
+        float e[2] = {floorf(fmaf(bm0, alpha, -m)) - 2.0f, floorf(fmaf(bm1, alpha, -m)) - 2.0f};
+        if (!(e[0] >= -127.0f)) e[0] = -127.0f;
+        if (!(e[1] >= -127.0f)) e[1] = -127.0f;
+        const uint32_t p_row = p_row0_4 + static_cast<uint32_t>(slot / kSteps) * 16384;
+        const float2 alpha2 = make_float2(alpha, alpha);
+        float lsum = 0.0f;
 #pragma unroll
-      for (int ch = 0; ch < kStep / 16; ++ch) {
-        uint32_t pk[4];
+        for (int blk = 0; blk < 2; ++blk) {
+          const float2 bias2 = make_float2(-m - e[blk], -m - e[blk]);
+          float2 acc = make_float2(0.0f, 0.0f);
+          uint32_t pk[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = ch * 16 + q * 4;
-          const float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), alpha2, bias2);
-          const float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), alpha2, bias2);
-          const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-          const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-          acc0 = __fadd2_rn(acc0, e01);
-          acc1 = __fadd2_rn(acc1, e23);
-          pk[q] = e4m3x4(e01.x, e01.y, e23.x, e23.y);
+          for (int q = 0; q < 4; ++q) {
+            float ev[8];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              const int c = blk * 32 + q * 8 + i;
+              const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), alpha2, bias2);
+              ev[i] = ex2_approx(x.x);
+              ev[i + 1] = ex2_approx(x.y);
+              acc = __fadd2_rn(acc, make_float2(ev[i], ev[i + 1]));
+            }
+            pk[q] = e2m1x8(ev);
+          }
+          lsum += (acc.x + acc.y) * exp2_neg_int(e[blk]);
+          const uint32_t chunk = static_cast<uint32_t>(hu * 2 + blk);  // 16-byte chunk of the row
+          st_shared_v4(p_row + ((chunk ^ swz64) << 4), pk[0], pk[1], pk[2], pk[3]);
         }
-        // 16-byte chunk of this step's keys within the 128-key P row.
-        const uint32_t chunk = static_cast<uint32_t>(hu * (kStep / 16) + ch);
-        st_shared_v4(p_row + ((chunk ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+        l += lsum;
+        const uint32_t sfw = (static_cast<uint32_t>(e[0] + 127.0f) |
+                              (static_cast<uint32_t>(e[1] + 127.0f) << 8)) << (16 * hu);
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(psf_row + slot * 512), "r"(sfw) : "memory");
+      } else {
+        const float bias = 8.0f - kHeadroom - m;
+        const uint32_t p_row = p_row0 + static_cast<uint32_t>(slot / kSteps) * 16384;
+        // The P slot was last read by P V of step u - kPSlots. No wait is
+        // needed for it: the MMA warp issued that P V before the S of step u
+        // (its loop issues S of step w + 1 after P V of step w - 1, and
+        // u - kPSlots <= u - 2), and the s_full commit this warp waited for
+        // completes only after every earlier MMA of that warp.
+        // x = S * alpha + (8 - m) two at a time (packed FP32x2 FMA), p8 = 2^x,
+        // four partial row sums (packed FP32x2 adds).
+        const float2 alpha2 = make_float2(alpha, alpha), bias2 = make_float2(bias, bias);
+        float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int ch = 0; ch < kStep / 16; ++ch) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = ch * 16 + q * 4;
+            const float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), alpha2, bias2);
+            const float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), alpha2, bias2);
+            const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+            const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+            acc0 = __fadd2_rn(acc0, e01);
+            acc1 = __fadd2_rn(acc1, e23);
+            pk[q] = e4m3x4(e01.x, e01.y, e23.x, e23.y);
+          }
+          // 16-byte chunk of this step's keys within the 128-key P row.
+          const uint32_t chunk = static_cast<uint32_t>(hu * (kStep / 16) + ch);
+          st_shared_v4(p_row + ((chunk ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+        }
+        l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
-      l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       fence_proxy_async_smem();
       mbar_arrive(&p_full[t * kPSlots + slot]);
     }
@@ -763,7 +905,10 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         if (p.k_mean && (ok = warp_wait(q_full, 0, abort, p.status)))
           lse_add = alpha_q * q_dot_kmean(smem_u32(sQ + t * 32768), r, p.k_mean + bh * 128);
       }
-      const float lse = (m + log2f(l) - 8.0f + kHeadroom + lse_add) * kLn2;
+      // l is in units of P: 2^(8 - kHeadroom) times 2^(t - m) for the FP8 P,
+      // 2^(t - m) for the MXFP4 P.
+      constexpr float kLUnits = FMT == 4 ? 0.0f : 8.0f - kHeadroom;
+      const float lse = (m + log2f(l) - kLUnits + lse_add) * kLn2;
       const bool store = row < p.Nq;
       if (p.num_splits > 1) {
         float* op = p.o_part + ((static_cast<int64_t>(split) * p.B * p.H + bh) * p.Nq + row) * 128;
@@ -970,9 +1115,16 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
                           CU_TENSOR_MAP_SWIZZLE_64B) &&
               make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, k_rows, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_64B);
+  // V^T: E4M3 rows of Nk_pad bytes (128-byte boxes), or for format 4 packed
+  // E2M1 rows of Nk_pad / 2 bytes (64-byte boxes, the layout of a K tile).
+  const uint64_t v_rows = static_cast<uint64_t>(a.p.B * a.p.H * 128);
   if (!maps_ok ||
-      !make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(Nk_pad),
-                   static_cast<uint64_t>(a.p.B * a.p.H * 128), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      !(a.fmt == 4 ? make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                                 static_cast<uint64_t>(Nk_pad / 2), v_rows, 64, 128,
+                                 CU_TENSOR_MAP_SWIZZLE_64B)
+                   : make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                                 static_cast<uint64_t>(Nk_pad), v_rows, 128, 128,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)))
     return cudaErrorInvalidValue;
   // O through a 4-D map over the caller's [B][Nq][H][D] strides (boxes of
   // 128 rows x 64 channels); the kernel falls back to direct stores when the
@@ -1000,6 +1152,9 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   else if (a.fmt == 2)
     e = two ? launch_variant<2, 2, 4>(mq, mk, mv, mo, p, stream)
             : launch_variant<2, 1, 4>(mq, mk, mv, mo, p, stream);
+  else if (a.fmt == 4)
+    e = two ? launch_variant<4, 2, 4>(mq, mk, mv, mo, p, stream)
+            : launch_variant<4, 1, 4>(mq, mk, mv, mo, p, stream);
   else
     e = two ? launch_variant<1, 2, 4>(mq, mk, mv, mo, p, stream)
             : launch_variant<1, 1, 4>(mq, mk, mv, mo, p, stream);

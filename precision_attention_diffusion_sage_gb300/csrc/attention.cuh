@@ -12,7 +12,8 @@ struct AttnParams {
   const float* k_scale;  // INT8: [B][H][nbk]
   const uint32_t* q_sf;  // MXFP4: E8M0 bytes [B][H][Nq_pad][4], one word per row
   const uint32_t* k_sf;  // MXFP4: [B][H][Nk_pad][4]
-  const float* v_scale;  // [B][H][128]
+  const float* v_scale;  // [B][H][128] (E4M3 V)
+  const uint32_t* v_sf;  // MXFP4 V: E8M0 bytes [B][H][nbk][128][4], one word per channel row
   const int32_t* k_lens; // nullable [B]
   int64_t B, H, Nq, Nk;
   int64_t nbq, nbk;      // 128-token tiles of the padded Q / K
@@ -29,7 +30,7 @@ struct AttnParams {
 };
 
 struct AttnLaunch {
-  int fmt;        // 0: INT8 Q/K, 1: MXFP4 Q/K, 2: FP8 E4M3 Q/K
+  int fmt;        // 0: INT8 Q/K, 1: MXFP4 Q/K, 2: FP8 E4M3 Q/K, 4: MXFP4 Q/K, V and P
   const void* q;  // INT8: FP16-held codes [B][H][Nq_pad][128]; MXFP4: packed E2M1 [B][H][Nq_pad][64]
   const void* k;  // same layout with Nk_pad
   const void* v;  // FP8 [B][H][128][Nk_pad]

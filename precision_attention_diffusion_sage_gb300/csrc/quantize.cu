@@ -351,6 +351,52 @@ __global__ void __launch_bounds__(256) quantize_qk_mxfp4_kernel(QuantQKArgs a) {
   }
 }
 
+// V to MXFP4 along tokens, one CTA per (h, 128-token block, b): thread t owns
+// channels d = 2 (t % 64), d + 1 and the 32 tokens of block t / 64 (4-byte
+// loads; a warp reads 128 contiguous bytes of a token row). Per channel: the
+// OCP MX exponent of the valid tokens' maximum, E2M1 codes of the 32 tokens
+// (one 16-byte store into the channel's token-contiguous row), the scale
+// byte at [b][h][block / 4][d][block % 4].
+__global__ void __launch_bounds__(256) v_quantize_mxfp4_kernel(QuantVArgs a) {
+  const int64_t h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
+  const int64_t Np = pad128(a.N), nb = Np / 128;
+  const int64_t nv = valid_tokens(a.lens, b, a.N, a.status);
+  const int64_t bh = b * a.H + h;
+  const int d0 = 2 * (threadIdx.x & 63);
+  const int tb = static_cast<int>(threadIdx.x >> 6);
+  const int64_t n0 = blk * 128 + tb * 32;
+  float x[2][32];
+  float mx[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int64_t n = n0 + i;
+    uint32_t w = 0;
+    if (n < nv) w = __ldg(reinterpret_cast<const uint32_t*>(a.v + b * a.sb + n * a.sn + h * a.sh + d0));
+    x[0][i] = bf16_lo(w);
+    x[1][i] = bf16_hi(w);
+    mx[0] = fmaxf(mx[0], fabsf(x[0][i]));
+    mx[1] = fmaxf(mx[1], fabsf(x[1][i]));
+  }
+  uint8_t* e8 = reinterpret_cast<uint8_t*>(a.scale);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int d = d0 + c;
+    int byte = 0;
+    if (mx[c] > 0.0f) byte = max(0, min(254, floor_log2(mx[c]) - 2 + 127));
+    const float inv = exp2_int(127 - byte);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = x[c][q * 8 + i];
+      w[q] = e2m1x8(f, inv);
+    }
+    *reinterpret_cast<uint4*>(a.out + (bh * 128 + d) * (Np / 2) + n0 / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+    e8[((bh * nb + blk) * 128 + d) * 4 + tb] = static_cast<uint8_t>(byte);
+  }
+}
+
 // V pass 1: channel maxima of one 128-token block, folded into the per-(b,h)
 // channel maxima with an integer atomic maximum (non-negative binary32
 // values order like their bit patterns).
@@ -1236,6 +1282,13 @@ cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s, bool 
     quantize_qk_mxfp4_kernel<true><<<grid, 256, 0, s>>>(a);
   else
     quantize_qk_mxfp4_kernel<false><<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_v_mxfp4(const QuantVArgs& a, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(a.H), static_cast<unsigned>(pad128(a.N) / 128),
+            static_cast<unsigned>(a.B));
+  v_quantize_mxfp4_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

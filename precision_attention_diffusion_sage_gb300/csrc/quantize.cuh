@@ -32,6 +32,9 @@ struct QuantVArgs {
 // Workspace of the V quantization: one int per (b, h, channel).
 inline int64_t v_workspace_bytes(int64_t B, int64_t H) { return B * H * 128 * 4; }
 cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s);
+// MXFP4 V along tokens: codes [B][H][D][Npad/2] into out, E8M0 bytes
+// [B][H][Npad/128][D][4] into scale (as bytes); no workspace.
+cudaError_t launch_quantize_v_mxfp4(const QuantVArgs& a, cudaStream_t s);
 // Q and K (INT8, or FP8 when fp8) and V in one call: the Q/K quantize and the
 // V channel maxima share one persistent launch; then the V encode.
 cudaError_t launch_quantize_qkv(bool fp8, const QuantQKArgs& q, const QuantQKArgs& k,

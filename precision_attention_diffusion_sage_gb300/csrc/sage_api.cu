@@ -61,7 +61,14 @@ sage_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAG
 
 bool known_format(sage_format_t fmt) {
   return fmt == SAGE_FMT_QK_INT8_V_FP8 || fmt == SAGE_FMT_QK_MXFP4_V_FP8 ||
-         fmt == SAGE_FMT_QK_FP8_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
+         fmt == SAGE_FMT_QK_FP8_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8 ||
+         fmt == SAGE_FMT_QK_MXFP4_V_MXFP4;
+}
+
+// Formats whose Q/K are MXFP4 (E2M1 codes with E8M0 scales per 32 channels).
+bool mx_qk(sage_format_t fmt) {
+  return fmt == SAGE_FMT_QK_MXFP4_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8 ||
+         fmt == SAGE_FMT_QK_MXFP4_V_MXFP4;
 }
 
 int64_t resolve_splits(int num_splits, int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
@@ -81,17 +88,18 @@ size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, 
   if (check_shape(B, N, H, D) != SAGE_OK) return 0;
   if (!known_format(fmt)) return 0;
   const int64_t Np = pad128(N);
-  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
+  const bool mx = mx_qk(fmt);
+  const bool v4 = fmt == SAGE_FMT_QK_MXFP4_V_MXFP4;
   switch (which) {
     case 0:  // FP16-held INT8 codes: 2 B, E4M3: 1 B, packed E2M1: 1/2 B per element
       return static_cast<size_t>(mx ? B * H * Np * D / 2
                                     : B * H * Np * D * (fmt == SAGE_FMT_QK_INT8_V_FP8 ? 2 : 1));
     case 1:
       return static_cast<size_t>(mx ? B * H * Np * (D / 32) : B * H * (Np / 128) * 4);
-    case 2:
-      return static_cast<size_t>(B * H * D * Np);
-    case 3:
-      return static_cast<size_t>(B * H * D * 4);
+    case 2:  // V: E4M3 [B][H][D][Npad], or E2M1 [B][H][D][Npad/2]
+      return static_cast<size_t>(v4 ? B * H * D * Np / 2 : B * H * D * Np);
+    case 3:  // V scales: float [B][H][D], or E8M0 [B][H][Npad/128][D][4]
+      return static_cast<size_t>(v4 ? B * H * Np * D / 32 : B * H * D * 4);
     default:
       return 0;
   }
@@ -103,8 +111,8 @@ size_t sage_workspace_bytes(int op, sage_format_t fmt, int64_t B, int64_t H, int
   switch (op) {
     case 0:
       return 0;
-    case 1:
-      if (check_shape(B, Nk, H, D) != SAGE_OK) return 0;
+    case 1:  // (MXFP4 V needs none)
+      if (check_shape(B, Nk, H, D) != SAGE_OK || fmt == SAGE_FMT_QK_MXFP4_V_MXFP4) return 0;
       return static_cast<size_t>(v_workspace_bytes(B, H));
     case 3:
       if (fmt != SAGE_FMT_QK_INT8_V_FP8 || check_shape(B, Nk, H, D) != SAGE_OK) return 0;
@@ -176,7 +184,8 @@ sage_status_t sage_quantize_qkv(sage_format_t fmt, const void* q, sage_strides_t
       (k_lens && !aligned(k_lens, 4)))
     return SAGE_ERR_INVALID_ARG;
   const size_t need = sage_workspace_bytes(1, fmt, B, H, Nk, Nk, D, 0);
-  if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return SAGE_ERR_WORKSPACE;
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16)))
+    return SAGE_ERR_WORKSPACE;
   int* status = nullptr;
   if ((st = device_state(&status)) != SAGE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -191,7 +200,8 @@ sage_status_t sage_quantize_qkv(sage_format_t fmt, const void* q, sage_strides_t
   const bool rot = fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
   cudaError_t e = launch_quantize_qk_mxfp4(aq, s, rot);
   if (e == cudaSuccess) e = launch_quantize_qk_mxfp4(ak, s, rot);
-  if (e == cudaSuccess) e = launch_quantize_v(av, s);
+  if (e == cudaSuccess)
+    e = fmt == SAGE_FMT_QK_MXFP4_V_MXFP4 ? launch_quantize_v_mxfp4(av, s) : launch_quantize_v(av, s);
   return from_cuda(e);
 }
 
@@ -215,6 +225,21 @@ sage_status_t sage_quantize_k_smooth(sage_format_t fmt, const void* k, sage_stri
                 status};
   return from_cuda(launch_quantize_k_smooth(a, k_mean, workspace,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sage_status_t sage_quantize_v_mxfp4(const void* v, sage_strides_t vs, int64_t B, int64_t N,
+                                    int64_t H, int64_t D, const int32_t* lens, void* v_q,
+                                    void* v_scale, sage_stream_t stream) {
+  sage_status_t st = check_shape(B, N, H, D);
+  if (st != SAGE_OK) return st;
+  if (!v || !v_q || !v_scale || !aligned(v, 16) || !aligned(v_q, 16) || !aligned(v_scale, 4) ||
+      !strides_ok(vs) || (lens && !aligned(lens, 4)))
+    return SAGE_ERR_INVALID_ARG;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != SAGE_OK) return st;
+  QuantVArgs a{static_cast<const uint16_t*>(v), vs.b, vs.n, vs.h, B, N, H, lens,
+               static_cast<uint8_t*>(v_q), static_cast<float*>(v_scale), nullptr, status};
+  return from_cuda(launch_quantize_v_mxfp4(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_scale,
@@ -248,9 +273,10 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   int* status = nullptr;
   if ((st = device_state(&status)) != SAGE_OK) return st;
   const float c = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  const bool mx = fmt == SAGE_FMT_QK_MXFP4_V_FP8 || fmt == SAGE_FMT_QK_MXFP4H_V_FP8;
+  const bool mx = mx_qk(fmt);
+  const bool v4 = fmt == SAGE_FMT_QK_MXFP4_V_MXFP4;
   AttnLaunch a;
-  a.fmt = mx ? 1 : (fmt == SAGE_FMT_QK_FP8_V_FP8 ? 2 : 0);
+  a.fmt = v4 ? 4 : (mx ? 1 : (fmt == SAGE_FMT_QK_FP8_V_FP8 ? 2 : 0));
   a.q = q_q;
   a.k = k_q;
   a.v = v_q;
@@ -259,7 +285,8 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   p.k_scale = mx ? nullptr : static_cast<const float*>(k_scale);
   p.q_sf = mx ? static_cast<const uint32_t*>(q_scale) : nullptr;
   p.k_sf = mx ? static_cast<const uint32_t*>(k_scale) : nullptr;
-  p.v_scale = v_scale;
+  p.v_scale = v4 ? nullptr : v_scale;
+  p.v_sf = v4 ? reinterpret_cast<const uint32_t*>(v_scale) : nullptr;
   p.k_lens = k_lens;
   p.B = B;
   p.H = H;

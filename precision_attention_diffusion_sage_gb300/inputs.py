@@ -23,7 +23,8 @@ class Workload:
     Nq: int
     Nk: int
     seed: int
-    fmt: int = 0                      # 0: INT8, 1: MXFP4, 2: FP8, 3: rotated MXFP4 Q/K (V FP8)
+    fmt: int = 0                      # 0: INT8, 1: MXFP4, 2: FP8, 3: rotated MXFP4 Q/K (V FP8);
+                                      # 4: MXFP4 Q/K, V and P
     structure: str = "plain"
     smooth_k: bool = False            # K smoothing (INT8 only): channel means removed from K
     k_lens: Optional[List[int]] = field(default=None)
@@ -61,6 +62,8 @@ WORKLOADS = {
     # structure) taken out of K before INT8 quantization
     "video_dit_ksmooth": Workload("video_dit_ksmooth", 1, 40, 14040, 14040, seed=2,
                                   structure="k_mean", smooth_k=True),
+    # MXFP4 Q/K with MXFP4 V and P (the FP4 P V format) on the 8K shape
+    "mxfp4_v4_self": Workload("mxfp4_v4_self", 2, 24, 8192, 8192, seed=4, fmt=4),
     # Hadamard-rotated MXFP4 Q/K on the 8K shape, with the outlier-channel K
     # structure the rotation is meant to spread
     "mxfp4h_self": Workload("mxfp4h_self", 2, 24, 8192, 8192, seed=4, fmt=3,

@@ -28,10 +28,10 @@ def oracle_quantize(fmt, q, k, v, k_lens=None):
     elif fmt == 3:
         qz = oracle.quantize_mxfp4_hadamard(qb)
         kz = oracle.quantize_mxfp4_hadamard(kb, lens=k_lens)
-    else:
+    else:  # MXFP4 Q/K (formats 1 and 4)
         qz = oracle.quantize_mxfp4(qb)
         kz = oracle.quantize_mxfp4(kb, lens=k_lens)
-    vz = oracle.quantize_v_fp8(vb, lens=k_lens)
+    vz = oracle.quantize_v_mxfp4(vb, lens=k_lens) if fmt == 4 else oracle.quantize_v_fp8(vb, lens=k_lens)
     return qz, kz, vz
 
 
@@ -62,8 +62,14 @@ def assert_qk_equal(fmt, gpu_q, gpu_s, ref_q, ref_s):
 
 
 def assert_v_equal(gpu_v, gpu_s, ref_v, ref_s):
+    """V codes and scales bit for bit: FP32 channel scales (E4M3 V) or E8M0
+    bytes (MXFP4 V)."""
     np.testing.assert_array_equal(gpu_v.cpu().numpy(), ref_v)
-    np.testing.assert_array_equal(gpu_s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    gs = gpu_s.cpu().numpy()
+    if ref_s.dtype == np.uint8:
+        np.testing.assert_array_equal(gs, ref_s)
+    else:
+        np.testing.assert_array_equal(gs.view(np.uint32), ref_s.view(np.uint32))
 
 
 def compare_attention(o_gpu, lse_gpu, o_ref, lse_ref, rows=None):

@@ -45,7 +45,10 @@ def _run_gpu(fmt, q, k, v, k_lens=None, num_splits=0, softmax_scale=None):
     Nq, Nk = q.shape[1], k.shape[1]
     qq, qs = binding.sage_quantize_qk(q, fmt)
     kq, ks = binding.sage_quantize_qk(k, fmt, lens=k_lens)
-    vq, vs = binding.sage_quantize_v(v, lens=k_lens)
+    if fmt == binding.FMT_MXFP4_V4:
+        vq, vs = binding.sage_quantize_v_mxfp4(v, lens=k_lens)
+    else:
+        vq, vs = binding.sage_quantize_v(v, lens=k_lens)
     o, lse = binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
                                    num_splits=num_splits, softmax_scale=softmax_scale)
     torch.cuda.synchronize()
@@ -606,7 +609,7 @@ def test_quantize_k_smooth_direct_load_path():
 
 
 # ------------------------------------------------------------------ one-call Q/K/V quantization
-@pytest.mark.parametrize("fmt", [0, 2, 1, 3])
+@pytest.mark.parametrize("fmt", [0, 2, 1, 3, 4])
 @pytest.mark.parametrize("B,Nq,Nk,lens", [(1, 300, 300, None), (2, 257, 512, [512, 300]),
                                           (2, 129, 1000, [0, 999])])
 def test_quantize_qkv_equals_separate_calls_and_oracle(fmt, B, Nq, Nk, lens):
@@ -617,7 +620,8 @@ def test_quantize_qkv_equals_separate_calls_and_oracle(fmt, B, Nq, Nk, lens):
     assert binding.sage_last_device_status() == 0
     sq = binding.sage_quantize_qk(q, fmt)
     sk = binding.sage_quantize_qk(k, fmt, lens=lens)
-    sv = binding.sage_quantize_v(v, lens=lens)
+    sv = (binding.sage_quantize_v_mxfp4(v, lens=lens) if fmt == 4
+          else binding.sage_quantize_v(v, lens=lens))
     for a, b in zip((qq, qs, kq, ks, vq, vs), (*sq, *sk, *sv)):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     qz, kz, vz = oracle_quantize(fmt, q, k, v, k_lens=lens)
@@ -641,3 +645,75 @@ def test_quantize_qkv_packed_and_broadcast_layouts():
         assert_qk_equal(0, *outs[0], *qz)
         assert_qk_equal(0, *outs[1], *kz)
         assert_v_equal(*outs[2], *vz)
+
+
+# ------------------------------------------------------------------ MXFP4 V and P (format 4)
+@pytest.mark.parametrize("B,N,lens", [(1, 256, None), (1, 1, None), (1, 129, None),
+                                      (1, 300, [173]), (2, 512, [512, 0])])
+def test_quantize_v_mxfp4_bitexact(B, N, lens):
+    w = Workload("case", B, 2, N, N, seed=100 + N)
+    _, _, v = make_qkv(w)
+    vq, vs = binding.sage_quantize_v_mxfp4(v.cuda(), lens=lens)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    assert_v_equal(vq, vs, *oracle.quantize_v_mxfp4(bf16_bits(v), lens=lens))
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (127, 64), (129, 65), (300, 300), (513, 77),
+                                   (256, 384), (128, 1000)])
+def test_attention_v4_ragged_tails(Nq, Nk):
+    w, q, k, v = _small(1, 2, Nq, Nk, seed=Nq * 11 + Nk)
+    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(4, q, k, v)
+    qz, kz, vz = oracle_quantize(4, q, k, v)
+    assert_qk_equal(4, qq, qs, *qz)
+    assert_qk_equal(4, kq, ks, *kz)
+    assert_v_equal(vq, vs, *vz)
+    ro, rl = _oracle_attention(4, qz, kz, vz, Nq, Nk)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_v4_cross_ragged_splits_and_scale():
+    w, q, k, v = _small(2, 2, 300, 1000, seed=101, structure="k_offset_std2")
+    lens = [1000, 333]
+    for splits, c in ((1, None), (3, None), (2, 0.05)):
+        _, _, _, o, lse = _run_gpu(4, q, k, v, k_lens=lens, num_splits=splits, softmax_scale=c)
+        qz, kz, vz = oracle_quantize(4, q, k, v, k_lens=lens)
+        ro, rl = _oracle_attention(4, qz, kz, vz, 300, 1000, k_lens=lens, softmax_scale=c)
+        assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_v4_zero_length_batch():
+    w, q, k, v = _small(2, 2, 200, 256, seed=102)
+    lens = [0, 256]
+    _, _, _, o, lse = _run_gpu(4, q, k, v, k_lens=lens)
+    assert torch.all(o[0] == 0)
+    assert torch.all(torch.isneginf(lse[0]))
+    qz, kz, vz = oracle_quantize(4, q, k, v, k_lens=lens)
+    ro, rl = _oracle_attention(4, qz, kz, vz, 200, 256, k_lens=lens)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_v4_deterministic():
+    w = WORKLOADS["mxfp4_v4_self"]
+    q, k, v = make_qkv(w, device="cuda")
+    o1, l1 = binding.sage_attention(q, k, v, fmt=4)
+    for _ in range(2):
+        o2, l2 = binding.sage_attention(q, k, v, fmt=4)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+
+
+def test_full_size_workload_v4():
+    w = WORKLOADS["mxfp4_v4_self"]
+    q, k, v = make_qkv(w, device="cuda")
+    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(4, q, k, v)
+    hs = [0, 11, 23]
+    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
+    qz, kz, vz = oracle_quantize(4, sub(q), sub(k), sub(v))
+    assert_qk_equal(4, qq[:, hs], qs[:, hs], *qz)
+    assert_qk_equal(4, kq[:, hs], ks[:, hs], *kz)
+    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
+    rows = _sample_rows(w.Nq)
+    ro, rl = _oracle_attention(4, qz, kz, vz, w.Nq, w.Nk, rows=rows)
+    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
