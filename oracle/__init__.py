@@ -79,7 +79,12 @@ def _L():
         lib.oracle_fwht128.argtypes = [P, P, I64]
         lib.oracle_attention.restype = None
         lib.oracle_attention.argtypes = [I32, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, D,
-                                         P, I64, P, P, P, I32]
+                                         P, I64, P, P, P, I32, P]
+        lib.oracle_quantize_int8_qsmooth.restype = None
+        lib.oracle_quantize_int8_qsmooth.argtypes = [P, I64, I64, I64, I64, I64, I64, I64, P, P, P,
+                                                     P]
+        lib.oracle_delta_s.restype = None
+        lib.oracle_delta_s.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, P]
         lib.oracle_attention_exact.restype = None
         lib.oracle_attention_exact.argtypes = [P, I64, I64, I64, P, I64, I64, I64, P, I64, I64,
                                                I64, P, I64, I64, I64, I64, I64, D, P, I64, P, P,
@@ -217,6 +222,31 @@ def quantize_int8_smooth(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarr
     return q, s, mu
 
 
+def quantize_int8_qsmooth(x: np.ndarray, lens=None):
+    """Q smoothing then INT8: (codes [B,H,Npad,D], block scales [B,H,Npad/128],
+    block channel means [B,H,Npad/128,D])."""
+    B, N, H, D, sb, sn, sh = _bnhd(x)
+    Np = pad128(N)
+    q = np.zeros((B, H, Np, D), np.int8)
+    s = np.zeros((B, H, Np // 128), np.float32)
+    m = np.zeros((B, H, Np // 128, D), np.float32)
+    ln = _lens(lens)
+    _L().oracle_quantize_int8_qsmooth(_ptr(x), sb, sn, sh, B, N, H, D, _ptr(ln), _ptr(q), _ptr(s),
+                                      _ptr(m))
+    return q, s, m
+
+
+def delta_s(k8: np.ndarray, k_scale: np.ndarray, q_mean: np.ndarray, *, Nq: int, Nk: int,
+            k_mean=None) -> np.ndarray:
+    """dS [B,H,Nq_pad/128,Nk_pad] float64: q_mean . (dequantized K + K's channel means)."""
+    B, H, _, D = k8.shape
+    out = np.zeros((B, H, pad128(Nq) // 128, pad128(Nk)), np.float64)
+    ka, sa, qa = (np.ascontiguousarray(a) for a in (k8, k_scale, q_mean))
+    km = None if k_mean is None else np.ascontiguousarray(k_mean, dtype=np.float32)
+    _L().oracle_delta_s(_ptr(ka), _ptr(sa), _ptr(km), _ptr(qa), B, H, Nq, Nk, D, _ptr(out))
+    return out
+
+
 def k_mean_lse_term(q: np.ndarray, q_scale: np.ndarray, mu: np.ndarray, *, Nq: int,
                     softmax_scale: Optional[float] = None, rows=None) -> np.ndarray:
     """softmax_scale * (s_q q8_i) . mu for every (b, h, evaluated row): the
@@ -257,10 +287,12 @@ def quantize_mxfp4(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
 # ------------------------------------------------------------------ attention
 def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: int = 128,
               softmax_scale: Optional[float] = None, k_lens=None, rows=None,
-              want_weights: bool = False, nthreads: int = 0, k_mean=None):
+              want_weights: bool = False, nthreads: int = 0, k_mean=None, delta_s=None):
     """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K; fmt 2: E4M3 Q/K (V E4M3);
     fmt 4: MXFP4 Q/K with MXFP4 V (quantize_v_mxfp4) and MXFP4 P per 32 keys.
 
+    delta_s (fmt 0 only): the Q smoothing correction of delta_s(), added to every
+    logit of the rows of each 128-query block.
     k_mean (fmt 0 only): the channel means that K smoothing subtracted before
     quantizing K; O is that of the smoothed logits and LSE adds back the
     per-row term softmax_scale * q^ . mean (k_mean_lse_term).
@@ -276,8 +308,10 @@ def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: 
     lse = np.zeros((B, H, nr), np.float64)
     w = np.zeros((B, H, nr, Nk), np.float64) if want_weights else None
     ln = _lens(k_lens)
+    ds = None if delta_s is None else np.ascontiguousarray(delta_s, dtype=np.float64)
+    assert ds is None or fmt == 0, "Q smoothing is defined for the INT8 Q/K format"
     _L().oracle_attention(fmt, *(_ptr(a) for a in arrs), _ptr(ln), B, H, Nq, Nk, D, c, _ptr(r),
-                          nr, _ptr(o), _ptr(lse), _ptr(w), nthreads)
+                          nr, _ptr(o), _ptr(lse), _ptr(w), nthreads, _ptr(ds))
     if k_mean is not None:
         assert fmt == 0, "K smoothing is defined for the INT8 Q/K format"
         lse = lse + k_mean_lse_term(q, q_scale, k_mean, Nq=Nq, softmax_scale=c, rows=r)

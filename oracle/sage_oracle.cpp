@@ -85,6 +85,33 @@ void parallel_for(int64_t n, int nthreads, F f) {
   for (auto& th : pool) th.join();
 }
 
+// The order-independent mean of `count` BF16 values (x[0], x[stride], ...):
+// E = binary32 exponent of their absolute maximum (field at least 1, minus
+// 127); each value m * 2^x contributes m * 2^(x + 40 - E) truncated toward
+// zero; mean = (float)((double)S * 2^(E - 40) / count); 0 when count is 0 or
+// every value is zero.
+float exact_mean(const uint16_t* x, int64_t stride, int64_t count) {
+  float amax = 0.0f;
+  for (int64_t n = 0; n < count; ++n) amax = std::max(amax, std::fabs(bf16_to_float(x[n * stride])));
+  if (count <= 0 || amax == 0.0f) return 0.0f;
+  uint32_t abits;
+  std::memcpy(&abits, &amax, 4);
+  const int E = std::max<int>(1, (abits >> 23) & 0xFF) - 127;
+  int64_t S = 0;
+  for (int64_t n = 0; n < count; ++n) {
+    const uint16_t v = x[n * stride];
+    const int ef = (v >> 7) & 0xFF;
+    const int64_t m = (v & 0x7F) | (ef ? 0x80 : 0);  // integer significand
+    const int xe = std::max(ef, 1) - 127 - 7;          // value = m * 2^xe
+    // <= 33 since |v| <= amax; capped at 40 so a NaN (which the maximum
+    // passes over) still gives a defined shift
+    const int shift = std::min(xe + 40 - E, 40);
+    const int64_t c = shift >= 0 ? (m << shift) : (-shift >= 63 ? 0 : (m >> -shift));
+    S += (v & 0x8000) ? -c : c;
+  }
+  return static_cast<float>(std::ldexp(static_cast<double>(S), E - 40) / static_cast<double>(count));
+}
+
 }  // namespace
 
 extern "C" {
@@ -223,33 +250,8 @@ void oracle_k_mean(const uint16_t* k, int64_t sb, int64_t sn, int64_t sh, int64_
   for (int64_t b = 0; b < B; ++b) {
     const int64_t nv = valid_len(lens, b, N);
     for (int64_t h = 0; h < H; ++h)
-      for (int64_t d = 0; d < D; ++d) {
-        float amax = 0.0f;
-        for (int64_t n = 0; n < nv; ++n)
-          amax = std::max(amax, std::fabs(bf16_to_float(k[b * sb + n * sn + h * sh + d])));
-        float& out = mu[(b * H + h) * D + d];
-        if (nv <= 0 || amax == 0.0f) {
-          out = 0.0f;
-          continue;
-        }
-        uint32_t abits;
-        std::memcpy(&abits, &amax, 4);
-        const int E = std::max<int>(1, (abits >> 23) & 0xFF) - 127;
-        int64_t S = 0;
-        for (int64_t n = 0; n < nv; ++n) {
-          const uint16_t v = k[b * sb + n * sn + h * sh + d];
-          const int ef = (v >> 7) & 0xFF;
-          const int64_t m = (v & 0x7F) | (ef ? 0x80 : 0);     // integer significand
-          const int x = std::max(ef, 1) - 127 - 7;              // value = m * 2^x
-          // <= 33 since |v| <= amax; capped at 40 so a NaN (which the maximum
-          // passes over) still gives a defined shift
-          const int shift = std::min(x + 40 - E, 40);
-          int64_t c = shift >= 0 ? (m << shift) : (-shift >= 63 ? 0 : (m >> -shift));
-          S += (v & 0x8000) ? -c : c;
-        }
-        const double mean = std::ldexp(static_cast<double>(S), E - 40) / static_cast<double>(nv);
-        out = static_cast<float>(mean);
-      }
+      for (int64_t d = 0; d < D; ++d)
+        mu[(b * H + h) * D + d] = exact_mean(k + b * sb + h * sh + d, sn, nv);
   }
 }
 
@@ -300,6 +302,65 @@ void oracle_k_mean_lse_term(const int8_t* q, const float* q_scale, const float* 
       for (int64_t d = 0; d < D; ++d)
         acc += static_cast<double>(q[(bh * Nqp + i) * D + d]) * sq * static_cast<double>(mu[bh * D + d]);
       term[bh * nrows + r] = softmax_scale * acc;
+    }
+}
+
+// Q smoothing for INT8 Q/K (the "_q_smooth_int8_kernel" named on "new MHA v4
+// entrypoint ..."; reading): each 128-token block of Q has its channel means
+// over the block's valid tokens (the exact mean above) subtracted, then the
+// INT8 block rule on y = (float)q - mean. q_mean: float [B][H][Npad/128][D].
+void oracle_quantize_int8_qsmooth(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
+                                  int64_t B, int64_t N, int64_t H, int64_t D,
+                                  const int32_t* lens, int8_t* q, float* scale, float* q_mean) {
+  const int64_t Np = pad128(N), nb = Np / 128;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t nv = valid_len(lens, b, N);
+    for (int64_t h = 0; h < H; ++h)
+      for (int64_t blk = 0; blk < nb; ++blk) {
+        const int64_t n0 = blk * 128, n1 = std::min(n0 + 128, nv);
+        float* m = q_mean + ((b * H + h) * nb + blk) * D;
+        for (int64_t d = 0; d < D; ++d)
+          m[d] = exact_mean(x + b * sb + n0 * sn + h * sh + d, sn, std::max<int64_t>(0, n1 - n0));
+        float amax = 0.0f;
+        for (int64_t n = n0; n < n1; ++n)
+          for (int64_t d = 0; d < D; ++d)
+            amax = std::max(amax, std::fabs(bf16_to_float(x[b * sb + n * sn + h * sh + d]) - m[d]));
+        const float s = amax / 127.0f;
+        scale[(b * H + h) * nb + blk] = s;
+        for (int64_t n = n0; n < n0 + 128; ++n)
+          for (int64_t d = 0; d < D; ++d) {
+            int v = 0;
+            if (n < n1 && s > 0.0f)
+              v = oracle_int8_quantize_value(bf16_to_float(x[b * sb + n * sn + h * sh + d]) - m[d],
+                                             s);
+            q[((b * H + h) * Np + n) * D + d] = static_cast<int8_t>(v);
+          }
+      }
+  }
+}
+
+// The logit correction of Q smoothing ("_compute_delta_s_kernel" on the same
+// page; reading): for query block qb and key j, dS = q_mean[qb] . (k^_j + mu)
+// with k^ = s_k q8 the dequantized INT8 K and mu its channel means when K was
+// smoothed (else 0), in FP64. The logits of the rows of block qb are then
+// softmax_scale * ((s_q q8_i) . k^_j + dS_j) = softmax_scale * (q^_i + q_mean)
+// . (k^_j + mu) up to a per-row constant. Out: double [B][H][Nq_pad/128][Nk_pad].
+void oracle_delta_s(const int8_t* k8, const float* k_scale, const float* k_mean,
+                    const float* q_mean, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
+                    double* out) {
+  const int64_t nbq = pad128(Nq) / 128, Nkp = pad128(Nk), nbk = Nkp / 128;
+  for (int64_t bh = 0; bh < B * H; ++bh)
+    for (int64_t qb = 0; qb < nbq; ++qb) {
+      const float* qm = q_mean + (bh * nbq + qb) * D;
+      for (int64_t j = 0; j < Nkp; ++j) {
+        const double sk = k_scale[bh * nbk + j / 128];
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+          acc += static_cast<double>(qm[d]) *
+                 (sk * static_cast<double>(k8[(bh * Nkp + j) * D + d]) +
+                  (k_mean ? static_cast<double>(k_mean[bh * D + d]) : 0.0));
+        out[(bh * nbq + qb) * Nkp + j] = acc;
+      }
     }
 }
 
@@ -495,7 +556,7 @@ void oracle_attention(int fmt, const void* q_data, const void* q_scale, const vo
                       const void* k_scale, const uint8_t* v8, const float* sv,
                       const int32_t* k_lens, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                       int64_t D, double softmax_scale, const int64_t* rows, int64_t nrows,
-                      double* o, double* lse, double* w, int nthreads) {
+                      double* o, double* lse, double* w, int nthreads, const double* delta_s) {
   const int64_t Nqp = pad128(Nq), Nkp = pad128(Nk);
   if (!rows) nrows = Nq;
   parallel_for(B * H * nrows, nthreads, [&](int64_t idx) {
@@ -553,6 +614,9 @@ void oracle_attention(int fmt, const void* q_data, const void* q_scale, const vo
         t[j] = S * softmax_scale * kLog2e;
       }
     }
+    if (delta_s)  // Q smoothing: the block's correction dS_j, in log2 units
+      for (int64_t j = 0; j < nk; ++j)
+        t[j] += delta_s[(bh * (Nqp / 128) + i / 128) * Nkp + j] * softmax_scale * kLog2e;
     double tmax = -INFINITY;
     for (int64_t j = 0; j < nk; ++j) tmax = std::max(tmax, t[j]);
     const double M = std::ceil(tmax);  // integer row maximum

@@ -74,6 +74,17 @@ void oracle_k_mean(const uint16_t* k, int64_t sb, int64_t sn, int64_t sh, int64_
 void oracle_quantize_int8_smooth(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
                                  int64_t B, int64_t N, int64_t H, int64_t D, const int32_t* lens,
                                  const float* mu, int8_t* q, float* scale);
+/* Q smoothing: per 128-token block the channel means over the block's valid
+ * tokens (the exact mean of oracle_k_mean, over the block) subtracted before
+ * the INT8 block rule. q_mean: float [B][H][Npad/128][D]. */
+void oracle_quantize_int8_qsmooth(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
+                                  int64_t B, int64_t N, int64_t H, int64_t D,
+                                  const int32_t* lens, int8_t* q, float* scale, float* q_mean);
+/* dS[bh][qb][j] = q_mean[bh][qb] . (s_k q8_k[bh][j] + k_mean[bh]) in FP64
+ * (k_mean nullable: K not smoothed). out: double [B][H][Nq_pad/128][Nk_pad]. */
+void oracle_delta_s(const int8_t* k8, const float* k_scale, const float* k_mean,
+                    const float* q_mean, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
+                    double* out);
 /* term[bh][r] = softmax_scale * sum_d (s_q q8_id) mu_d for the evaluated rows
  * (rows NULL: all Nq): what smoothing removed from every logit of row i. */
 void oracle_k_mean_lse_term(const int8_t* q, const float* q_scale, const float* mu, int64_t B,
@@ -105,12 +116,14 @@ void oracle_quantize_v_mxfp4(const uint16_t* v, int64_t sb, int64_t sn, int64_t 
  * Outputs, for the evaluated rows only:
  *   o: double [B][H][nrows][D] (before BF16 rounding), lse: double [B][H][nrows],
  *   w (nullable): double [B][H][nrows][Nk] effective weights dq(P8)/256/l
- *   (0 for masked keys). */
+ *   (0 for masked keys).
+ * delta_s (nullable, fmt 0): the Q smoothing correction of oracle_delta_s,
+ *   added to every logit as softmax_scale * dS[b][h][i / 128][j]. */
 void oracle_attention(int fmt, const void* q_data, const void* q_scale, const void* k_data,
                       const void* k_scale, const uint8_t* v8, const float* sv,
                       const int32_t* k_lens, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                       int64_t D, double softmax_scale, const int64_t* rows, int64_t nrows,
-                      double* o, double* lse, double* w, int nthreads);
+                      double* o, double* lse, double* w, int nthreads, const double* delta_s);
 
 /* Unquantized FP64 softmax attention on the BF16 inputs ([B][N][H][D] with
  * strides), for accuracy reporting and self-tests. Same output layout. */

@@ -718,3 +718,76 @@ def test_mxfp4_pv_close_to_exact():
     oe, _ = oracle.attention_exact(bf16_bits(q), bf16_bits(k), bf16_bits(v))
     cos = (o * oe).sum() / math.sqrt((o * o).sum() * (oe * oe).sum())
     assert cos >= 0.95
+
+
+# ------------------------------------------------------------------ Q smoothing and dS
+def test_qsmooth_block_means_exact_and_ragged():
+    """Per 128-token block: on multiples of 1/8 the block mean is the exact
+    sum divided by the block's valid-token count (the last block partial,
+    tokens past the length left out); padding rows are zero codes."""
+    rng = np.random.RandomState(21)
+    x = rng.randint(-64, 65, size=(1, 300, 2, 128)).astype(np.float32) / 8
+    x += rng.randint(-4, 5, size=(1, 1, 2, 128))
+    x[:, 250:] = 1000.0                      # past the valid length
+    q8, s, m = oracle.quantize_int8_qsmooth(_bits(x), lens=[250])
+    for blk, (n0, n1) in enumerate([(0, 128), (128, 250), (256, 256)]):
+        want = (x[0, n0:n1].astype(np.float64).sum(0) / max(n1 - n0, 1)).astype(np.float32)
+        np.testing.assert_array_equal(m[0, :, blk], want if n1 > n0 else np.zeros((2, 128), np.float32))
+    assert np.all(q8[0, :, 250:] == 0)
+
+
+def test_qsmooth_block_translation_invariance():
+    """Adding a constant per (block, channel) moves that block's mean by it and
+    leaves every code and scale unchanged (dyadic values: all steps exact)."""
+    rng = np.random.RandomState(22)
+    x = rng.randint(-64, 65, size=(1, 256, 2, 128)).astype(np.float32) / 8
+    c = np.zeros_like(x)
+    c[:, :128] = rng.randint(-4, 5, size=(1, 1, 2, 128))
+    c[:, 128:] = rng.randint(-4, 5, size=(1, 1, 2, 128))
+    q0, s0, m0 = oracle.quantize_int8_qsmooth(_bits(x))
+    q1, s1, m1 = oracle.quantize_int8_qsmooth(_bits(x + c))
+    np.testing.assert_array_equal(m1[0, :, 0], m0[0, :, 0] + c[0, 0].astype(np.float32))
+    np.testing.assert_array_equal(m1[0, :, 1], m0[0, :, 1] + c[0, 128].astype(np.float32))
+    np.testing.assert_array_equal(q1, q0)
+    np.testing.assert_array_equal(s1.view(np.uint32), s0.view(np.uint32))
+
+
+def test_qsmooth_zero_mean_reduces_to_plain_int8():
+    w, q, k, v = _tiny(N=64)
+    qf = _f32(bf16_bits(q))
+    x = np.concatenate([qf, -qf], axis=1)    # one block of +-pairs: mean 0
+    q0, s0 = oracle.quantize_int8(_bits(x))
+    q1, s1, m1 = oracle.quantize_int8_qsmooth(_bits(x))
+    assert np.all(m1 == 0.0)
+    np.testing.assert_array_equal(q1, q0)
+    np.testing.assert_array_equal(s1.view(np.uint32), s0.view(np.uint32))
+
+
+@pytest.mark.parametrize("smooth_k", [False, True])
+def test_qsmooth_logits_identity(smooth_k):
+    """With the dS correction the LSE is the logsumexp of softmax_scale *
+    (q^_s + q_mean) . (k^ + mu): the reconstructed Q against the dequantized
+    (and, with K smoothing, re-centred) K, in numpy from the quantized data."""
+    w = Workload("qs", 1, 2, 300, 200, seed=23)
+    q, k, v = make_qkv(w)
+    g = torch.Generator().manual_seed(24)
+    q = (q.float() + 2.0 * torch.randn(1, 1, 2, 128, generator=g)).to(torch.bfloat16)
+    k = (k.float() + 2.0 * torch.randn(1, 1, 2, 128, generator=g)).to(torch.bfloat16)
+    qq, qs, qm = oracle.quantize_int8_qsmooth(bf16_bits(q))
+    if smooth_k:
+        kq, ks, mu = oracle.quantize_int8_smooth(bf16_bits(k))
+    else:
+        (kq, ks), mu = oracle.quantize_int8(bf16_bits(k)), None
+    vz = oracle.quantize_v_fp8(bf16_bits(v))
+    ds = oracle.delta_s(kq, ks, qm, Nq=300, Nk=200, k_mean=mu)
+    o, lse, _ = oracle.attention(0, qq, qs, kq, ks, *vz, Nq=300, Nk=200, delta_s=ds, k_mean=mu)
+    qhat = _dequant_int8(qq, qs)[:, :, :300] + np.repeat(qm.astype(np.float64), 128, axis=2)[:, :, :300]
+    khat = _dequant_int8(kq, ks)[:, :, :200] + (0 if mu is None else mu.astype(np.float64)[:, :, None, :])
+    z = (1 / math.sqrt(128)) * np.einsum("bhid,bhjd->bhij", qhat, khat)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(z, axis=-1), rtol=0, atol=1e-9)
+    # and the output is close to unquantized attention, closer than without Q smoothing
+    oe, _ = oracle.attention_exact(bf16_bits(q), bf16_bits(k), bf16_bits(v))
+    o0, _, _ = oracle.attention(0, *oracle.quantize_int8(bf16_bits(q)), kq, ks, *vz, Nq=300,
+                                Nk=200, k_mean=mu)
+    err = lambda a: float(np.abs(a - oe).max())  # noqa: E731
+    assert err(o) < err(o0)
