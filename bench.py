@@ -108,6 +108,8 @@ def _quant_bytes(w, Nqp: int, Nkp: int) -> float:
           + B * H * Nkp * D * code)
     if w.smooth_k:  # K also read by the channel-maximum and the fixed-point-sum passes
         qk += 2 * B * w.Nk * H * D * 2
+    if w.smooth_q:  # dS: K codes read, one FP32 per (query block, key) written
+        qk += B * H * Nkp * D * code + B * H * (Nqp // 128) * Nkp * 4
     if w.fmt == 4:  # MXFP4 V: one pass, read once, packed E2M1 + E8M0 per 32 tokens
         return qk + B * w.Nk * H * D * 2 + B * H * D * Nkp * (0.5 + 1.0 / 32)
     return qk + B * w.Nk * H * D * 2 * 2 + B * H * D * Nkp
@@ -181,18 +183,23 @@ def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64, nthreads: int = 0
         t0 = time.perf_counter()
         quant_qk = {0: oracle.quantize_int8, 1: oracle.quantize_mxfp4, 2: oracle.quantize_fp8_qk,
                     3: oracle.quantize_mxfp4_hadamard, 4: oracle.quantize_mxfp4}[w.fmt]
-        qz = quant_qk(qb)
-        km = None
+        qm = km = ds = None
+        if w.smooth_q:
+            *qz, qm = oracle.quantize_int8_qsmooth(qb)
+        else:
+            qz = quant_qk(qb)
         if w.smooth_k:
             *kz, km = oracle.quantize_int8_smooth(kb, lens=lens)
         else:
             kz = quant_qk(kb, lens=lens)
         vz = (oracle.quantize_v_mxfp4(vb, lens=lens) if w.fmt == 4
               else oracle.quantize_v_fp8(vb, lens=lens))
+        if w.smooth_q:
+            ds = oracle.delta_s(kz[0], kz[1], qm, Nq=w.Nq, Nk=w.Nk, k_mean=km)
         # rotated MXFP4: MXFP4 codes of QH and KH, logits (QH)(KH)^T / 128
         afmt, c = (1, 1.0 / math.sqrt(w.D) / 128) if w.fmt == 3 else (w.fmt, None)
         oracle.attention(afmt, *qz, *kz, *vz, Nq=w.Nq, Nk=w.Nk, k_lens=lens, rows=rows,
-                         softmax_scale=c, nthreads=nthreads, k_mean=km)
+                         softmax_scale=c, nthreads=nthreads, k_mean=km, delta_s=ds)
         return time.perf_counter() - t0
 
     def rows_of(n):
@@ -324,8 +331,16 @@ def main():
     # lands on the next kernel).
     flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
 
+    qm = (torch.empty((B, H, Nqp // 128, D), dtype=torch.float32, device=dev) if w.smooth_q
+          else None)
+    dsb = (torch.empty((B, H, Nqp // 128, Nkp), dtype=torch.float32, device=dev) if w.smooth_q
+           else None)
+
     def quant_q():
-        binding.sage_quantize_qk(q, fmt, out=qq, scale=qs)
+        if w.smooth_q:
+            binding.sage_quantize_q_smooth(q, out=qq, scale=qs, q_mean=qm)
+        else:
+            binding.sage_quantize_qk(q, fmt, out=qq, scale=qs)
 
     km = torch.empty((B, H, D), dtype=torch.float32, device=dev) if w.smooth_k else None
     kws = (torch.empty(binding.sage_workspace_bytes(3, fmt, B, H, Nk, Nk), dtype=torch.uint8,
@@ -344,18 +359,28 @@ def main():
         else:
             binding.sage_quantize_v(v, lens=k_lens, out=vq, scale=vs, workspace=vws)
 
+    def delta_s():
+        binding.sage_delta_s(qm, kq, ks, Nq=Nq, Nk=Nk, k_mean=km, out=dsb)
+
     def attn():
         binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens, out=o,
-                              lse=lse, num_splits=args.splits, workspace=aws, k_mean=km)
+                              lse=lse, num_splits=args.splits, workspace=aws, k_mean=km,
+                              delta_s=dsb)
 
     def quant_qkv():
         binding.sage_quantize_qkv(q, k, v, fmt, k_lens=k_lens, outs=((qq, qs), (kq, ks), (vq, vs)),
                                   workspace=vws)
 
-    # The step: one quantize call for Q, K and V (K smoothing: the three calls
-    # it needs), then attention. The separate calls are timed as a diagnostic.
+    # The step: one quantize call for Q, K and V (with smoothing: the three
+    # calls it needs, and Q smoothing's dS), then attention. The separate
+    # calls are timed as a diagnostic.
     calls = (quant_q, quant_k, quant_v, attn)
-    quant_step = (quant_q, quant_k, quant_v) if w.smooth_k else (quant_qkv,)
+    if w.smooth_q:
+        quant_step = (quant_q, quant_k, quant_v, delta_s)
+    elif w.smooth_k:
+        quant_step = (quant_q, quant_k, quant_v)
+    else:
+        quant_step = (quant_qkv,)
     step_calls = quant_step + (attn,)
     for _ in range(args.warmup):
         for c in calls + step_calls:
@@ -444,7 +469,8 @@ def main():
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
             oo, ll = binding.sage_attention(qd, kd, vd, fmt=fmt, k_lens=k_lens,
-                                            num_splits=args.splits, smooth_k=w.smooth_k)
+                                            num_splits=args.splits, smooth_k=w.smooth_k,
+                                            smooth_q=w.smooth_q)
             oh.copy_(oo, non_blocking=True)
             lh.copy_(ll, non_blocking=True)
 
@@ -482,8 +508,8 @@ def main():
     # Kernels per step: INT8/FP8 fused Q/K/V pass + V encode; MXFP4 formats Q,
     # K, V maxima, V encode; K smoothing Q, four K kernels (maxima, sums,
     # means, encode), V maxima, V encode; then attention (+ split merge).
-    if w.smooth_k:
-        quant_launches = 1 + 4 + 2
+    if w.smooth_k or w.smooth_q:
+        quant_launches = 1 + (4 if w.smooth_k else 1) + 2 + (1 if w.smooth_q else 0)
     elif fmt in (binding.FMT_INT8, binding.FMT_FP8):
         quant_launches = 2
     else:
@@ -514,6 +540,7 @@ def main():
                    "heads_override": args.heads > 0,
                    "format": fmt_names[fmt][1],
                    "k_smoothing": w.smooth_k,
+                   "q_smoothing": w.smooth_q,
                    "splits": nsplit,
                    "l2": "flushed between steps (256 MiB read outside the timed events)",
                    "launch": ("two CUDA graphs per step: the quantize call (sage_quantize_qkv; with K "

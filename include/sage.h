@@ -240,6 +240,34 @@ sage_status_t sage_quantize_k_smooth(sage_format_t fmt, const void* k, sage_stri
                                      float* k_mean, void* workspace, size_t ws_bytes,
                                      sage_stream_t stream);
 
+/* Q smoothing for the INT8 Q/K format (the "_q_smooth_int8_kernel" named on
+ * "new MHA v4 entrypoint ..."; reading): each 128-token block of Q has its
+ * channel means over the block's tokens subtracted (the exact mean of
+ * sage_quantize_k_smooth, taken over the block) before the INT8 block rule
+ * of sage_quantize_qk. The removed part is restored inside the logits by
+ * sage_delta_s and sage_attn_options_t.delta_s.
+ *   q, qs, B, N, H, D, q_q, q_scale : as sage_quantize_qk (Q has no lens).
+ *   q_mean : output float [B][H][Npad/128][D], 16-byte aligned.
+ * One launch, no workspace. Q must be finite. */
+sage_status_t sage_quantize_q_smooth(sage_format_t fmt, const void* q, sage_strides_t qs,
+                                     int64_t B, int64_t N, int64_t H, int64_t D, void* q_q,
+                                     void* q_scale, float* q_mean, sage_stream_t stream);
+
+/* The logit correction of Q smoothing (the "_compute_delta_s_kernel" of the
+ * same page; reading): delta_s[b][h][qb][j] = q_mean[b][h][qb] . (k^_j + mu)
+ * with k^ = s_k k8 the dequantized INT8 K of sage_quantize_qk or
+ * sage_quantize_k_smooth and mu the K channel means (k_mean, nullable: K not
+ * smoothed), for every query block qb < Nq_pad/128 and padded key j <
+ * Nk_pad, in binary32. With it the attention logits are softmax_scale *
+ * (q^_s + q_mean) . (k^ + mu) up to a per-row constant that the K-smoothing
+ * LSE term supplies.
+ *   delta_s : output float [B][H][Nq_pad/128][Nk_pad], 16-byte aligned.
+ * One launch, no workspace. */
+sage_status_t sage_delta_s(sage_format_t fmt, const float* q_mean, const void* k_q,
+                           const void* k_scale, const float* k_mean, int64_t B, int64_t H,
+                           int64_t Nq, int64_t Nk, int64_t D, float* delta_s,
+                           sage_stream_t stream);
+
 typedef struct {
   int32_t num_splits;   /* KV splits: 0 = library choice, 1 = no split, >1 = forced */
   int32_t cta_mode;     /* reserved: 0 = library choice */
@@ -247,6 +275,9 @@ typedef struct {
                            was smoothed (SAGE_FMT_QK_INT8_V_FP8 only; 16-byte aligned);
                            LSE_i then adds softmax_scale * (s_q q8_i) . k_mean, the
                            per-row logit term smoothing removed (O is unchanged by it) */
+  const float* delta_s; /* nullable: Q smoothing's dS from sage_delta_s (INT8 only;
+                           16-byte aligned): every logit of row i gains
+                           softmax_scale * delta_s[b][h][i / 128][j] */
 } sage_attn_options_t;
 
 /* Attention forward ("[ROCm] Add aiter_sage_attn ...", Changes; "new MHA v4

@@ -238,13 +238,24 @@ def quantize_int8_qsmooth(x: np.ndarray, lens=None):
 
 def delta_s(k8: np.ndarray, k_scale: np.ndarray, q_mean: np.ndarray, *, Nq: int, Nk: int,
             k_mean=None) -> np.ndarray:
-    """dS [B,H,Nq_pad/128,Nk_pad] float64: q_mean . (dequantized K + K's channel means)."""
+    """dS [B,H,Nq_pad/128,Nk_pad] float64: q_grid . (dequantized K + K's channel means),
+    q_grid the block means on the 16-bit grid 2^(E-13) (see q_grid())."""
     B, H, _, D = k8.shape
     out = np.zeros((B, H, pad128(Nq) // 128, pad128(Nk)), np.float64)
     ka, sa, qa = (np.ascontiguousarray(a) for a in (k8, k_scale, q_mean))
     km = None if k_mean is None else np.ascontiguousarray(k_mean, dtype=np.float32)
     _L().oracle_delta_s(_ptr(ka), _ptr(sa), _ptr(km), _ptr(qa), B, H, Nq, Nk, D, _ptr(out))
     return out
+
+
+def q_grid(q_mean: np.ndarray) -> np.ndarray:
+    """The block means as dS uses them: per block, E = exponent of the largest
+    |mean|, values rounded (nearest even) to multiples of 2^(E - 13)."""
+    qm = np.asarray(q_mean, dtype=np.float32)
+    amax = np.abs(qm).max(axis=-1, keepdims=True)
+    e = ((amax.view(np.uint32) >> 23) & 0xFF).astype(np.int64)
+    E = np.maximum(e, 1) - 127
+    return np.rint(qm.astype(np.float64) * np.exp2(13.0 - E)) * np.exp2(E - 13.0)
 
 
 def k_mean_lse_term(q: np.ndarray, q_scale: np.ndarray, mu: np.ndarray, *, Nq: int,

@@ -340,26 +340,40 @@ void oracle_quantize_int8_qsmooth(const uint16_t* x, int64_t sb, int64_t sn, int
 }
 
 // The logit correction of Q smoothing ("_compute_delta_s_kernel" on the same
-// page; reading): for query block qb and key j, dS = q_mean[qb] . (k^_j + mu)
-// with k^ = s_k q8 the dequantized INT8 K and mu its channel means when K was
-// smoothed (else 0), in FP64. The logits of the rows of block qb are then
-// softmax_scale * ((s_q q8_i) . k^_j + dS_j) = softmax_scale * (q^_i + q_mean)
-// . (k^_j + mu) up to a per-row constant. Out: double [B][H][Nq_pad/128][Nk_pad].
+// page; reading): the block means go on a 16-bit grid relative to the
+// block's largest, so that the correction is an exact integer dot product.
+// With E the binary32 exponent of max_d |q_mean_d| (field at least 1, minus
+// 127), q_int_d = rne(q_mean_d 2^(13 - E)) (|q_int| <= 2^14, a 16-bit integer)
+// and q_grid_d = q_int_d 2^(E - 13); then for key j
+//   dS_j = s_k 2^(E - 13) sum_d q_int_d k8_jd + q_grid . mu
+// (the sum exact; mu = K's channel means when K was smoothed, else 0), in
+// FP64. The logits of the block's rows are softmax_scale * ((s_q q8_i) . k^_j
+// + dS_j) = softmax_scale * (q^_i + q_grid) . (k^_j + mu) up to a per-row
+// constant. Out: double [B][H][Nq_pad/128][Nk_pad].
 void oracle_delta_s(const int8_t* k8, const float* k_scale, const float* k_mean,
                     const float* q_mean, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
                     double* out) {
   const int64_t nbq = pad128(Nq) / 128, Nkp = pad128(Nk), nbk = Nkp / 128;
+  std::vector<int64_t> qi(D);
   for (int64_t bh = 0; bh < B * H; ++bh)
     for (int64_t qb = 0; qb < nbq; ++qb) {
       const float* qm = q_mean + (bh * nbq + qb) * D;
+      float amax = 0.0f;
+      for (int64_t d = 0; d < D; ++d) amax = std::max(amax, std::fabs(qm[d]));
+      uint32_t abits;
+      std::memcpy(&abits, &amax, 4);
+      const int E = std::max<int>(1, (abits >> 23) & 0xFF) - 127;
+      double cmu = 0.0;  // q_grid . mu
+      for (int64_t d = 0; d < D; ++d) {
+        qi[d] = static_cast<int64_t>(std::nearbyint(std::ldexp(static_cast<double>(qm[d]), 13 - E)));
+        if (k_mean)
+          cmu += std::ldexp(static_cast<double>(qi[d]), E - 13) * static_cast<double>(k_mean[bh * D + d]);
+      }
       for (int64_t j = 0; j < Nkp; ++j) {
-        const double sk = k_scale[bh * nbk + j / 128];
-        double acc = 0.0;
-        for (int64_t d = 0; d < D; ++d)
-          acc += static_cast<double>(qm[d]) *
-                 (sk * static_cast<double>(k8[(bh * Nkp + j) * D + d]) +
-                  (k_mean ? static_cast<double>(k_mean[bh * D + d]) : 0.0));
-        out[(bh * nbq + qb) * Nkp + j] = acc;
+        int64_t S = 0;
+        for (int64_t d = 0; d < D; ++d) S += qi[d] * static_cast<int64_t>(k8[(bh * Nkp + j) * D + d]);
+        out[(bh * nbq + qb) * Nkp + j] =
+            static_cast<double>(k_scale[bh * nbk + j / 128]) * std::ldexp(static_cast<double>(S), E - 13) + cmu;
       }
     }
 }

@@ -80,8 +80,11 @@ void oracle_quantize_int8_smooth(const uint16_t* x, int64_t sb, int64_t sn, int6
 void oracle_quantize_int8_qsmooth(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
                                   int64_t B, int64_t N, int64_t H, int64_t D,
                                   const int32_t* lens, int8_t* q, float* scale, float* q_mean);
-/* dS[bh][qb][j] = q_mean[bh][qb] . (s_k q8_k[bh][j] + k_mean[bh]) in FP64
- * (k_mean nullable: K not smoothed). out: double [B][H][Nq_pad/128][Nk_pad]. */
+/* dS[bh][qb][j] = q_grid[bh][qb] . (s_k q8_k[bh][j] + k_mean[bh]) in FP64, with
+ * q_grid the block means on the 16-bit grid 2^(E - 13) (E = exponent of the
+ * block's largest |mean|, round to nearest even); the integer part of the
+ * sum is exact. k_mean nullable (K not smoothed).
+ * out: double [B][H][Nq_pad/128][Nk_pad]. */
 void oracle_delta_s(const int8_t* k8, const float* k_scale, const float* k_mean,
                     const float* q_mean, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
                     double* out);

@@ -38,7 +38,7 @@ class Strides(ctypes.Structure):
 
 class AttnOptions(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int32), ("cta_mode", ctypes.c_int32),
-                ("k_mean", ctypes.c_void_p)]
+                ("k_mean", ctypes.c_void_p), ("delta_s", ctypes.c_void_p)]
 
 
 _P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
@@ -57,6 +57,10 @@ _lib.sage_quantize_qkv.restype = _I32
 _lib.sage_quantize_qkv.argtypes = [_I32, _P, Strides, _P, Strides, _P, Strides, _I64, _I64, _I64,
                                    _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                    _P]
+_lib.sage_quantize_q_smooth.restype = _I32
+_lib.sage_quantize_q_smooth.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P]
+_lib.sage_delta_s.restype = _I32
+_lib.sage_delta_s.argtypes = [_I32, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P]
 _lib.sage_quantize_k_smooth.restype = _I32
 _lib.sage_quantize_k_smooth.argtypes = [_I32, _P, Strides, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
                                         _P, ctypes.c_size_t, _P]
@@ -245,6 +249,40 @@ def sage_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: in
     return (qq, qs), (kq, ks), (vq, vs)
 
 
+def sage_quantize_q_smooth(q: torch.Tensor, out: Optional[torch.Tensor] = None,
+                           scale: Optional[torch.Tensor] = None,
+                           q_mean: Optional[torch.Tensor] = None):
+    """Q smoothing + INT8 quantization of BF16 Q ``[B, N, H, D]``: (codes held as
+    float16 ``[B, H, Npad, D]``, float32 block scales ``[B, H, Npad/128]``,
+    float32 block channel means ``[B, H, Npad/128, D]``)."""
+    B, N, H, D = q.shape
+    Np = pad128(N)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, Np, D), dtype=torch.float16, device=dev)
+    if scale is None:
+        scale = torch.empty((B, H, Np // 128), dtype=torch.float32, device=dev)
+    if q_mean is None:
+        q_mean = torch.empty((B, H, Np // 128, D), dtype=torch.float32, device=dev)
+    _check(_lib.sage_quantize_q_smooth(FMT_INT8, _ptr(q), _bnhd_strides(q), B, N, H, D, _ptr(out),
+                                       _ptr(scale), _ptr(q_mean), _stream()),
+           "sage_quantize_q_smooth")
+    return out, scale, q_mean
+
+
+def sage_delta_s(q_mean: torch.Tensor, k_q: torch.Tensor, k_scale: torch.Tensor, *, Nq: int,
+                 Nk: int, k_mean: Optional[torch.Tensor] = None,
+                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Q smoothing's logit correction dS ``[B, H, Nq_pad/128, Nk_pad]`` (float32)."""
+    B, H = k_q.shape[0], k_q.shape[1]
+    if out is None:
+        out = torch.empty((B, H, pad128(Nq) // 128, pad128(Nk)), dtype=torch.float32,
+                          device=k_q.device)
+    _check(_lib.sage_delta_s(FMT_INT8, _ptr(q_mean), _ptr(k_q), _ptr(k_scale), _ptr(k_mean), B, H,
+                             Nq, Nk, 128, _ptr(out), _stream()), "sage_delta_s")
+    return out
+
+
 def sage_quantize_k_smooth(k: torch.Tensor, lens=None, out: Optional[torch.Tensor] = None,
                            scale: Optional[torch.Tensor] = None,
                            k_mean: Optional[torch.Tensor] = None,
@@ -275,7 +313,8 @@ def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int
                   k_lens=None, softmax_scale: Optional[float] = None, causal: int = 0,
                   out: Optional[torch.Tensor] = None, return_lse: bool = True,
                   lse: Optional[torch.Tensor] = None, num_splits: int = 0,
-                  workspace: Optional[torch.Tensor] = None, k_mean: Optional[torch.Tensor] = None):
+                  workspace: Optional[torch.Tensor] = None, k_mean: Optional[torch.Tensor] = None,
+                  delta_s: Optional[torch.Tensor] = None):
     """Attention forward on quantized operands. Returns (O ``[B, Nq, H, D]`` bf16, LSE or None).
     k_mean: the channel means from sage_quantize_k_smooth when K was smoothed."""
     B, H = q_q.shape[0], q_q.shape[1]
@@ -289,7 +328,8 @@ def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int
     if need > 0 and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ln = _lens_tensor(k_lens, dev)
-    opts = AttnOptions(num_splits, 0, None if k_mean is None else k_mean.data_ptr())
+    opts = AttnOptions(num_splits, 0, None if k_mean is None else k_mean.data_ptr(),
+                       None if delta_s is None else delta_s.data_ptr())
     sc = -1.0 if softmax_scale is None else float(softmax_scale)
     _check(_lib.sage_attn_fwd(fmt, _ptr(q_q), _ptr(q_scale), _ptr(k_q), _ptr(k_scale), _ptr(v_q),
                               _ptr(v_scale), _ptr(ln), B, H, Nq, Nk, D, sc, causal, _ptr(out),
@@ -306,22 +346,32 @@ def sage_last_device_status() -> int:
 
 def sage_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: int = FMT_INT8,
                    k_lens=None, softmax_scale: Optional[float] = None, num_splits: int = 0,
-                   return_lse: bool = True, smooth_k: bool = False):
-    """Quantize Q/K/V (one sage_quantize_qkv call) and attend. smooth_k
+                   return_lse: bool = True, smooth_k: bool = False, smooth_q: bool = False):
+    """Quantize Q/K/V (one sage_quantize_qkv call) and attend. smooth_q (INT8
+    only) quantizes Q with sage_quantize_q_smooth and adds sage_delta_s's
+    correction to the logits. smooth_k
     (INT8 only) quantizes K with sage_quantize_k_smooth and passes its channel
     means to the attention call."""
     B, Nq, H, D = q.shape
     Nk = k.shape[1]
-    km = None
-    if smooth_k:
-        qq, qs = sage_quantize_qk(q, fmt)
-        kq, ks, km = sage_quantize_k_smooth(k, lens=k_lens)
+    km = ds = None
+    if smooth_k or smooth_q:
+        if smooth_q:
+            qq, qs, qm = sage_quantize_q_smooth(q)
+        else:
+            qq, qs = sage_quantize_qk(q, fmt)
+        if smooth_k:
+            kq, ks, km = sage_quantize_k_smooth(k, lens=k_lens)
+        else:
+            kq, ks = sage_quantize_qk(k, fmt, lens=k_lens)
         vq, vs = sage_quantize_v(v, lens=k_lens)
+        if smooth_q:
+            ds = sage_delta_s(qm, kq, ks, Nq=Nq, Nk=Nk, k_mean=km)
     else:
         (qq, qs), (kq, ks), (vq, vs) = sage_quantize_qkv(q, k, v, fmt, k_lens=k_lens)
     return sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
                          softmax_scale=softmax_scale, num_splits=num_splits,
-                         return_lse=return_lse, k_mean=km)
+                         return_lse=return_lse, k_mean=km, delta_s=ds)
 
 
 def int8_codes(x_q: torch.Tensor) -> torch.Tensor:

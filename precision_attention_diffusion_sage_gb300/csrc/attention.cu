@@ -289,7 +289,9 @@ constexpr int attn_threads() { return NQT == 1 ? 7 * 32 : 12 * 32; }
 template <int FMT, int NQT>
 __host__ __device__ constexpr bool attn_split_regs() { return !is_mx<FMT>() && NQT == 2; }
 
-template <int FMT, int NQT, int STAGES>
+// DS: Q smoothing's dS is added to the logits (INT8 only; a separate
+// instance, so the plain path keeps its register allocation).
+template <int FMT, int NQT, int STAGES, bool DS = false>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     sage_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
@@ -727,8 +729,9 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     float alpha_q = p.scale_log2;
     const float* kscale = nullptr;
     float sk_next = 1.0f;  // K block scale, loaded one tile ahead
+    float sq = 0.0f;       // Q block scale (INT8 / FP8)
     if constexpr (!kMx) {
-      const float sq = qt < p.nbq ? __ldg(&p.q_scale[bh * p.nbq + qt]) : 0.0f;
+      sq = qt < p.nbq ? __ldg(&p.q_scale[bh * p.nbq + qt]) : 0.0f;
       alpha_q = sq * p.scale_log2;
       kscale = p.k_scale + bh * p.nbk;
       sk_next = __ldg(&kscale[j0]);
@@ -773,13 +776,38 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       // and p = 0 with no per-element test in the exponential loop. A zero
       // scale (an all-zero block) only has exact-zero scores, for which
       // FLT_MIN gives the same x as zero would.
-      const float alpha = fmaxf(alpha_q * sk, 1.17549435e-38f);
+      float alpha = fmaxf(alpha_q * sk, 1.17549435e-38f);
       const int key0 = j * 128 + hu * kStep;
       const int nvalid = nk - key0 < kStep ? nk - key0 : kStep;
       if (nvalid < kStep) {  // keys past the end: -inf, p = 0
 #pragma unroll
         for (int c = 0; c < kStep; ++c)
           if (c >= nvalid) s[c] = -INFINITY;
+      }
+      if constexpr (DS) {
+        // Q smoothing: every logit of this query block gains dS_j (natural
+        // units, the same for all rows), read through L1 (uniform addresses)
+        // after a prefetch one key tile ahead. s becomes the natural-unit
+        // logit S s_q s_k + dS_j and the multiplier softmax_scale log2(e).
+        static_assert(FMT == 0, "dS is defined for the INT8 format");
+        if (qt < p.nbq) {
+          const float* dsr = p.delta_s + (bh * p.nbq + qt) * Nk_pad + key0;
+          if (lane == 0 && iu + 1 < niter)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(dsr + 128 + (warp & 3) * 32));
+          const float beta = fmaxf(sq * sk, 1.17549435e-38f);  // > 0: -inf stays -inf
+          const float2 beta2 = make_float2(beta, beta);
+#pragma unroll
+          for (int c = 0; c < kStep; c += 4) {
+            const float4 d = __ldg(reinterpret_cast<const float4*>(dsr + c));
+            const float2 t01 = __ffma2_rn(make_float2(s[c], s[c + 1]), beta2, make_float2(d.x, d.y));
+            const float2 t23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), beta2, make_float2(d.z, d.w));
+            s[c] = t01.x;
+            s[c + 1] = t01.y;
+            s[c + 2] = t23.x;
+            s[c + 3] = t23.y;
+          }
+          alpha = p.scale_log2;
+        }
       }
       // Format 4 also keeps the maxima of the two 32-key blocks (P's scales).
       float bm0 = 0.0f, bm1 = 0.0f, mx;
@@ -1053,12 +1081,12 @@ bool make_map_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int es
   return encode_tiled(m, dt, 2, ptr, dims, strides, box, swizzle);
 }
 
-template <int FMT, int NQT, int STAGES>
+template <int FMT, int NQT, int STAGES, bool DS = false>
 cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mo, const AttnParams& p, cudaStream_t stream) {
   using L = SmemLayout<FMT, NQT, STAGES>;
   static_assert(L::kDynamic <= 232448, "shared memory budget");
-  constexpr auto kern = sage_attn_kernel<FMT, NQT, STAGES>;
+  constexpr auto kern = sage_attn_kernel<FMT, NQT, STAGES, DS>;
   cudaError_t e = once_per_device<kern>([]() {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
     if (r != cudaSuccess) return r;
@@ -1147,8 +1175,10 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   const bool two = attn_q_tiles_per_cta(p.nbq) == 2;
   cudaError_t e;
   if (a.fmt == 0)
-    e = two ? launch_variant<0, 2, 2>(mq, mk, mv, mo, p, stream)
-            : launch_variant<0, 1, 3>(mq, mk, mv, mo, p, stream);
+    e = p.delta_s ? (two ? launch_variant<0, 2, 2, true>(mq, mk, mv, mo, p, stream)
+                         : launch_variant<0, 1, 3, true>(mq, mk, mv, mo, p, stream))
+                  : (two ? launch_variant<0, 2, 2>(mq, mk, mv, mo, p, stream)
+                         : launch_variant<0, 1, 3>(mq, mk, mv, mo, p, stream));
   else if (a.fmt == 2)
     e = two ? launch_variant<2, 2, 4>(mq, mk, mv, mo, p, stream)
             : launch_variant<2, 1, 4>(mq, mk, mv, mo, p, stream);

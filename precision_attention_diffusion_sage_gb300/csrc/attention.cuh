@@ -22,6 +22,7 @@ struct AttnParams {
   int64_t osb, osn, osh;
   float* lse;            // nullable [B][H][Nq]
   const float* k_mean;   // nullable [B][H][128], INT8 only: channel means removed by K smoothing
+  const float* delta_s;  // nullable [B][H][nbq][Nk_pad], INT8 only: Q smoothing's dS (natural units)
   int num_splits;
   int o_tma;             // 1: O stored through the tensor map (set by the launcher)
   float* o_part;         // [splits][B][H][Nq][128] when num_splits > 1

@@ -659,6 +659,215 @@ __global__ void __launch_bounds__(256) quantize_k_smooth_kernel(KSmoothArgs a) {
 }
 
 // ----------------------------------------------------------------------------
+// Q smoothing (INT8): one CTA per (h, 128-token block, b). The block's channel
+// means over its valid tokens (the exact fixed-point mean of K smoothing,
+// over the block), y = q - mean in binary32, then the INT8 block rule on y.
+__global__ void __launch_bounds__(256) quantize_q_smooth_kernel(QuantQKArgs a, float* q_mean) {
+  __shared__ float redf[16][128];
+  __shared__ long long redl[8][128];
+  __shared__ float smu[128];
+  __shared__ float red8[8];
+  const int64_t h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
+  const int64_t Np = pad128(a.N), nb = Np / 128;
+  const int64_t nv = valid_tokens(a.lens, b, a.N, a.status);
+  const int64_t n0 = blk * 128;
+  const int cnt = nv - n0 <= 0 ? 0 : (nv - n0 >= 128 ? 128 : static_cast<int>(nv - n0));
+  const int64_t bh = b * a.H + h;
+  const int col = (threadIdx.x & 15) * 8;
+  const int rg = threadIdx.x >> 4;
+  uint4 raw[8];
+  uint4 m2 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int rr = rg + 16 * j;
+    raw[j] = rr < cnt ? ldg_v4(a.x + b * a.sb + (n0 + rr) * a.sn + h * a.sh + col)
+                      : make_uint4(0, 0, 0, 0);
+    m2.x = bf16x2_absmax(m2.x, raw[j].x);
+    m2.y = bf16x2_absmax(m2.y, raw[j].y);
+    m2.z = bf16x2_absmax(m2.z, raw[j].z);
+    m2.w = bf16x2_absmax(m2.w, raw[j].w);
+  }
+  {
+    float m[8];
+    unpack8(m2, m);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) redf[rg][col + q] = m[q];
+  }
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    float r = redf[0][threadIdx.x];
+#pragma unroll
+    for (int g = 1; g < 16; ++g) r = fmaxf(r, redf[g][threadIdx.x]);
+    smu[threadIdx.x] = r;  // the channel maximum, for now
+  }
+  __syncthreads();
+  // fixed-point channel sums of the valid rows
+  float2 c1[4], c2[4], hi[4], lo[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    k_term_scales(__float_as_int(smu[col + 2 * q]), c1[q].x, c2[q].x);
+    k_term_scales(__float_as_int(smu[col + 2 * q + 1]), c1[q].y, c2[q].y);
+    hi[q] = lo[q] = make_float2(0.0f, 0.0f);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (rg + 16 * j < cnt) k_fixed_terms8(raw[j], c1, c2, hi, lo);
+  long long acc[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = k_term_sum(hi[q].x, lo[q].x);
+    acc[2 * q + 1] = k_term_sum(hi[q].y, lo[q].y);
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], 16);
+  if ((threadIdx.x & 16) == 0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) redl[threadIdx.x >> 5][col + q] = acc[q];
+  }
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    long long S = 0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) S += redl[g][threadIdx.x];
+    const int ab = __float_as_int(smu[threadIdx.x]);
+    float mu = 0.0f;
+    if (cnt > 0 && ab != 0) {
+      const int E = k_grid_exp(ab);
+      const double grid = __longlong_as_double(static_cast<long long>(E - 40 + 1023) << 52);
+      mu = __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(S), grid), static_cast<double>(cnt)));
+    }
+    smu[threadIdx.x] = mu;
+    q_mean[(bh * nb + blk) * 128 + threadIdx.x] = mu;
+  }
+  __syncthreads();
+  float mu[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) mu[q] = smu[col + q];
+  float y[8][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float f[8];
+    unpack8(raw[j], f);
+    const bool valid = rg + 16 * j < cnt;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      y[j][q] = valid ? __fsub_rn(f[q], mu[q]) : 0.0f;
+      amax = fmaxf(amax, fabsf(y[j][q]));
+    }
+  }
+  amax = block_max_256(amax, red8);
+  const float sc = __fdiv_rn(amax, 127.0f);
+  const float inv = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+  if (threadIdx.x == 0) static_cast<float*>(a.scale)[bh * nb + blk] = sc;
+  __half* orow0 = static_cast<__half*>(a.out) + (bh * Np + n0 + rg) * 128 + col;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float dmax = 0.0f;
+    uint4 cw = int8_codes8f(y[j], inv, dmax);
+    if (!(dmax <= 0.5f - 0x1p-14f) && sc > 0.0f) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float c0 = fminf(fmaxf(round_rne(__fdiv_rn(y[j][2 * q], sc)), -127.0f), 127.0f);
+        const float c1v = fminf(fmaxf(round_rne(__fdiv_rn(y[j][2 * q + 1], sc)), -127.0f), 127.0f);
+        const __half2 h2 = __floats2half2_rn(c0, c1v);
+        w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      cw = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
+  }
+}
+
+// dS of Q smoothing: one CTA per (b * H + h, 128-key tile). The block means
+// go on the 16-bit grid 2^(E - 13) (E the exponent of the block's largest
+// |mean|): q_int = rne(q_mean 2^(13 - E)), |q_int| <= 2^14. Thread t holds
+// key j = t % 128's codes as packed bytes and takes the query blocks of
+// parity t / 128; sum_d q_int_d k8_jd is exact in int32 (two-way byte dot
+// products, |sum| < 2^28). dS = s_k 2^(E - 13) sum + q_grid . mu.
+__global__ void __launch_bounds__(256, 2) delta_s_kernel(DeltaSArgs a) {
+  __shared__ __align__(16) uint32_t sqi[32][64];  // q_int pairs of up to 32 query blocks
+  __shared__ float sgrid[32], scmu[32];
+  const int64_t bh = blockIdx.x, jt = blockIdx.y;
+  const int64_t nbq = pad128(a.Nq) / 128, Nkp = pad128(a.Nk), nbk = Nkp / 128;
+  const int key = static_cast<int>(threadIdx.x & 127), par = static_cast<int>(threadIdx.x >> 7);
+  const int64_t j = jt * 128 + key;
+  uint32_t kw[32];  // codes d = 4w .. 4w + 3 of key j, byte i = code 4w + i
+  {
+    const __half* row = a.k_q + (bh * Nkp + j) * 128;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + c * 8));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t b[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
+        b[2 * i] = static_cast<uint32_t>(__half2int_rn(__low2half(h2))) & 0xFFu;
+        b[2 * i + 1] = static_cast<uint32_t>(__half2int_rn(__high2half(h2))) & 0xFFu;
+      }
+      kw[2 * c] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+      kw[2 * c + 1] = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+    }
+  }
+  const float sk = __ldg(&a.k_scale[bh * nbk + jt]);
+  for (int64_t q0 = 0; q0 < nbq; q0 += 32) {
+    const int nq = nbq - q0 < 32 ? static_cast<int>(nbq - q0) : 32;
+    __syncthreads();  // the previous chunk has been read
+    // Warp w prepares blocks w, w + 8, ...: each lane takes channels 4 lane ..
+    // 4 lane + 3 (one 16-byte load), the block maximum and q_grid . mu by
+    // shuffle reductions.
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    for (int qi = static_cast<int>(threadIdx.x >> 5); qi < nq; qi += 8) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(a.q_mean + (bh * nbq + q0 + qi) * 128) + lane);
+      float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const int E = max((__float_as_int(amax) >> 23) & 0xFF, 1) - 127;
+      // 2^(13 - E) in two exact steps (2^(13 - E) alone overflows for E < -114)
+      const float c1 = E < 0 ? 0x1p64f : 1.0f;
+      const float c2 = exp2_int(E < 0 ? 13 - E - 64 : 13 - E);
+      const float grid = exp2_int(E - 13);
+      const int i0 = __float2int_rn(__fmul_rn(__fmul_rn(v.x, c1), c2));
+      const int i1 = __float2int_rn(__fmul_rn(__fmul_rn(v.y, c1), c2));
+      const int i2 = __float2int_rn(__fmul_rn(__fmul_rn(v.z, c1), c2));
+      const int i3 = __float2int_rn(__fmul_rn(__fmul_rn(v.w, c1), c2));
+      sqi[qi][2 * lane] = (static_cast<uint32_t>(i0) & 0xFFFFu) | (static_cast<uint32_t>(i1) << 16);
+      sqi[qi][2 * lane + 1] = (static_cast<uint32_t>(i2) & 0xFFFFu) | (static_cast<uint32_t>(i3) << 16);
+      float cmu = 0.0f;
+      if (a.k_mean) {
+        const float4 mu = __ldg(reinterpret_cast<const float4*>(a.k_mean + bh * 128) + lane);
+        cmu = fmaf(static_cast<float>(i0) * grid, mu.x, cmu);
+        cmu = fmaf(static_cast<float>(i1) * grid, mu.y, cmu);
+        cmu = fmaf(static_cast<float>(i2) * grid, mu.z, cmu);
+        cmu = fmaf(static_cast<float>(i3) * grid, mu.w, cmu);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cmu += __shfl_xor_sync(0xffffffffu, cmu, o);
+      }
+      if (lane == 0) {
+        sgrid[qi] = grid;
+        scmu[qi] = cmu;
+      }
+    }
+    __syncthreads();
+    for (int qi = par; qi < nq; qi += 2) {
+      int acc[4] = {0, 0, 0, 0};  // four independent chains (exact: each < 2^26)
+#pragma unroll
+      for (int w = 0; w < 32; w += 2) {
+        const uint4 qp = *reinterpret_cast<const uint4*>(&sqi[qi][2 * w]);  // q_int 4w .. 4w + 7
+        asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(acc[0]) : "r"(qp.x), "r"(kw[w]));
+        asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(acc[1]) : "r"(qp.y), "r"(kw[w]));
+        asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(acc[2]) : "r"(qp.z), "r"(kw[w + 1]));
+        asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(acc[3]) : "r"(qp.w), "r"(kw[w + 1]));
+      }
+      const int sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      a.out[(bh * nbq + q0 + qi) * Nkp + j] = fmaf(sk * sgrid[qi], static_cast<float>(sum), scmu[qi]);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
 // TMA-fed persistent variants. A grid of about two CTAs per SM walks the
 // 128-token blocks (head index fastest, so concurrent CTAs read contiguous
 // token rows); each block's 128 x 128 BF16 tile arrives by one 4-D TMA box
@@ -1282,6 +1491,19 @@ cudaError_t launch_quantize_qk_mxfp4(const QuantQKArgs& a, cudaStream_t s, bool 
     quantize_qk_mxfp4_kernel<true><<<grid, 256, 0, s>>>(a);
   else
     quantize_qk_mxfp4_kernel<false><<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q_smooth(const QuantQKArgs& q, float* q_mean, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(q.H), static_cast<unsigned>(pad128(q.N) / 128),
+            static_cast<unsigned>(q.B));
+  quantize_q_smooth_kernel<<<grid, 256, 0, s>>>(q, q_mean);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delta_s(const DeltaSArgs& a, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(a.B * a.H), static_cast<unsigned>(pad128(a.Nk) / 128));
+  delta_s_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

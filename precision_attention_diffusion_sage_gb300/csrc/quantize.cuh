@@ -1,6 +1,8 @@
 // Quantization launchers (defined in quantize.cu, called from sage_api.cu and
 // noalloc.cu): argument blocks, workspace sizes.
 #pragma once
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace sage {
@@ -39,6 +41,22 @@ cudaError_t launch_quantize_v_mxfp4(const QuantVArgs& a, cudaStream_t s);
 // V channel maxima share one persistent launch; then the V encode.
 cudaError_t launch_quantize_qkv(bool fp8, const QuantQKArgs& q, const QuantQKArgs& k,
                                 const QuantVArgs& v, cudaStream_t s);
+
+// Q smoothing (INT8): per 128-token block channel means (q_mean, float
+// [B][H][Npad/128][128]) subtracted before the INT8 block quantization.
+cudaError_t launch_quantize_q_smooth(const QuantQKArgs& q, float* q_mean, cudaStream_t s);
+
+// dS of Q smoothing: out[b][h][qb][j] = q_mean[b][h][qb] . (s_k k8_j + k_mean)
+// for every query block qb and padded key j.
+struct DeltaSArgs {
+  const __half* k_q;     // FP16-held INT8 K codes [B][H][Nk_pad][128]
+  const float* k_scale;  // [B][H][Nk_pad/128]
+  const float* k_mean;   // nullable [B][H][128]
+  const float* q_mean;   // [B][H][Nq_pad/128][128]
+  int64_t B, H, Nq, Nk;
+  float* out;            // [B][H][Nq_pad/128][Nk_pad]
+};
+cudaError_t launch_delta_s(const DeltaSArgs& a, cudaStream_t s);
 
 // K smoothing workspace: an int64 sum and a binary32 maximum per (b, h, channel).
 inline int64_t k_smooth_workspace_bytes(int64_t B, int64_t H) { return B * H * 128 * 12; }

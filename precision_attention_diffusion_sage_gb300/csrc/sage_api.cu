@@ -205,6 +205,40 @@ sage_status_t sage_quantize_qkv(sage_format_t fmt, const void* q, sage_strides_t
   return from_cuda(e);
 }
 
+sage_status_t sage_quantize_q_smooth(sage_format_t fmt, const void* q, sage_strides_t qs,
+                                     int64_t B, int64_t N, int64_t H, int64_t D, void* q_q,
+                                     void* q_scale, float* q_mean, sage_stream_t stream) {
+  if (fmt != SAGE_FMT_QK_INT8_V_FP8) return SAGE_ERR_UNSUPPORTED;
+  sage_status_t st = check_shape(B, N, H, D);
+  if (st != SAGE_OK) return st;
+  if (!q || !q_q || !q_scale || !q_mean || !aligned(q, 16) || !aligned(q_q, 16) ||
+      !aligned(q_scale, 4) || !aligned(q_mean, 16) || !strides_ok(qs))
+    return SAGE_ERR_INVALID_ARG;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != SAGE_OK) return st;
+  QuantQKArgs a{static_cast<const uint16_t*>(q), qs.b, qs.n, qs.h, B, N, H, nullptr, q_q, q_scale,
+                status};
+  return from_cuda(launch_quantize_q_smooth(a, q_mean, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sage_status_t sage_delta_s(sage_format_t fmt, const float* q_mean, const void* k_q,
+                           const void* k_scale, const float* k_mean, int64_t B, int64_t H,
+                           int64_t Nq, int64_t Nk, int64_t D, float* delta_s,
+                           sage_stream_t stream) {
+  if (fmt != SAGE_FMT_QK_INT8_V_FP8) return SAGE_ERR_UNSUPPORTED;
+  sage_status_t st = check_shape(B, Nq, H, D);
+  if (st != SAGE_OK) return st;
+  if ((st = check_shape(B, Nk, H, D)) != SAGE_OK) return st;
+  if (!q_mean || !k_q || !k_scale || !delta_s || !aligned(q_mean, 16) || !aligned(k_q, 16) ||
+      !aligned(k_scale, 4) || (k_mean && !aligned(k_mean, 4)) || !aligned(delta_s, 16))
+    return SAGE_ERR_INVALID_ARG;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != SAGE_OK) return st;
+  DeltaSArgs a{static_cast<const __half*>(k_q), static_cast<const float*>(k_scale), k_mean, q_mean,
+               B, H, Nq, Nk, delta_s};
+  return from_cuda(launch_delta_s(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 sage_status_t sage_quantize_k_smooth(sage_format_t fmt, const void* k, sage_strides_t ks,
                                      int64_t B, int64_t N, int64_t H, int64_t D,
                                      const int32_t* lens, void* k_q, void* k_scale,
@@ -261,9 +295,10 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
     return SAGE_ERR_INVALID_ARG;
   if (!(softmax_scale <= 0.0f) && !std::isfinite(softmax_scale)) return SAGE_ERR_INVALID_ARG;
   const float* k_mean = opts ? opts->k_mean : nullptr;
-  if (k_mean && (fmt != SAGE_FMT_QK_INT8_V_FP8 || !aligned(k_mean, 16))) {
-    return fmt != SAGE_FMT_QK_INT8_V_FP8 ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_INVALID_ARG;
-  }
+  const float* delta_s = opts ? opts->delta_s : nullptr;
+  if ((k_mean || delta_s) && fmt != SAGE_FMT_QK_INT8_V_FP8) return SAGE_ERR_UNSUPPORTED;
+  if ((k_mean && !aligned(k_mean, 16)) || (delta_s && !aligned(delta_s, 16)))
+    return SAGE_ERR_INVALID_ARG;
   const int req = opts ? opts->num_splits : 0;
   if (req < 0 || req > 64) return SAGE_ERR_INVALID_ARG;
   const int64_t splits = resolve_splits(req, B, H, Nq, Nk);
@@ -303,6 +338,7 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   p.osh = os.h;
   p.lse = lse;
   p.k_mean = k_mean;
+  p.delta_s = delta_s;
   p.num_splits = static_cast<int>(splits);
   p.o_part = splits > 1 ? static_cast<float*>(workspace) : nullptr;
   p.lse_part = splits > 1 ? static_cast<float*>(workspace) + splits * B * H * Nq * D : nullptr;

@@ -27,6 +27,7 @@ class Workload:
                                       # 4: MXFP4 Q/K, V and P
     structure: str = "plain"
     smooth_k: bool = False            # K smoothing (INT8 only): channel means removed from K
+    smooth_q: bool = False            # Q smoothing (INT8 only): block means removed, dS added
     k_lens: Optional[List[int]] = field(default=None)
     D: int = 128
 
@@ -64,6 +65,9 @@ WORKLOADS = {
                                   structure="k_mean", smooth_k=True),
     # MXFP4 Q/K with MXFP4 V and P (the FP4 P V format) on the 8K shape
     "mxfp4_v4_self": Workload("mxfp4_v4_self", 2, 24, 8192, 8192, seed=4, fmt=4),
+    # video DiT with Q and K smoothing (Q block means out, dS in the logits)
+    "video_dit_qksmooth": Workload("video_dit_qksmooth", 1, 40, 14040, 14040, seed=2,
+                                   structure="k_mean", smooth_k=True, smooth_q=True),
     # Hadamard-rotated MXFP4 Q/K on the 8K shape, with the outlier-channel K
     # structure the rotation is meant to spread
     "mxfp4h_self": Workload("mxfp4h_self", 2, 24, 8192, 8192, seed=4, fmt=3,

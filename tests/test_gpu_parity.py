@@ -717,3 +717,115 @@ def test_full_size_workload_v4():
     rows = _sample_rows(w.Nq)
     ro, rl = _oracle_attention(4, qz, kz, vz, w.Nq, w.Nk, rows=rows)
     assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+
+
+# ------------------------------------------------------------------ Q smoothing and dS (INT8)
+@pytest.mark.parametrize("B,N", [(1, 256), (1, 1), (1, 129), (2, 300)])
+def test_quantize_q_smooth_bitexact(B, N):
+    w = Workload("case", B, 2, N, N, seed=110 + N, structure="k_mean")
+    q, _, _ = make_qkv(w)
+    q = (q.float() + 3.0 * torch.randn(1, 1, 2, 128, generator=torch.Generator().manual_seed(N))
+         ).to(torch.bfloat16)
+    qq, qs, qm = binding.sage_quantize_q_smooth(q.cuda())
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    rq, rs, rm = oracle.quantize_int8_qsmooth(bf16_bits(q))
+    assert_qk_equal(0, qq, qs, rq, rs)
+    np.testing.assert_array_equal(qm.cpu().numpy().view(np.uint32), rm.view(np.uint32))
+
+
+def _ds_close(gpu, ref):
+    g = gpu.cpu().numpy().astype(np.float64)
+    scale = float(np.abs(ref).max()) + 1e-30
+    np.testing.assert_allclose(g, ref, rtol=2e-5, atol=2e-5 * scale)
+
+
+@pytest.mark.parametrize("smooth_k", [False, True])
+def test_delta_s_close_to_oracle(smooth_k):
+    w = Workload("case", 2, 2, 300, 1000, seed=111, structure="k_mean")
+    q, k, _ = (t.cuda() for t in make_qkv(w))
+    qq, qs, qm = binding.sage_quantize_q_smooth(q)
+    if smooth_k:
+        kq, ks, km = binding.sage_quantize_k_smooth(k)
+    else:
+        (kq, ks), km = binding.sage_quantize_qk(k, 0), None
+    ds = binding.sage_delta_s(qm, kq, ks, Nq=300, Nk=1000, k_mean=km)
+    torch.cuda.synchronize()
+    ref = oracle.delta_s(binding.int8_codes(kq).cpu().numpy(), ks.cpu().numpy(), qm.cpu().numpy(),
+                         Nq=300, Nk=1000, k_mean=None if km is None else km.cpu().numpy())
+    _ds_close(ds, ref)
+
+
+def _qsmooth_case(q, k, v, k_lens=None, num_splits=0, softmax_scale=None, smooth_k=False):
+    Nq, Nk = q.shape[1], k.shape[1]
+    qq, qs, qm = binding.sage_quantize_q_smooth(q)
+    if smooth_k:
+        kq, ks, km = binding.sage_quantize_k_smooth(k, lens=k_lens)
+    else:
+        (kq, ks), km = binding.sage_quantize_qk(k, 0, lens=k_lens), None
+    vq, vs = binding.sage_quantize_v(v, lens=k_lens)
+    ds = binding.sage_delta_s(qm, kq, ks, Nq=Nq, Nk=Nk, k_mean=km)
+    o, lse = binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
+                                   num_splits=num_splits, softmax_scale=softmax_scale, k_mean=km,
+                                   delta_s=ds)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    # oracle on its own quantization (bit-exact with the GPU's, checked above) and its FP64 dS
+    rq, rs, rm = oracle.quantize_int8_qsmooth(bf16_bits(q))
+    if smooth_k:
+        rk, rks, rmu = oracle.quantize_int8_smooth(bf16_bits(k), lens=k_lens)
+    else:
+        (rk, rks), rmu = oracle.quantize_int8(bf16_bits(k), lens=k_lens), None
+    rv = oracle.quantize_v_fp8(bf16_bits(v), lens=k_lens)
+    rds = oracle.delta_s(rk, rks, rm, Nq=Nq, Nk=Nk, k_mean=rmu)
+    return (o, lse), (rq, rs, rk, rks, rv, rds, rmu)
+
+
+@pytest.mark.parametrize("Nq,Nk,splits,smooth_k", [(256, 256, 0, False), (300, 333, 0, True),
+                                                   (129, 1000, 3, True), (513, 77, 0, False)])
+def test_attention_q_smooth(Nq, Nk, splits, smooth_k):
+    w = Workload("case", 1, 2, Nq, Nk, seed=Nq + 5 * Nk, structure="k_mean")
+    q, k, v = make_qkv(w)
+    q = (q.float() + 2.0 * torch.randn(1, 1, 2, 128, generator=torch.Generator().manual_seed(7))
+         ).to(torch.bfloat16)
+    (o, lse), (rq, rs, rk, rks, rv, rds, rmu) = _qsmooth_case(
+        q.cuda(), k.cuda(), v.cuda(), num_splits=splits, smooth_k=smooth_k)
+    ro, rl, _ = oracle.attention(0, rq, rs, rk, rks, *rv, Nq=Nq, Nk=Nk, delta_s=rds, k_mean=rmu)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_q_smooth_cross_ragged_and_scale():
+    w = Workload("case", 2, 2, 300, 512, seed=112, structure="k_mean")
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    lens = [512, 300]
+    (o, lse), (rq, rs, rk, rks, rv, rds, rmu) = _qsmooth_case(q, k, v, k_lens=lens,
+                                                               softmax_scale=0.2, smooth_k=True)
+    ro, rl, _ = oracle.attention(0, rq, rs, rk, rks, *rv, Nq=300, Nk=512, k_lens=lens,
+                                 softmax_scale=0.2, delta_s=rds, k_mean=rmu)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_full_size_video_q_and_k_smooth():
+    w = WORKLOADS["video_dit"]
+    q, k, v = make_qkv(w, device="cuda")
+    qq, qs, qm = binding.sage_quantize_q_smooth(q)
+    kq, ks, km = binding.sage_quantize_k_smooth(k)
+    vq, vs = binding.sage_quantize_v(v)
+    ds = binding.sage_delta_s(qm, kq, ks, Nq=w.Nq, Nk=w.Nk, k_mean=km)
+    o, lse = binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=w.Nq, Nk=w.Nk, k_mean=km,
+                                   delta_s=ds)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    hs = [0, 39]
+    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
+    rq, rs, rm = oracle.quantize_int8_qsmooth(bf16_bits(sub(q)))
+    rk, rks, rmu = oracle.quantize_int8_smooth(bf16_bits(sub(k)))
+    rv = oracle.quantize_v_fp8(bf16_bits(sub(v)))
+    assert_qk_equal(0, qq[:, hs], qs[:, hs], rq, rs)
+    np.testing.assert_array_equal(qm[:, hs].cpu().numpy().view(np.uint32), rm.view(np.uint32))
+    rds = oracle.delta_s(rk, rks, rm, Nq=w.Nq, Nk=w.Nk, k_mean=rmu)
+    _ds_close(ds[:, hs], rds)
+    rows = _sample_rows(w.Nq)
+    ro, rl, _ = oracle.attention(0, rq, rs, rk, rks, *rv, Nq=w.Nq, Nk=w.Nk, rows=rows,
+                                 delta_s=rds, k_mean=rmu)
+    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)

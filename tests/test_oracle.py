@@ -766,8 +766,9 @@ def test_qsmooth_zero_mean_reduces_to_plain_int8():
 @pytest.mark.parametrize("smooth_k", [False, True])
 def test_qsmooth_logits_identity(smooth_k):
     """With the dS correction the LSE is the logsumexp of softmax_scale *
-    (q^_s + q_mean) . (k^ + mu): the reconstructed Q against the dequantized
-    (and, with K smoothing, re-centred) K, in numpy from the quantized data."""
+    (q^_s + q_grid) . (k^ + mu): the reconstructed Q (block means on their
+    16-bit grid) against the dequantized (and, with K smoothing, re-centred)
+    K, in numpy from the quantized data."""
     w = Workload("qs", 1, 2, 300, 200, seed=23)
     q, k, v = make_qkv(w)
     g = torch.Generator().manual_seed(24)
@@ -781,7 +782,10 @@ def test_qsmooth_logits_identity(smooth_k):
     vz = oracle.quantize_v_fp8(bf16_bits(v))
     ds = oracle.delta_s(kq, ks, qm, Nq=300, Nk=200, k_mean=mu)
     o, lse, _ = oracle.attention(0, qq, qs, kq, ks, *vz, Nq=300, Nk=200, delta_s=ds, k_mean=mu)
-    qhat = _dequant_int8(qq, qs)[:, :, :300] + np.repeat(qm.astype(np.float64), 128, axis=2)[:, :, :300]
+    qg = oracle.q_grid(qm)
+    # the grid keeps the means within half a step of 2^(E-13): 2^-14 of the largest
+    assert np.all(np.abs(qg - qm) <= np.abs(qm).max(-1, keepdims=True) * 2.0 ** -14)
+    qhat = _dequant_int8(qq, qs)[:, :, :300] + np.repeat(qg, 128, axis=2)[:, :, :300]
     khat = _dequant_int8(kq, ks)[:, :, :200] + (0 if mu is None else mu.astype(np.float64)[:, :, None, :])
     z = (1 / math.sqrt(128)) * np.einsum("bhid,bhjd->bhij", qhat, khat)
     np.testing.assert_allclose(lse, scipy.special.logsumexp(z, axis=-1), rtol=0, atol=1e-9)
