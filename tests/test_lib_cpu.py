@@ -108,3 +108,43 @@ def test_status_strings():
     for code in range(-7, 1):
         assert lib.sage_status_string(code).decode().startswith("SAGE_")
     assert binding.sage_version().startswith("libsage")
+
+
+def test_new_entry_points_validate_before_launch():
+    """The quantize / dS entry points reject bad formats, shapes, pointers and
+    workspaces on the host, before any launch (no GPU is touched)."""
+    lib = binding.library()
+    S = binding.Strides(0, 0, 0)
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    # Q smoothing and dS: INT8 only, D = 128, aligned outputs
+    assert lib.sage_quantize_q_smooth(2, fake, S, 1, 128, 1, 128, fake, fake, fake, None) == -2
+    assert lib.sage_quantize_q_smooth(0, fake, S, 1, 128, 1, 64, fake, fake, fake, None) == -2
+    assert lib.sage_quantize_q_smooth(0, fake, S, 1, 128, 1, 128, fake, fake, odd, None) == -1
+    assert lib.sage_delta_s(1, fake, fake, fake, None, 1, 1, 128, 128, 128, fake, None) == -2
+    assert lib.sage_delta_s(0, fake, fake, fake, None, 1, 1, 0, 128, 128, fake, None) == -1
+    assert lib.sage_delta_s(0, fake, fake, fake, None, 1, 1, 128, 128, 128, odd, None) == -1
+    # MXFP4 V: D = 128 and aligned data
+    assert lib.sage_quantize_v_mxfp4(fake, S, 1, 128, 1, 64, None, fake, fake, None) == -2
+    assert lib.sage_quantize_v_mxfp4(odd, S, 1, 128, 1, 128, None, fake, fake, None) == -1
+    # one-call quantization: unknown format, empty K, missing FP8 workspace
+    assert lib.sage_quantize_qkv(9, fake, S, fake, S, fake, S, 1, 128, 128, 1, 128, None, fake,
+                                 fake, fake, fake, fake, fake, None, 0, None) == -2
+    assert lib.sage_quantize_qkv(0, fake, S, fake, S, fake, S, 1, 128, 0, 1, 128, None, fake,
+                                 fake, fake, fake, fake, fake, None, 0, None) == -1
+    assert lib.sage_quantize_qkv(0, fake, S, fake, S, fake, S, 1, 128, 128, 1, 128, None, fake,
+                                 fake, fake, fake, fake, fake, None, 0, None) == -3
+    # dS only goes with the INT8 format
+    opts = binding.AttnOptions(1, 0, None, 1 << 20)
+    assert lib.sage_attn_fwd(2, fake, fake, fake, fake, fake, fake, None, 1, 1, 128, 128, 128,
+                             -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None) == -2
+
+
+def test_format4_byte_counts():
+    B, N, H, D = 2, 300, 3, 128
+    Np = 384
+    assert binding.sage_quantized_bytes(4, 0, B, N, H, D) == B * H * Np * 64      # E2M1 Q/K
+    assert binding.sage_quantized_bytes(4, 1, B, N, H, D) == B * H * Np * 4       # E8M0 Q/K
+    assert binding.sage_quantized_bytes(4, 2, B, N, H, D) == B * H * D * Np // 2  # E2M1 V^T
+    assert binding.sage_quantized_bytes(4, 3, B, N, H, D) == B * H * Np * D // 32  # E8M0 V
+    assert binding.sage_workspace_bytes(1, 4, B, H, N, N) == 0                     # no V maxima
