@@ -48,6 +48,24 @@ _FP8_RATIO, _FP4_RATIO = 2.0, 6.0
 _EX2_PER_CLK_SM = 32
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself on one rank. Collective over the default process group."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(flops_per_rank: float, steps: int, ms_max: float, world: int) -> float:
+    """Whole-job TFLOP/s of `world` replicas that each ran `steps` steps of
+    `flops_per_rank` work, the slowest taking `ms_max` milliseconds in total."""
+    return world * flops_per_rank * steps / (ms_max * 1e-3) / 1e12
+
+
 def _roofline_peak(p16: float, fmt: int) -> float:
     """Tensor roofline of the attention: half the flops (Q K^T) on the 16-bit
     pipe (INT8 codes held as FP16), the FP4 pipe (MXFP4) or the FP8 pipe (FP8
@@ -445,12 +463,9 @@ def main():
     assert binding.sage_last_device_status() == 0
     total_ms = sum(t_quant) + sum(t_attn)
     eager_ms = (sum(t_quant_eager) + sum(t_attn_eager)) / args.steps
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     flops = w.flops
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = replica_throughput(flops, args.steps, total_ms, world)
     attn_ms = statistics.mean(t_attn)
     hbm, p16, peak_kind = _peaks()
     peak = _roofline_peak(p16, fmt)
@@ -487,13 +502,10 @@ def main():
         torch.cuda.synchronize()
         barrier()
         e_ms = sum(a.elapsed_time(b) for a, b in ee)
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-        e2e = {"value": world * flops * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": replica_throughput(flops, args.steps, e_ms, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.steps}
 
