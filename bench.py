@@ -536,7 +536,9 @@ def main():
     exp2_ms = exp2_count / (_EX2_PER_CLK_SM * 152 * mhz * 1e6) * 1e3
     nqt = 2 if Nqp >= 256 else 1
     kfmt = 1 if fmt == 3 else fmt   # the rotated MXFP4 format runs the MXFP4 kernel
-    kernel = f"sage_attn_kernel<{kfmt},{nqt},{(2 if nqt == 2 else 3) if kfmt == 0 else 4}>"
+    # Q smoothing runs the instance that adds dS to the logits (last template flag).
+    ds_flag = ",1" if w.smooth_q else ""
+    kernel = f"sage_attn_kernel<{kfmt},{nqt},{(2 if nqt == 2 else 3) if kfmt == 0 else 4}{ds_flag}>"
     fmt_names = {0: ("int8+fp8e4m3", "int8_qk_fp8_v"), 1: ("mxfp4+fp8e4m3", "mxfp4_qk_fp8_v"),
                  4: ("mxfp4", "mxfp4_qk_mxfp4_pv"),
                  2: ("fp8e4m3", "fp8_qk_fp8_v"),
