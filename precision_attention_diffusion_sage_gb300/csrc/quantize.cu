@@ -1155,11 +1155,12 @@ __global__ void __launch_bounds__(256, 2) quantize_qkv_tma_kernel(
 
 constexpr int kVStages = 2;
 
-// V encode, TMA-fed: thread t owns channels d = 2 (t % 64), d + 1 and tokens
-// 32 (t / 64) .. + 31 of the staged block. Its 4-byte shared loads (one token,
-// both channels) are conflict-free across a warp; each channel's 32 codes
-// (E4M3 of the binary32 quotient v / s_d, exact as in e4m3x2_fast) go out as
-// two 16-byte stores into that channel's token-contiguous row.
+// V encode, TMA-fed: thread t owns channels 8 (t % 16) .. + 7 and, in each
+// 64-token half of the staged block, tokens 4 (t / 16) .. + 3. It packs the
+// four tokens' codes of each channel (E4M3 of the binary32 quotient v / s_d,
+// exact as in e4m3x2_fast) into one word of a transposed block in shared
+// memory (128 channel rows, 33-word pitch against bank conflicts), which the
+// warps then store as 128-byte token-contiguous rows of V^T.
 __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
     const __grid_constant__ CUtensorMap tmV, QuantVArgs a) {
   constexpr int kPitchWords = 33;
