@@ -79,7 +79,7 @@ def _L():
         lib.oracle_fwht128.argtypes = [P, P, I64]
         lib.oracle_attention.restype = None
         lib.oracle_attention.argtypes = [I32, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, D,
-                                         P, I64, P, P, P, I32, P]
+                                         P, I64, P, P, P, I32, P, I32]
         lib.oracle_quantize_int8_qsmooth.restype = None
         lib.oracle_quantize_int8_qsmooth.argtypes = [P, I64, I64, I64, I64, I64, I64, I64, P, P, P,
                                                      P]
@@ -298,9 +298,14 @@ def quantize_mxfp4(x: np.ndarray, lens=None) -> Tuple[np.ndarray, np.ndarray]:
 # ------------------------------------------------------------------ attention
 def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: int = 128,
               softmax_scale: Optional[float] = None, k_lens=None, rows=None,
-              want_weights: bool = False, nthreads: int = 0, k_mean=None, delta_s=None):
+              want_weights: bool = False, nthreads: int = 0, k_mean=None, delta_s=None,
+              logits32: bool = False):
     """Quantized attention. fmt 0: INT8 Q/K; fmt 1: MXFP4 Q/K; fmt 2: E4M3 Q/K (V E4M3);
     fmt 4: MXFP4 Q/K with MXFP4 V (quantize_v_mxfp4) and MXFP4 P per 32 keys.
+
+    logits32 (fmt 0 only): form the logits in binary32, the precision in which
+    the INT8 format decides its FP8 P codes (see oracle_attention in
+    sage_oracle.h); the default forms them in binary64.
 
     delta_s (fmt 0 only): the Q smoothing correction of delta_s(), added to every
     logit of the rows of each 128-query block.
@@ -321,8 +326,9 @@ def attention(fmt: int, q, q_scale, k, k_scale, v8, sv, *, Nq: int, Nk: int, D: 
     ln = _lens(k_lens)
     ds = None if delta_s is None else np.ascontiguousarray(delta_s, dtype=np.float64)
     assert ds is None or fmt == 0, "Q smoothing is defined for the INT8 Q/K format"
+    assert not logits32 or fmt == 0, "binary32 logits are defined for the INT8 Q/K format"
     _L().oracle_attention(fmt, *(_ptr(a) for a in arrs), _ptr(ln), B, H, Nq, Nk, D, c, _ptr(r),
-                          nr, _ptr(o), _ptr(lse), _ptr(w), nthreads, _ptr(ds))
+                          nr, _ptr(o), _ptr(lse), _ptr(w), nthreads, _ptr(ds), int(logits32))
     if k_mean is not None:
         assert fmt == 0, "K smoothing is defined for the INT8 Q/K format"
         lse = lse + k_mean_lse_term(q, q_scale, k_mean, Nq=Nq, softmax_scale=c, rows=r)

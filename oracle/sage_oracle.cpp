@@ -570,9 +570,13 @@ void oracle_attention(int fmt, const void* q_data, const void* q_scale, const vo
                       const void* k_scale, const uint8_t* v8, const float* sv,
                       const int32_t* k_lens, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                       int64_t D, double softmax_scale, const int64_t* rows, int64_t nrows,
-                      double* o, double* lse, double* w, int nthreads, const double* delta_s) {
+                      double* o, double* lse, double* w, int nthreads, const double* delta_s,
+                      int logits32) {
   const int64_t Nqp = pad128(Nq), Nkp = pad128(Nk);
   if (!rows) nrows = Nq;
+  // The multiplier c log2(e) in binary32 (the logit precision of the INT8
+  // format when logits32 is set).
+  const float c_log2e_32 = static_cast<float>(softmax_scale * kLog2e);
   parallel_for(B * H * nrows, nthreads, [&](int64_t idx) {
     const int64_t r = idx % nrows, bh = idx / nrows, b = bh / H;
     const int64_t i = rows ? rows[r] : r;
@@ -596,8 +600,24 @@ void oracle_attention(int fmt, const void* q_data, const void* q_scale, const vo
         int64_t S = 0;  // exact integer dot product
         for (int64_t d = 0; d < D; ++d)
           S += static_cast<int64_t>(q[d]) * static_cast<int64_t>(k[j * D + d]);
-        t[j] = static_cast<double>(S) * sq * static_cast<double>(sk[j / 128]) * softmax_scale *
-               kLog2e;
+        if (!logits32) {
+          t[j] = static_cast<double>(S) * sq * static_cast<double>(sk[j / 128]) * softmax_scale *
+                 kLog2e;
+        } else if (!delta_s) {
+          // binary32: multiplier rn(rn(s_q c log2e) s_k), logit rn(S multiplier)
+          // (|S| < 2^24 and the product of two binary32 values is exact in
+          // binary64, so each cast rounds once)
+          const float alpha = (static_cast<float>(sq) * c_log2e_32) * sk[j / 128];
+          t[j] = static_cast<double>(static_cast<float>(static_cast<double>(S) * alpha));
+        } else {
+          // binary32 with Q smoothing: s = rn(S rn(s_q s_k) + rn(dS)) (one
+          // fused rounding), logit rn(s c log2e)
+          const float beta = static_cast<float>(sq) * sk[j / 128];
+          const float ds32 =
+              static_cast<float>(delta_s[(bh * (Nqp / 128) + i / 128) * Nkp + j]);
+          const float s32 = std::fmaf(static_cast<float>(S), beta, ds32);
+          t[j] = static_cast<double>(static_cast<float>(static_cast<double>(s32) * c_log2e_32));
+        }
       }
     } else if (fmt == 2) {
       const uint8_t* q = static_cast<const uint8_t*>(q_data) + (bh * Nqp + i) * D;
@@ -628,7 +648,7 @@ void oracle_attention(int fmt, const void* q_data, const void* q_scale, const vo
         t[j] = S * softmax_scale * kLog2e;
       }
     }
-    if (delta_s)  // Q smoothing: the block's correction dS_j, in log2 units
+    if (delta_s && !(logits32 && fmt == 0))  // Q smoothing: dS_j, in log2 units
       for (int64_t j = 0; j < nk; ++j)
         t[j] += delta_s[(bh * (Nqp / 128) + i / 128) * Nkp + j] * softmax_scale * kLog2e;
     double tmax = -INFINITY;

@@ -121,12 +121,18 @@ void oracle_quantize_v_mxfp4(const uint16_t* v, int64_t sb, int64_t sn, int64_t 
  *   w (nullable): double [B][H][nrows][Nk] effective weights dq(P8)/256/l
  *   (0 for masked keys).
  * delta_s (nullable, fmt 0): the Q smoothing correction of oracle_delta_s,
- *   added to every logit as softmax_scale * dS[b][h][i / 128][j]. */
+ *   added to every logit as softmax_scale * dS[b][h][i / 128][j].
+ * logits32 (fmt 0 only; 0 elsewhere): form the logits in binary32, the
+ *   precision in which the INT8 format decides its FP8 P codes: multiplier
+ *   rn(rn(s_q rn(c log2e)) s_k) and logit rn(S multiplier); with delta_s,
+ *   s = rn(S rn(s_q s_k) + rn(dS)) in one fused rounding and logit
+ *   rn(s rn(c log2e)). Everything after the logits stays binary64. */
 void oracle_attention(int fmt, const void* q_data, const void* q_scale, const void* k_data,
                       const void* k_scale, const uint8_t* v8, const float* sv,
                       const int32_t* k_lens, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                       int64_t D, double softmax_scale, const int64_t* rows, int64_t nrows,
-                      double* o, double* lse, double* w, int nthreads, const double* delta_s);
+                      double* o, double* lse, double* w, int nthreads, const double* delta_s,
+                      int logits32);
 
 /* Unquantized FP64 softmax attention on the BF16 inputs ([B][N][H][D] with
  * strides), for accuracy reporting and self-tests. Same output layout. */

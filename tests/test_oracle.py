@@ -795,3 +795,67 @@ def test_qsmooth_logits_identity(smooth_k):
                                 Nk=200, k_mean=mu)
     err = lambda a: float(np.abs(a - oe).max())  # noqa: E731
     assert err(o) < err(o0)
+
+
+# ------------------------------------------------------------------ binary32 logits (INT8)
+def _int8_case(seed, pow2_scales):
+    """Quantized INT8 operands built directly: random codes, scales either
+    powers of two (so binary32 logits are exact) or general binary32 values."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 1, 2, 256, 128
+    q = rng.integers(-127, 128, (B, H, N, D), dtype=np.int8)
+    k = rng.integers(-127, 128, (B, H, N, D), dtype=np.int8)
+    if pow2_scales:
+        qs = (2.0 ** rng.integers(-12, -6, (B, H, 2))).astype(np.float32)
+        ks = (2.0 ** rng.integers(-12, -6, (B, H, 2))).astype(np.float32)
+    else:
+        qs = rng.uniform(0.004, 0.03, (B, H, 2)).astype(np.float32)
+        ks = rng.uniform(0.004, 0.03, (B, H, 2)).astype(np.float32)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    v8 = rng.choice(codes, (B, H, D, N)).astype(np.uint8)
+    sv = rng.uniform(0.001, 0.01, (B, H, D)).astype(np.float32)
+    return q, qs, k, ks, v8, sv
+
+
+def test_logits32_equals_binary64_where_binary32_is_exact():
+    """With power-of-two scales and c log2(e) = 1/8 the binary32 logits are the
+    exact ones, so both modes agree (to the 1e-16 of the binary64 constant):
+    the binary32 path forms the same logit, with and without dS."""
+    q, qs, k, ks, v8, sv = _int8_case(1, True)
+    c = 0.125 / L2E
+    o64, l64, w64 = oracle.attention(0, q, qs, k, ks, v8, sv, Nq=256, Nk=256, softmax_scale=c,
+                                     want_weights=True)
+    o32, l32, w32 = oracle.attention(0, q, qs, k, ks, v8, sv, Nq=256, Nk=256, softmax_scale=c,
+                                     want_weights=True, logits32=True)
+    np.testing.assert_allclose(o32, o64, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l32, l64, rtol=1e-12)
+    np.testing.assert_array_equal(w32 > 0, w64 > 0)
+    np.testing.assert_allclose(w32, w64, rtol=1e-12)
+    # with dS: codes within +-7 and scales 2^-4 keep S s_q s_k on the 2^-8 grid
+    # below 2^5, and dS (multiples of 2^-8 below 8) keeps the sum exact in binary32
+    rng = np.random.default_rng(2)
+    q7 = rng.integers(-7, 8, q.shape, dtype=np.int8)
+    k7 = rng.integers(-7, 8, k.shape, dtype=np.int8)
+    s16 = np.full(qs.shape, 2.0 ** -4, np.float32)
+    ds = (rng.integers(-2048, 2048, (1, 2, 2, 256)) / 256.0).astype(np.float64)
+    o64, l64, _ = oracle.attention(0, q7, s16, k7, s16, v8, sv, Nq=256, Nk=256, softmax_scale=c,
+                                   delta_s=ds)
+    o32, l32, _ = oracle.attention(0, q7, s16, k7, s16, v8, sv, Nq=256, Nk=256, softmax_scale=c,
+                                   delta_s=ds, logits32=True)
+    np.testing.assert_allclose(o32, o64, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l32, l64, rtol=1e-12)
+
+
+def test_logits32_within_binary32_rounding_of_binary64():
+    """General scales: the binary32 logits differ from the binary64 ones by
+    rounding only, so the LSE moves by ~1e-7 and O by the rare E4M3 code that
+    crosses a boundary (the rows stay cosine-close)."""
+    q, qs, k, ks, v8, sv = _int8_case(3, False)
+    for ds in (None, np.random.default_rng(4).normal(0, 2, (1, 2, 2, 256))):
+        o64, l64, _ = oracle.attention(0, q, qs, k, ks, v8, sv, Nq=256, Nk=256, delta_s=ds)
+        o32, l32, _ = oracle.attention(0, q, qs, k, ks, v8, sv, Nq=256, Nk=256, delta_s=ds,
+                                       logits32=True)
+        assert np.abs(l32 - l64).max() < 1e-5
+        cos = float((o32 * o64).sum() / np.sqrt((o32 * o32).sum() * (o64 * o64).sum()))
+        assert cos > 0.99999
+        assert not np.array_equal(l32, l64)  # the modes do differ
