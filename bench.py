@@ -2,10 +2,13 @@
 """Benchmark: effective attention TFLOPS on GB300 with quantization included.
 
 One step = the whole hot path on one batch of seeded synthetic input already
-resident in HBM: quantize Q (INT8), quantize K (INT8), quantize V (FP8 E4M3,
-two launches), attention forward (BF16 O + FP32 LSE). Effective TFLOPS =
-4*B*H*Nq*Nk*D / (summed step time). L2 is flushed between steps (a 256 MiB
-write outside the timed events). Prints one JSON line on rank 0.
+resident in HBM: one sage_quantize_qkv call (Q and K to INT8 codes with their
+block scales, V's channel maxima, then the V encode to FP8 E4M3; with K or Q
+smoothing the separate quantize calls it needs) and one attention call (BF16 O
++ FP32 LSE), each replayed from a CUDA graph. Effective TFLOPS =
+4*B*H*Nq*Nk*D / (summed step time). Between steps, outside the timed events,
+L2 is flushed by reading a 256 MiB buffer. The default workload is the
+65520-token long-video self-attention. Prints one JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -29,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "effective attention TFLOPS at 1 GB300 (incl. quant) and % of dense INT8/FP8 peak"
-DEFAULT_WORKLOAD = "image_dit"
+DEFAULT_WORKLOAD = "long_video"
 
 
 def _peaks():
@@ -46,6 +49,21 @@ _FP8_RATIO, _FP4_RATIO = 2.0, 6.0
 # Hardware exp2 (MUFU) throughput per SM per clock, measured on GB300 with a
 # microbenchmark of back-to-back ex2.approx.ftz.f32.
 _EX2_PER_CLK_SM = 32
+# Dense tcgen05 MMA throughput per SM per clock measured on GB300 with
+# microbenchmarks (M128, N >= 128, operands in shared memory): kind::f16,
+# kind::f8f6f4 (E4M3) and kind::mxf4.block_scale.
+_MMA_FLOP_PER_CLK_SM = {"f16": 8192.0, "f8": 16384.0, "f4": 32768.0}
+_SMS = 152
+
+
+def _clock_peak(fmt: int, mhz: float) -> float:
+    """The attention's tensor roofline (TFLOP/s) rebuilt from the measured
+    per-clock MMA rates at SM clock `mhz`: Q K^T on the f16 (INT8 codes), f4
+    (MXFP4) or f8 (FP8) kind, P V on f8 (f4 for MXFP4 P V), harmonic."""
+    r = _MMA_FLOP_PER_CLK_SM
+    qk = {0: r["f16"], 1: r["f4"], 2: r["f8"], 3: r["f4"], 4: r["f4"]}[fmt]
+    pv = r["f4"] if fmt == 4 else r["f8"]
+    return 2.0 / (1.0 / qk + 1.0 / pv) * _SMS * mhz * 1e6 / 1e12
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -184,16 +202,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _cpu_oracle_sample(w, seconds: float, seed_rows: int = 64, nthreads: int = 0):
-    """Time the CPU oracle (as it stands) on a bounded sample of workload w:
-    quantization of the first `nh` heads' Q/K/V plus attention for `n` query
-    rows of those heads, sized from a short calibration run to take about
-    `seconds`. Returns (flops, time_s, description, rows)."""
+def _cpu_oracle_sample(w, seconds: float, qkv, seed_rows: int = 64, nthreads: int = 0):
+    """Time the CPU oracle (as it stands) on a bounded sample of workload w
+    (host tensors `qkv`): quantization of the first `nh` heads' Q/K/V plus
+    attention for `n` query rows of those heads, sized from a short
+    calibration run to take about `seconds`. Returns (flops, time_s,
+    description, rows)."""
     import numpy as np
     import oracle
-    from precision_attention_diffusion_sage_gb300.inputs import bf16_bits, make_qkv
+    from precision_attention_diffusion_sage_gb300.inputs import bf16_bits
 
-    q, k, v = make_qkv(w)
+    q, k, v = qkv
     lens = None if w.k_lens is None else w.k_lens
 
     def run(nh, rows):
@@ -242,12 +261,14 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    from precision_attention_diffusion_sage_gb300.inputs import make_qkv
     cores = os.cpu_count()
     budget = 150.0 / max(1, args.steps + args.warmup)
     times, flops = [], 0.0
     desc, n = "", 0
+    qkv = make_qkv(w)
     for i in range(args.warmup + args.steps):
-        f, dt, desc, n = _cpu_oracle_sample(w, budget)
+        f, dt, desc, n = _cpu_oracle_sample(w, budget, qkv)
         if i >= args.warmup:
             times.append(dt)
             flops = f
@@ -511,8 +532,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f, dt, desc, n = _cpu_oracle_sample(w, args.cpu_seconds)
-        f1, dt1, desc1, _ = _cpu_oracle_sample(w, args.cpu_seconds / 3, nthreads=1)
+        host = tuple(t.cpu() for t in (q, k, v))
+        f, dt, desc, n = _cpu_oracle_sample(w, args.cpu_seconds, host)
+        f1, dt1, desc1, _ = _cpu_oracle_sample(w, args.cpu_seconds / 3, host, nthreads=1)
+        del host
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                "kind": "oracle", "sample": desc, "seconds": dt,
                "value_1core": f1 / dt1 / 1e12, "sample_1core": desc1, "seconds_1core": dt1}
@@ -579,7 +602,12 @@ def main():
                                     f"{ {0: 'fp16 x1', 1: 'fp4 x6', 2: 'fp8 x2', 3: 'fp4 x6', 4: 'fp4 x6'}[fmt] }, "
                                     f"P V { 'fp4 x6' if fmt == 4 else 'fp8 x2' }, "
                                     f"harmonic combination"),
-                     "kernel": kernel},
+                     "kernel": kernel,
+                     "peak_at_sampled_clock": _clock_peak(fmt, mhz),
+                     "frac_at_sampled_clock": achieved / _clock_peak(fmt, mhz),
+                     "sampled_clock_basis": (f"measured tcgen05 FLOP/clk/SM (f16 8192, f8 16384, "
+                                             f"f4 32768) x {_SMS} SMs x median SM clock {mhz} MHz "
+                                             f"sampled during the timed region; informational")},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk, "wall_s": wall,
     }

@@ -180,7 +180,9 @@ sage_status_t sage_quantize_v(const void* v, sage_strides_t vs, int64_t B, int64
  *     (any N); larger calls return SAGE_ERR_WORKSPACE and launch nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is cached for the life of the
+ *     process: resetting the device (cudaDeviceReset) after that first call
+ *     is not supported, since the array may move when the module reloads.
  *   - All calls on a device share the one array and it keeps the previous
  *     call's contents; each call clears the part it uses (on its stream)
  *     before using it. Calls that overlap on the GPU (other streams, other

@@ -212,9 +212,9 @@ void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
                           int64_t N, int64_t H, int64_t D, const int32_t* lens, int8_t* q,
                           float* scale) {
   const int64_t Np = pad128(N), nb = Np / 128;
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h) {
       for (int64_t blk = 0; blk < nb; ++blk) {
         const int64_t n0 = blk * 128, n1 = std::min(n0 + 128, nv);
         float amax = 0.0f;
@@ -231,8 +231,7 @@ void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
             q[((b * H + h) * Np + n) * D + d] = static_cast<int8_t>(v);
           }
       }
-    }
-  }
+  });
 }
 
 // K smoothing: the per-(b,h,channel) mean of K over the valid tokens.
@@ -247,12 +246,12 @@ void oracle_quantize_int8(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh,
 // infinity makes the library's mean unspecified).
 void oracle_k_mean(const uint16_t* k, int64_t sb, int64_t sn, int64_t sh, int64_t B, int64_t N,
                    int64_t H, int64_t D, const int32_t* lens, float* mu) {
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h)
       for (int64_t d = 0; d < D; ++d)
         mu[(b * H + h) * D + d] = exact_mean(k + b * sb + h * sh + d, sn, nv);
-  }
+  });
 }
 
 // INT8 quantization of smoothed K: y = (float)k - mu[b,h,d] in binary32, then
@@ -261,9 +260,9 @@ void oracle_quantize_int8_smooth(const uint16_t* x, int64_t sb, int64_t sn, int6
                                  int64_t B, int64_t N, int64_t H, int64_t D, const int32_t* lens,
                                  const float* mu, int8_t* q, float* scale) {
   const int64_t Np = pad128(N), nb = Np / 128;
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h) {
       const float* m = mu + (b * H + h) * D;
       for (int64_t blk = 0; blk < nb; ++blk) {
         const int64_t n0 = blk * 128, n1 = std::min(n0 + 128, nv);
@@ -282,8 +281,7 @@ void oracle_quantize_int8_smooth(const uint16_t* x, int64_t sb, int64_t sn, int6
             q[((b * H + h) * Np + n) * D + d] = static_cast<int8_t>(v);
           }
       }
-    }
-  }
+  });
 }
 
 // The logit term that K smoothing removes, per query row: softmax_scale *
@@ -313,9 +311,9 @@ void oracle_quantize_int8_qsmooth(const uint16_t* x, int64_t sb, int64_t sn, int
                                   int64_t B, int64_t N, int64_t H, int64_t D,
                                   const int32_t* lens, int8_t* q, float* scale, float* q_mean) {
   const int64_t Np = pad128(N), nb = Np / 128;
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h)
       for (int64_t blk = 0; blk < nb; ++blk) {
         const int64_t n0 = blk * 128, n1 = std::min(n0 + 128, nv);
         float* m = q_mean + ((b * H + h) * nb + blk) * D;
@@ -336,7 +334,7 @@ void oracle_quantize_int8_qsmooth(const uint16_t* x, int64_t sb, int64_t sn, int
             q[((b * H + h) * Np + n) * D + d] = static_cast<int8_t>(v);
           }
       }
-  }
+  });
 }
 
 // The logit correction of Q smoothing ("_compute_delta_s_kernel" on the same
@@ -354,8 +352,8 @@ void oracle_delta_s(const int8_t* k8, const float* k_scale, const float* k_mean,
                     const float* q_mean, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
                     double* out) {
   const int64_t nbq = pad128(Nq) / 128, Nkp = pad128(Nk), nbk = Nkp / 128;
-  std::vector<int64_t> qi(D);
-  for (int64_t bh = 0; bh < B * H; ++bh)
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    std::vector<int64_t> qi(D);
     for (int64_t qb = 0; qb < nbq; ++qb) {
       const float* qm = q_mean + (bh * nbq + qb) * D;
       float amax = 0.0f;
@@ -376,6 +374,7 @@ void oracle_delta_s(const int8_t* k8, const float* k_scale, const float* k_mean,
             static_cast<double>(k_scale[bh * nbk + j / 128]) * std::ldexp(static_cast<double>(S), E - 13) + cmu;
       }
     }
+  });
 }
 
 void oracle_fwht128(const float* in, float* out, int64_t rows) {
@@ -397,9 +396,9 @@ void oracle_quantize_mxfp4_hadamard(const uint16_t* x, int64_t sb, int64_t sn, i
                                     int64_t B, int64_t N, int64_t H, int64_t D,
                                     const int32_t* lens, uint8_t* codes, uint8_t* e8m0) {
   const int64_t Np = pad128(N), G = D / 32;
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h)
       for (int64_t n = 0; n < Np; ++n) {
         uint8_t* crow = codes + ((b * H + h) * Np + n) * (D / 2);
         uint8_t* srow = e8m0 + ((b * H + h) * Np + n) * G;
@@ -429,16 +428,16 @@ void oracle_quantize_mxfp4_hadamard(const uint16_t* x, int64_t sb, int64_t sn, i
           }
         }
       }
-  }
+  });
 }
 
 void oracle_quantize_fp8_qk(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh, int64_t B,
                             int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* q,
                             float* scale) {
   const int64_t Np = pad128(N), nb = Np / 128;
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h)
       for (int64_t blk = 0; blk < nb; ++blk) {
         const int64_t n0 = blk * 128, n1 = std::min(n0 + 128, nv);
         float amax = 0.0f;
@@ -457,42 +456,44 @@ void oracle_quantize_fp8_qk(const uint16_t* x, int64_t sb, int64_t sn, int64_t s
             q[((b * H + h) * Np + n) * D + d] = c;
           }
       }
-  }
+  });
 }
 
 void oracle_quantize_v_fp8(const uint16_t* v, int64_t sb, int64_t sn, int64_t sh, int64_t B,
                            int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* v8,
                            float* sv) {
   const int64_t Np = pad128(N);
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h)
+    const uint16_t* vb = v + b * sb + h * sh;
+    std::vector<float> s(D, 0.0f);  // channel maxima over the valid tokens, then scales
+    for (int64_t n = 0; n < nv; ++n)
+      for (int64_t d = 0; d < D; ++d) s[d] = std::max(s[d], std::fabs(bf16_to_float(vb[n * sn + d])));
+    for (int64_t d = 0; d < D; ++d) {
+      s[d] = s[d] / 448.0f;
+      sv[bh * D + d] = s[d];
+    }
+    uint8_t* out = v8 + bh * D * Np;  // [D][Np]
+    for (int64_t n = 0; n < Np; ++n)
       for (int64_t d = 0; d < D; ++d) {
-        float amax = 0.0f;
-        for (int64_t n = 0; n < nv; ++n)
-          amax = std::max(amax, std::fabs(bf16_to_float(v[b * sb + n * sn + h * sh + d])));
-        const float s = amax / 448.0f;
-        sv[(b * H + h) * D + d] = s;
-        uint8_t* row = v8 + ((b * H + h) * D + d) * Np;
-        for (int64_t n = 0; n < Np; ++n) {
-          uint8_t c = 0;
-          if (n < nv && s > 0.0f) {
-            const float r = bf16_to_float(v[b * sb + n * sn + h * sh + d]) / s;  // binary32
-            c = oracle_e4m3_encode(static_cast<double>(r));
-          }
-          row[n] = c;
+        uint8_t c = 0;
+        if (n < nv && s[d] > 0.0f) {
+          const float r = bf16_to_float(vb[n * sn + d]) / s[d];  // binary32
+          c = oracle_e4m3_encode(static_cast<double>(r));
         }
+        out[d * Np + n] = c;
       }
-  }
+  });
 }
 
 void oracle_quantize_mxfp4(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh, int64_t B,
                            int64_t N, int64_t H, int64_t D, const int32_t* lens, uint8_t* codes,
                            uint8_t* e8m0) {
   const int64_t Np = pad128(N), G = D / 32;
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h)
       for (int64_t n = 0; n < Np; ++n) {
         uint8_t* crow = codes + ((b * H + h) * Np + n) * (D / 2);
         uint8_t* srow = e8m0 + ((b * H + h) * Np + n) * G;
@@ -522,7 +523,7 @@ void oracle_quantize_mxfp4(const uint16_t* x, int64_t sb, int64_t sn, int64_t sh
           }
         }
       }
-  }
+  });
 }
 
 // MXFP4 V along tokens (the sage_quant_v_mxfp4_colmajor preprocessing named on
@@ -536,9 +537,9 @@ void oracle_quantize_v_mxfp4(const uint16_t* v, int64_t sb, int64_t sn, int64_t 
                              int64_t N, int64_t H, int64_t D, const int32_t* lens,
                              uint8_t* codes, uint8_t* e8m0) {
   const int64_t Np = pad128(N), nb = Np / 128;
-  for (int64_t b = 0; b < B; ++b) {
+  parallel_for(B * H, 0, [&](int64_t bh) {
+    const int64_t b = bh / H, h = bh % H;
     const int64_t nv = valid_len(lens, b, N);
-    for (int64_t h = 0; h < H; ++h)
       for (int64_t d = 0; d < D; ++d)
         for (int64_t blk = 0; blk < Np / 32; ++blk) {
           float amax = 0.0f;
@@ -562,7 +563,7 @@ void oracle_quantize_v_mxfp4(const uint16_t* v, int64_t sb, int64_t sn, int64_t 
             crow[n / 2] = static_cast<uint8_t>(c[0] | (c[1] << 4));
           }
         }
-  }
+  });
 }
 
 // ---------------------------------------------------------------- attention

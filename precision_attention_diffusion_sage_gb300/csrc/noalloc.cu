@@ -34,19 +34,21 @@ constexpr int kMaxNoAllocDevices = 64;
 float* g_noalloc_ptr[kMaxNoAllocDevices] = {};
 std::mutex g_noalloc_mu;
 
-// Device address of the scratch array for the current device (looked up
-// once per device).
+// Device address of the scratch array for the current device, looked up
+// (after an architecture check, so that a device the library has no code
+// for reports SAGE_ERR_ARCH) on the first call on that device and cached for
+// the life of the process.
 sage_status_t noalloc_scratch(float** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxNoAllocDevices)
     return SAGE_ERR_CUDA;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return SAGE_ERR_CUDA;
-  if (major != 10 || minor != 3) return SAGE_ERR_ARCH;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SAGE_ERR_CUDA;
+    if (major != 10 || minor != 3) return SAGE_ERR_ARCH;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SAGE_ERR_CUDA;
     g_noalloc_ptr[dev] = static_cast<float*>(p);

@@ -18,6 +18,17 @@ def test_roofline_peaks_per_format():
     assert bench._roofline_peak(p16, 4) == pytest.approx(11469.0)          # both halves FP4
 
 
+def test_clock_peak_from_measured_mma_rates():
+    """The informational peak at the sampled clock: measured FLOP/clk/SM of
+    each MMA kind (f16 8192, f8 16384, f4 32768) x 152 SMs x MHz, halves
+    combined harmonically; INT8 at 2070 MHz is 10922.7 x 152 x 2.07e9."""
+    assert bench._clock_peak(0, 2070) == pytest.approx(2 / (1 / 8192 + 1 / 16384) * 152 * 2.07e-3)
+    assert bench._clock_peak(0, 2070) == pytest.approx(3436.71, abs=0.01)
+    assert bench._clock_peak(2, 2070) == pytest.approx(16384 * 152 * 2.07e-3)
+    assert bench._clock_peak(4, 1000) == pytest.approx(32768 * 152 * 1e-3)
+    assert bench._clock_peak(0, 1035) == pytest.approx(bench._clock_peak(0, 2070) / 2)
+
+
 def test_quant_bytes_by_element_count():
     """Bytes per input element, from what each pass reads and writes: INT8
     Q and K read 2 and write 2 (FP16-held codes), V read twice (maxima, then

@@ -16,8 +16,9 @@ import torch
 import oracle
 from precision_attention_diffusion_sage_gb300.inputs import WORKLOADS, Workload, bf16_bits, make_qkv
 
-from _helpers import (assert_attention_close, assert_qk_equal, assert_v_equal, gpu_codes,
-                      oracle_attention_format, oracle_quantize)
+from _helpers import (LSE_MAX_ABS, O_MAX_ABS, O_MIN_COS, assert_attention_close, assert_qk_equal,
+                      assert_v_equal, compare_attention, gpu_codes, oracle_attention_format,
+                      oracle_quantize)
 
 pytestmark = pytest.mark.gpu
 
@@ -239,27 +240,71 @@ def test_device_status_reports_bad_k_lens():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _sample_rows(Nq):
-    rows = sorted(set([0, 1, 127, 128, Nq // 3, Nq // 2 + 5, Nq - 129, Nq - 2, Nq - 1]))
-    return [r for r in rows if 0 <= r < Nq]
+# Every full-size test compares the quantized tensors and scales of every
+# batch and head bit for bit, and attention on one query row of every 128-row
+# tile of the sampled heads (so every CTA of those heads' grid is compared),
+# the row's lane moving from tile to tile. Each row is exact to compute on its
+# own, so sampled parity is parity for those rows.
+def _tile_rows(Nq, salt=0):
+    """One row of every 128-row query tile (lane (37 t + salt) mod the tile's
+    length) plus the first and last rows."""
+    rows = {0, Nq - 1}
+    for t in range((Nq + 127) // 128):
+        span = min(128, Nq - t * 128)
+        rows.add(t * 128 + (37 * t + salt) % span)
+    return sorted(rows)
 
 
-@pytest.mark.parametrize("name,heads", [("image_dit", None), ("video_dit", [0, 17, 39]),
-                                        ("long_video", [0, 39]), ("cross", None),
-                                        ("cross_ragged", None)])
-def test_full_size_workload(name, heads):
+def _heads(arrays, hs):
+    """Head subset (axis 1) of the oracle's quantized arrays, contiguous."""
+    return tuple(np.ascontiguousarray(a[:, hs]) for a in arrays)
+
+
+def _assert_quantized_equal(fmt, gpu, ref):
+    (qq, qs), (kq, ks), (vq, vs) = gpu
+    qz, kz, vz = ref
+    assert_qk_equal(fmt, qq, qs, *qz)
+    assert_qk_equal(fmt, kq, ks, *kz)
+    assert_v_equal(vq, vs, *vz)
+
+
+def _full_size(fmt, name, heads, salt=0):
+    """Runs workload `name` in format `fmt`: all quantized tensors against
+    the oracle, attention on every query tile of `heads`."""
     w = WORKLOADS[name]
     q, k, v = make_qkv(w, device="cuda")
-    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(0, q, k, v, k_lens=w.k_lens)
-    hs = list(range(w.H)) if heads is None else heads
-    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
-    qz, kz, vz = oracle_quantize(0, sub(q), sub(k), sub(v), k_lens=w.k_lens)
-    assert_qk_equal(0, qq[:, hs], qs[:, hs], *qz)
-    assert_qk_equal(0, kq[:, hs], ks[:, hs], *kz)
-    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
-    rows = _sample_rows(w.Nq)
-    ro, rl = _oracle_attention(0, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
-    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+    qz_, kz_, vz_, o, lse = _run_gpu(fmt, q, k, v, k_lens=w.k_lens)
+    ref = oracle_quantize(fmt, q, k, v, k_lens=w.k_lens)
+    _assert_quantized_equal(fmt, (qz_, kz_, vz_), ref)
+    del qz_, kz_, vz_
+    rows = _tile_rows(w.Nq, salt)
+    ro, rl = _oracle_attention(fmt, *(_heads(z, heads) for z in ref), w.Nq, w.Nk,
+                               k_lens=w.k_lens, rows=rows)
+    assert_attention_close(o[:, :, heads], lse[:, heads], ro, rl, rows=rows)
+
+
+@pytest.mark.parametrize("name,heads", [("image_dit", [0, 11, 23]), ("video_dit", [0, 17, 39]),
+                                        ("long_video", [0, 39]), ("cross", [0, 23]),
+                                        ("cross_ragged", [0, 23])])
+def test_full_size_workload(name, heads):
+    _full_size(0, name, heads, salt=len(name))
+
+
+def test_full_size_long_video_split_kv():
+    """The 65520-token workload's heads 5 and 22 (their own contiguous
+    tensors) with the keys forced into 5 splits and merged: every query tile
+    against the oracle."""
+    w = WORKLOADS["long_video"]
+    q, k, v = make_qkv(w, device="cuda")
+    hs = [5, 22]
+    q, k, v = (t[:, :, hs].contiguous() for t in (q, k, v))
+    assert binding.attn_splits(1, len(hs), w.Nq, w.Nk, 5) == 5
+    qz_, kz_, vz_, o, lse = _run_gpu(0, q, k, v, num_splits=5)
+    ref = oracle_quantize(0, q, k, v)
+    _assert_quantized_equal(0, (qz_, kz_, vz_), ref)
+    rows = _tile_rows(w.Nq, salt=5)
+    ro, rl = _oracle_attention(0, *ref, w.Nq, w.Nk, rows=rows)
+    assert_attention_close(o, lse, ro, rl, rows=rows)
 
 
 # ------------------------------------------------------------------ MXFP4 Q/K attention
@@ -337,20 +382,10 @@ def test_attention_mxfp4_deterministic(name):
     assert binding.sage_last_device_status() == 0
 
 
-@pytest.mark.parametrize("name,heads", [("mxfp4_self", [0, 11, 23]), ("cross_ragged_mxfp4", None)])
+@pytest.mark.parametrize("name,heads", [("mxfp4_self", [0, 11, 23]),
+                                        ("cross_ragged_mxfp4", [0, 23])])
 def test_full_size_workload_mxfp4(name, heads):
-    w = WORKLOADS[name]
-    q, k, v = make_qkv(w, device="cuda")
-    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(1, q, k, v, k_lens=w.k_lens)
-    hs = list(range(w.H)) if heads is None else heads
-    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
-    qz, kz, vz = oracle_quantize(1, sub(q), sub(k), sub(v), k_lens=w.k_lens)
-    assert_qk_equal(1, qq[:, hs], qs[:, hs], *qz)
-    assert_qk_equal(1, kq[:, hs], ks[:, hs], *kz)
-    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
-    rows = _sample_rows(w.Nq)
-    ro, rl = _oracle_attention(1, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
-    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+    _full_size(1, name, heads, salt=3)
 
 
 # ------------------------------------------------------------------ FP8 E4M3 Q/K attention
@@ -414,17 +449,7 @@ def test_attention_fp8_deterministic():
 
 @pytest.mark.parametrize("name,heads", [("image_dit_fp8", [0, 5, 23]), ("video_dit_fp8", [0, 39])])
 def test_full_size_workload_fp8(name, heads):
-    w = WORKLOADS[name]
-    q, k, v = make_qkv(w, device="cuda")
-    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(2, q, k, v, k_lens=w.k_lens)
-    sub = lambda t: t[:, :, heads]  # noqa: E731  head slice of [B, N, H, D]
-    qz, kz, vz = oracle_quantize(2, sub(q), sub(k), sub(v), k_lens=w.k_lens)
-    assert_qk_equal(2, qq[:, heads], qs[:, heads], *qz)
-    assert_qk_equal(2, kq[:, heads], ks[:, heads], *kz)
-    assert_v_equal(vq[:, heads], vs[:, heads], *vz)
-    rows = _sample_rows(w.Nq)
-    ro, rl = _oracle_attention(2, qz, kz, vz, w.Nq, w.Nk, k_lens=w.k_lens, rows=rows)
-    assert_attention_close(o[:, :, heads], lse[:, heads], ro, rl, rows=rows)
+    _full_size(2, name, heads, salt=7)
 
 
 # ------------------------------------------------------------------ Hadamard-rotated MXFP4 Q/K
@@ -485,18 +510,7 @@ def test_attention_mxfp4h_deterministic():
 
 
 def test_full_size_workload_mxfp4h():
-    w = WORKLOADS["mxfp4h_self"]
-    q, k, v = make_qkv(w, device="cuda")
-    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(3, q, k, v)
-    hs = [0, 11, 23]
-    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
-    qz, kz, vz = oracle_quantize(3, sub(q), sub(k), sub(v))
-    assert_qk_equal(3, qq[:, hs], qs[:, hs], *qz)
-    assert_qk_equal(3, kq[:, hs], ks[:, hs], *kz)
-    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
-    rows = _sample_rows(w.Nq)
-    ro, rl = _oracle_attention(3, qz, kz, vz, w.Nq, w.Nk, rows=rows)
-    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+    _full_size(3, "mxfp4h_self", [0, 11, 23], salt=11)
 
 
 # ------------------------------------------------------------------ K smoothing (INT8)
@@ -582,15 +596,17 @@ def test_full_size_video_k_smooth():
     w = WORKLOADS["video_dit"]
     q, k, v = make_qkv(w, device="cuda")
     (qq, qs), (kq, ks, km), (vq, vs), o, lse = _run_gpu_smooth(q, k, v)
+    qz = oracle.quantize_int8(bf16_bits(q))
+    rq, rs, rm = oracle.quantize_int8_smooth(bf16_bits(k))
+    vz = oracle.quantize_v_fp8(bf16_bits(v))
+    assert_qk_equal(0, qq, qs, *qz)
+    _assert_smooth_equal(kq, ks, km, rq, rs, rm)
+    assert_v_equal(vq, vs, *vz)
+    del qq, kq, vq
     hs = [0, 17, 39]
-    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
-    qz = oracle.quantize_int8(bf16_bits(sub(q)))
-    rq, rs, rm = oracle.quantize_int8_smooth(bf16_bits(sub(k)))
-    vz = oracle.quantize_v_fp8(bf16_bits(sub(v)))
-    assert_qk_equal(0, qq[:, hs], qs[:, hs], *qz)
-    _assert_smooth_equal(kq[:, hs], ks[:, hs], km[:, hs], rq, rs, rm)
-    rows = _sample_rows(w.Nq)
-    ro, rl, _ = oracle.attention(0, *qz, rq, rs, *vz, Nq=w.Nq, Nk=w.Nk, rows=rows, k_mean=rm)
+    rows = _tile_rows(w.Nq, salt=17)
+    ro, rl, _ = oracle.attention(0, *_heads(qz, hs), *_heads((rq, rs), hs), *_heads(vz, hs),
+                                 Nq=w.Nq, Nk=w.Nk, rows=rows, k_mean=_heads((rm,), hs)[0])
     assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
 
 
@@ -706,18 +722,7 @@ def test_attention_v4_deterministic():
 
 
 def test_full_size_workload_v4():
-    w = WORKLOADS["mxfp4_v4_self"]
-    q, k, v = make_qkv(w, device="cuda")
-    (qq, qs), (kq, ks), (vq, vs), o, lse = _run_gpu(4, q, k, v)
-    hs = [0, 11, 23]
-    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
-    qz, kz, vz = oracle_quantize(4, sub(q), sub(k), sub(v))
-    assert_qk_equal(4, qq[:, hs], qs[:, hs], *qz)
-    assert_qk_equal(4, kq[:, hs], ks[:, hs], *kz)
-    assert_v_equal(vq[:, hs], vs[:, hs], *vz)
-    rows = _sample_rows(w.Nq)
-    ro, rl = _oracle_attention(4, qz, kz, vz, w.Nq, w.Nk, rows=rows)
-    assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
+    _full_size(4, "mxfp4_v4_self", [0, 11, 23], salt=13)
 
 
 # ------------------------------------------------------------------ Q smoothing and dS (INT8)
@@ -817,18 +822,21 @@ def test_full_size_video_q_and_k_smooth():
                                    delta_s=ds)
     torch.cuda.synchronize()
     assert binding.sage_last_device_status() == 0
-    hs = [0, 39]
-    sub = lambda t: t[:, :, hs]  # noqa: E731  head slice of [B, N, H, D]
-    rq, rs, rm = oracle.quantize_int8_qsmooth(bf16_bits(sub(q)))
-    rk, rks, rmu = oracle.quantize_int8_smooth(bf16_bits(sub(k)))
-    rv = oracle.quantize_v_fp8(bf16_bits(sub(v)))
-    assert_qk_equal(0, qq[:, hs], qs[:, hs], rq, rs)
-    np.testing.assert_array_equal(qm[:, hs].cpu().numpy().view(np.uint32), rm.view(np.uint32))
+    rq, rs, rm = oracle.quantize_int8_qsmooth(bf16_bits(q))
+    rk, rks, rmu = oracle.quantize_int8_smooth(bf16_bits(k))
+    rv = oracle.quantize_v_fp8(bf16_bits(v))
+    assert_qk_equal(0, qq, qs, rq, rs)
+    np.testing.assert_array_equal(qm.cpu().numpy().view(np.uint32), rm.view(np.uint32))
+    _assert_smooth_equal(kq, ks, km, rk, rks, rmu)
+    assert_v_equal(vq, vs, *rv)
+    del qq, kq, vq
     rds = oracle.delta_s(rk, rks, rm, Nq=w.Nq, Nk=w.Nk, k_mean=rmu)
-    _ds_close(ds[:, hs], rds)
-    rows = _sample_rows(w.Nq)
-    ro, rl, _ = oracle.attention(0, rq, rs, rk, rks, *rv, Nq=w.Nq, Nk=w.Nk, rows=rows,
-                                 delta_s=rds, k_mean=rmu)
+    _ds_close(ds, rds)
+    hs = [0, 39]
+    rows = _tile_rows(w.Nq, salt=23)
+    ro, rl, _ = oracle.attention(0, *_heads((rq, rs, rk, rks), hs), *_heads(rv, hs), Nq=w.Nq,
+                                 Nk=w.Nk, rows=rows, delta_s=_heads((rds,), hs)[0],
+                                 k_mean=_heads((rmu,), hs)[0])
     assert_attention_close(o[:, :, hs], lse[:, hs], ro, rl, rows=rows)
 
 
@@ -852,35 +860,53 @@ def _sweep_params(seed):
     return fmt, B, H, Nq, Nk, lens, splits, scale, structure, smooth
 
 
+# Draws whose FP8 P codes land on the other side of an E4M3 rounding boundary
+# for a dominant key of a peaked row: the kernel decides each code on a
+# binary32 logit, the oracle on a binary64 one, and one flipped code of weight
+# ~1/2 moves O by more than 1e-2 (cosine and LSE stay inside their bars).
+# Draw 20 (INT8, Q smoothing, softmax_scale 0.2, 256 x 200 keys): O max-abs
+# 0.0188 against the binary64 oracle; the same comparison with the decision
+# taken on binary32 logits passes.
+_BINARY32_DECISION_DRAWS = {20}
+
+
 @pytest.mark.parametrize("seed", range(24))
 def test_randomized_sweep_against_oracle(seed):
     fmt, B, H, Nq, Nk, lens, splits, scale, structure, smooth = _sweep_params(seed)
     w = Workload("case", B, H, Nq, Nk, seed=500 + seed, structure=structure)
     q, k, v = (t.cuda() for t in make_qkv(w))
-    # The INT8 format decides its FP8 P codes on binary32 logits, so the oracle
-    # takes that decision in binary32 too (logits32); the other formats' S is
-    # an FP32 sum in the tensor core's order and stays binary64.
+    # The reference is the binary64 oracle for every draw and format.
     if smooth == "none":
         _, _, _, o, lse = _run_gpu(fmt, q, k, v, k_lens=lens, num_splits=splits,
                                    softmax_scale=scale)
         qz, kz, vz = oracle_quantize(fmt, q, k, v, k_lens=lens)
-        if fmt == 0:
-            ro, rl, _ = oracle.attention(0, *qz, *kz, *vz, Nq=Nq, Nk=Nk, k_lens=lens,
-                                         softmax_scale=scale, logits32=True)
-        else:
-            ro, rl = _oracle_attention(fmt, qz, kz, vz, Nq, Nk, k_lens=lens, softmax_scale=scale)
+        ofmt, oscale = oracle_attention_format(fmt, scale)
+        oargs = (ofmt, *qz, *kz, *vz)
+        okw = dict(Nq=Nq, Nk=Nk, k_lens=lens, softmax_scale=oscale)
     elif smooth == "k":
         _, _, _, o, lse = _run_gpu_smooth(q, k, v, k_lens=lens, num_splits=splits,
                                           softmax_scale=scale)
         qz = oracle.quantize_int8(bf16_bits(q))
         rk, rks, rmu = oracle.quantize_int8_smooth(bf16_bits(k), lens=lens)
         vz = oracle.quantize_v_fp8(bf16_bits(v), lens=lens)
-        ro, rl, _ = oracle.attention(0, *qz, rk, rks, *vz, Nq=Nq, Nk=Nk, k_lens=lens,
-                                     softmax_scale=scale, k_mean=rmu, logits32=True)
+        oargs = (0, *qz, rk, rks, *vz)
+        okw = dict(Nq=Nq, Nk=Nk, k_lens=lens, softmax_scale=scale, k_mean=rmu)
     else:
         (o, lse), (rq, rs, rk, rks, rv, rds, rmu) = _qsmooth_case(
             q, k, v, k_lens=lens, num_splits=splits, softmax_scale=scale,
             smooth_k=(smooth == "qk"))
-        ro, rl, _ = oracle.attention(0, rq, rs, rk, rks, *rv, Nq=Nq, Nk=Nk, k_lens=lens,
-                                     softmax_scale=scale, delta_s=rds, k_mean=rmu, logits32=True)
-    assert_attention_close(o, lse, ro, rl)
+        oargs = (0, rq, rs, rk, rks, *rv)
+        okw = dict(Nq=Nq, Nk=Nk, k_lens=lens, softmax_scale=scale, delta_s=rds, k_mean=rmu)
+    ro, rl, _ = oracle.attention(*oargs, **okw)
+    max_abs, cos, lse_err = compare_attention(o, lse, ro, rl)
+    assert cos >= O_MIN_COS, f"O cosine {cos}"
+    assert lse_err <= LSE_MAX_ABS, f"LSE max-abs {lse_err}"
+    if max_abs > O_MAX_ABS and seed in _BINARY32_DECISION_DRAWS:
+        # Diagnostic only: the same oracle with the INT8 FP8-P decision taken
+        # on binary32 logits (the kernel's precision) must agree.
+        ro32, rl32, _ = oracle.attention(*oargs, **okw, logits32=True)
+        assert_attention_close(o, lse, ro32, rl32)
+        pytest.xfail(f"O max-abs {max_abs:.4f} > {O_MAX_ABS} against the binary64 oracle "
+                     f"(cosine {cos:.7f}, LSE {lse_err:.2e}): FP8 P codes decided on binary32 "
+                     "logits; within every bar against the binary32-decision oracle")
+    assert max_abs <= O_MAX_ABS, f"O max-abs {max_abs}"
