@@ -280,6 +280,18 @@ typedef struct {
   const float* delta_s; /* nullable: Q smoothing's dS from sage_delta_s (INT8 only;
                            16-byte aligned): every logit of row i gains
                            softmax_scale * delta_s[b][h][i / 128][j] */
+  int64_t wait_cycles;  /* bound of every wait between the kernel's warps, in SM
+                           cycles: 0 = default (2^31, about a second); 1 .. 2^31.
+                           A wait that runs out ends the launch early (no O or
+                           LSE written for the affected tiles) and sets the device
+                           status read by sage_last_device_status
+                           (SAGE_ERR_DEVICE_TIMEOUT) */
+  int32_t test_withhold_v; /* testing only; must be 0 in normal use. 1: the V
+                           producer of every CTA issues none of its loads, so the
+                           P V waits run out after wait_cycles (which must then be
+                           set, <= 2^24). The launch issues no copy or MMA that it
+                           does not also wait for before it exits. */
+  int32_t reserved;     /* must be 0 */
 } sage_attn_options_t;
 
 /* Attention forward ("[ROCm] Add aiter_sage_attn ...", Changes; "new MHA v4

@@ -38,7 +38,9 @@ class Strides(ctypes.Structure):
 
 class AttnOptions(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int32), ("cta_mode", ctypes.c_int32),
-                ("k_mean", ctypes.c_void_p), ("delta_s", ctypes.c_void_p)]
+                ("k_mean", ctypes.c_void_p), ("delta_s", ctypes.c_void_p),
+                ("wait_cycles", ctypes.c_int64), ("test_withhold_v", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
@@ -314,9 +316,12 @@ def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int
                   out: Optional[torch.Tensor] = None, return_lse: bool = True,
                   lse: Optional[torch.Tensor] = None, num_splits: int = 0,
                   workspace: Optional[torch.Tensor] = None, k_mean: Optional[torch.Tensor] = None,
-                  delta_s: Optional[torch.Tensor] = None):
+                  delta_s: Optional[torch.Tensor] = None, wait_cycles: int = 0,
+                  test_withhold_v: bool = False):
     """Attention forward on quantized operands. Returns (O ``[B, Nq, H, D]`` bf16, LSE or None).
-    k_mean: the channel means from sage_quantize_k_smooth when K was smoothed."""
+    k_mean: the channel means from sage_quantize_k_smooth when K was smoothed.
+    wait_cycles / test_withhold_v: sage_attn_options_t's wait bound and its
+    testing-only withheld V loads."""
     B, H = q_q.shape[0], q_q.shape[1]
     D = 128
     dev = q_q.device
@@ -329,7 +334,8 @@ def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ln = _lens_tensor(k_lens, dev)
     opts = AttnOptions(num_splits, 0, None if k_mean is None else k_mean.data_ptr(),
-                       None if delta_s is None else delta_s.data_ptr())
+                       None if delta_s is None else delta_s.data_ptr(), int(wait_cycles),
+                       int(bool(test_withhold_v)), 0)
     sc = -1.0 if softmax_scale is None else float(softmax_scale)
     _check(_lib.sage_attn_fwd(fmt, _ptr(q_q), _ptr(q_scale), _ptr(k_q), _ptr(k_scale), _ptr(v_q),
                               _ptr(v_scale), _ptr(ln), B, H, Nq, Nk, D, sc, causal, _ptr(out),

@@ -222,8 +222,8 @@ __device__ __forceinline__ float exp2_neg_int(float k) {
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                              int* status) {
-  if (mbar_wait(bar, parity, abort)) return true;
+                                              int* status, long long limit) {
+  if (mbar_wait(bar, parity, abort, limit)) return true;
   if (!*abort) {
     *abort = 1;
     atomicOr(status, kStatusTimeout);
@@ -235,13 +235,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // common case (phase already complete) costs one try_wait: the whole warp
 // executes it on the same barrier state, so its result is uniform already.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+                                          int* status, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
-  const bool r = wait_or_abort(bar, parity, abort, status);
+  const bool r = wait_or_abort(bar, parity, abort, status, limit);
   return __all_sync(0xffffffffu, r);
 }
 
-// Bounded wait that ignores the abort flag (used to drain in-flight work).
+// Bounded wait that ignores the abort flag (used to drain in-flight work,
+// which always completes; so it keeps the default bound).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
   const int zero = 0;
   if (!mbar_wait(bar, parity, &zero)) atomicOr(status, kStatusTimeout);
@@ -481,7 +482,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     int s = 0, filled = 0;
     uint32_t rph = 0;
     for (int it = 0; it < niter; ++it) {
-      if (it >= STAGES && !warp_wait(&k_empty[s], rph ^ 1u, abort, p.status)) break;
+      if (it >= STAGES && !warp_wait(&k_empty[s], rph ^ 1u, abort, p.status, p.wait_cycles)) break;
       if constexpr (kMx) {
         st_shared_v4(smem_u32(sSf + (NQT + s) * 512) + lane * 16, kw[0], kw[1], kw[2], kw[3]);
         fence_proxy_async_smem();
@@ -523,7 +524,10 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     int s = 0, filled = 0;
     uint32_t rph = 0;
     for (int it = 0; it < niter; ++it) {
-      if (it >= STAGES && !warp_wait(&v_empty[s], rph ^ 1u, abort, p.status)) break;
+      // Testing only: no V load at all, so that the P V waits run out (no
+      // copy is left in flight: nothing was issued to drain).
+      if (p.withhold_v) break;
+      if (it >= STAGES && !warp_wait(&v_empty[s], rph ^ 1u, abort, p.status, p.wait_cycles)) break;
       if constexpr (FMT == 4) {
         // The tile's E8M0 scales (128 channel rows x 4 bytes, contiguous),
         // written in the line order of the TMEM copy (line L: rows L, L+32,
@@ -656,8 +660,8 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     // V ring position of the P V steps; both advance after a tile's last step.
     int ks = 0, vs = 0;
     uint32_t kph = 0, vph = 0;
-    bool ok = warp_wait(q_full, 0, abort, p.status);
-    if (ok) ok = warp_wait(&k_full[0], 0, abort, p.status);
+    bool ok = warp_wait(q_full, 0, abort, p.status, p.wait_cycles);
+    if (ok) ok = warp_wait(&k_full[0], 0, abort, p.status, p.wait_cycles);
     tc_fence_after();
     if (ok) {
       if constexpr (kMx) {
@@ -679,10 +683,10 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       if (v < nsteps) {
         const int hv = v & (kSteps - 1);
         if (hv == 0) {
-          if (!(ok = warp_wait(&k_full[ks], kph, abort, p.status))) break;
+          if (!(ok = warp_wait(&k_full[ks], kph, abort, p.status, p.wait_cycles))) break;
           tc_fence_after();
         }
-        if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(u) & 1u, abort, p.status))) break;
+        if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(u) & 1u, abort, p.status, p.wait_cycles))) break;
         tc_fence_after();
         const int sf_slot = (v / kSteps) & 1;
         if constexpr (kMx) {
@@ -697,11 +701,11 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       const int hu = u & (kSteps - 1);
       const int slot = u & (kPSlots - 1);
       if (hu == 0) {
-        if (!(ok = warp_wait(&v_full[vs], vph, abort, p.status))) break;
+        if (!(ok = warp_wait(&v_full[vs], vph, abort, p.status, p.wait_cycles))) break;
         tc_fence_after();
       }
       if (!(ok = warp_wait(&p_full[t * kPSlots + slot],
-                           static_cast<uint32_t>(u >> kPSlotShift) & 1u, abort, p.status)))
+                           static_cast<uint32_t>(u >> kPSlotShift) & 1u, abort, p.status, p.wait_cycles)))
         break;
       tc_fence_after();
       issue_pv(slot, vs, hu, (u / kSteps) & 1, u > 0);
@@ -757,7 +761,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         sk = sk_next;
         if (iu + 1 < niter) sk_next = __ldg(&kscale[j + 1]);
       }
-      if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(u) & 1u, abort, p.status))) break;
+      if (!(ok = warp_wait(&s_full[t], static_cast<uint32_t>(u) & 1u, abort, p.status, p.wait_cycles))) break;
       tc_fence_after();
       float s[kStep];
       {
@@ -826,7 +830,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         // Conditional rescale: O_t must hold P V up to the previous step.
         const int ps = (u - 1) & (kPSlots - 1);
         if (!(ok = warp_wait(&o_done[t * kPSlots + ps],
-                             static_cast<uint32_t>((u - 1) >> kPSlotShift) & 1u, abort, p.status)))
+                             static_cast<uint32_t>((u - 1) >> kPSlotShift) & 1u, abort, p.status, p.wait_cycles)))
           break;
         tc_fence_after();
         const float f = rescale ? exp2_neg_int(m - m_new) : 1.0f;
@@ -921,7 +925,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     // ---- epilogue
     if (ok)
       ok = warp_wait(&o_done[t * kPSlots + ((nsteps - 1) & (kPSlots - 1))],
-                     static_cast<uint32_t>((nsteps - 1) >> kPSlotShift) & 1u, abort, p.status);
+                     static_cast<uint32_t>((nsteps - 1) >> kPSlotShift) & 1u, abort, p.status, p.wait_cycles);
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
@@ -930,7 +934,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       // units alpha_q * (q8 . mean_k), from this row's codes in the Q tile.
       float lse_add = 0.0f;
       if constexpr (FMT == 0) {
-        if (p.k_mean && (ok = warp_wait(q_full, 0, abort, p.status)))
+        if (p.k_mean && (ok = warp_wait(q_full, 0, abort, p.status, p.wait_cycles)))
           lse_add = alpha_q * q_dot_kmean(smem_u32(sQ + t * 32768), r, p.k_mean + bh * 128);
       }
       // l is in units of P: 2^(8 - kHeadroom) times 2^(t - m) for the FP8 P,

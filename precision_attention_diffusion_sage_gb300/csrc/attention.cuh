@@ -28,6 +28,8 @@ struct AttnParams {
   float* o_part;         // [splits][B][H][Nq][128] when num_splits > 1
   float* lse_part;       // [splits][B][H][Nq]
   int* status;
+  long long wait_cycles; // bound of each wait between warps (SM cycles)
+  int withhold_v;        // testing only: the V producer issues no load
 };
 
 struct AttnLaunch {

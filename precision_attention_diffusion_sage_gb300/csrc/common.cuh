@@ -12,6 +12,10 @@ namespace sage {
 constexpr int kStatusDeviceArg = 1;  // a k_lens / lens entry was out of range
 constexpr int kStatusTimeout = 2;    // a bounded wait ran out
 
+// Default bound of a wait between warps (mbarrier phases), in SM cycles:
+// about a second at 2 GHz.
+constexpr long long kWaitCycles = 1ll << 31;
+
 constexpr int kHeadDim = 128;
 constexpr int kTile = 128;  // tokens per quantization block and per MMA tile
 

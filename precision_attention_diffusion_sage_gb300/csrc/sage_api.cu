@@ -301,6 +301,12 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
     return SAGE_ERR_INVALID_ARG;
   const int req = opts ? opts->num_splits : 0;
   if (req < 0 || req > 64) return SAGE_ERR_INVALID_ARG;
+  const int64_t wait_cycles = opts ? opts->wait_cycles : 0;
+  const int withhold_v = opts ? opts->test_withhold_v : 0;
+  if (wait_cycles < 0 || wait_cycles > (int64_t{1} << 31) || (opts && opts->reserved != 0) ||
+      withhold_v < 0 || withhold_v > 1 ||
+      (withhold_v && (wait_cycles == 0 || wait_cycles > (int64_t{1} << 24))))
+    return SAGE_ERR_INVALID_ARG;
   const int64_t splits = resolve_splits(req, B, H, Nq, Nk);
   if (splits * B > kMaxGridYZ) return SAGE_ERR_INVALID_ARG;
   const size_t need = sage_workspace_bytes(2, fmt, B, H, Nq, Nk, D, static_cast<int>(splits));
@@ -343,6 +349,8 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   p.o_part = splits > 1 ? static_cast<float*>(workspace) : nullptr;
   p.lse_part = splits > 1 ? static_cast<float*>(workspace) + splits * B * H * Nq * D : nullptr;
   p.status = status;
+  p.wait_cycles = wait_cycles > 0 ? wait_cycles : kWaitCycles;
+  p.withhold_v = withhold_v;
   return from_cuda(launch_attention(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -374,6 +382,6 @@ sage_status_t sage_last_device_status(sage_stream_t stream) {
   return SAGE_OK;
 }
 
-const char* sage_version(void) { return "libsage 0.1 (sm_103a)"; }
+const char* sage_version(void) { return "libsage 0.2 (sm_103a)"; }
 
 }  // extern "C"

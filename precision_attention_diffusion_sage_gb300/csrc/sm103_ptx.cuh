@@ -10,9 +10,9 @@
 #include <cstdint>
 #include <cuda.h>
 
-namespace sage {
+#include "common.cuh"
 
-constexpr long long kWaitCycles = 1ll << 31;  // ~1 s at 2 GHz
+namespace sage {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -76,16 +76,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Waits for the phase with the given parity to complete. Gives up (returns
-// false) after kWaitCycles or as soon as *abort is non-zero. Between checks
-// the thread sleeps in the barrier (hardware wake-up on completion).
+// false) after `limit` SM cycles (default kWaitCycles) or as soon as *abort is
+// non-zero. Between checks the thread sleeps in the barrier (hardware wake-up
+// on completion).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort) {
+                                          const volatile int* abort,
+                                          long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
 

@@ -239,6 +239,30 @@ def test_device_status_reports_bad_k_lens():
     assert binding.sage_last_device_status() == 0   # read-and-clear
 
 
+def test_bounded_wait_runs_out_and_next_call_is_clean():
+    """The timeout path: with V's loads withheld (testing only) and a bound of
+    2^16 SM cycles, every CTA's P V waits run out; the launch ends with nothing
+    in flight, the device status reads SAGE_ERR_DEVICE_TIMEOUT once (then
+    clears), and the next ordinary call in the same process matches the
+    oracle."""
+    w, q, k, v = _small(1, 2, 256, 256, seed=48, structure="k_offset_std2")
+    qq, qs = binding.sage_quantize_qk(q, 0)
+    kq, ks = binding.sage_quantize_qk(k, 0)
+    vq, vs = binding.sage_quantize_v(v)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=256, Nk=256, wait_cycles=1 << 16,
+                          test_withhold_v=True)
+    assert binding.sage_last_device_status() == -5  # SAGE_ERR_DEVICE_TIMEOUT
+    assert binding.sage_last_device_status() == 0   # read-and-clear
+    o, lse = binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=256, Nk=256)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    qz, kz, vz = oracle_quantize(0, q, k, v)
+    ro, rl = _oracle_attention(0, qz, kz, vz, 256, 256)
+    assert_attention_close(o, lse, ro, rl)
+
+
 # ------------------------------------------------------------------ full-size workloads
 # Every full-size test compares the quantized tensors and scales of every
 # batch and head bit for bit, and attention on one query row of every 128-row

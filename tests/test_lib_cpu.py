@@ -103,6 +103,28 @@ def test_host_validation_rejects_before_launch():
                              -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None) == -1
 
 
+def test_wait_bound_options_validated_before_launch():
+    """The per-call wait bound and the testing-only withheld V loads are
+    checked on the host: bound in [0, 2^31], withholding only with an explicit
+    bound of at most 2^24 cycles, the reserved word zero."""
+    lib = binding.library()
+    S = binding.Strides(0, 0, 0)
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(**kw):
+        opts = binding.AttnOptions(1, 0, None, None, kw.get("wait", 0), kw.get("withhold", 0),
+                                   kw.get("reserved", 0))
+        return lib.sage_attn_fwd(0, fake, fake, fake, fake, fake, fake, None, 1, 1, 128, 128, 128,
+                                 -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None)
+
+    assert call(wait=-1) == -1
+    assert call(wait=(1 << 31) + 1) == -1
+    assert call(withhold=1) == -1                      # needs an explicit bound
+    assert call(withhold=1, wait=(1 << 24) + 1) == -1  # and a short one
+    assert call(withhold=2, wait=1 << 16) == -1
+    assert call(reserved=1) == -1
+
+
 def test_status_strings():
     lib = binding.library()
     for code in range(-7, 1):
