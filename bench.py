@@ -296,6 +296,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--cta-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="attention tiles: 0 library choice, 1 one CTA, 2 CTA pairs (cta_group::2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -404,7 +406,7 @@ def main():
     def attn():
         binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens, out=o,
                               lse=lse, num_splits=args.splits, workspace=aws, k_mean=km,
-                              delta_s=dsb)
+                              delta_s=dsb, cta_mode=args.cta_mode)
 
     def quant_qkv():
         binding.sage_quantize_qkv(q, k, v, fmt, k_lens=k_lens, outs=((qq, qs), (kq, ks), (vq, vs)),
@@ -506,7 +508,7 @@ def main():
             vd.copy_(vh, non_blocking=True)
             oo, ll = binding.sage_attention(qd, kd, vd, fmt=fmt, k_lens=k_lens,
                                             num_splits=args.splits, smooth_k=w.smooth_k,
-                                            smooth_q=w.smooth_q)
+                                            smooth_q=w.smooth_q, cta_mode=args.cta_mode)
             oh.copy_(oo, non_blocking=True)
             lh.copy_(ll, non_blocking=True)
 
@@ -558,10 +560,13 @@ def main():
     mhz = (clk or {}).get("sm_mhz") or 2070.0
     exp2_ms = exp2_count / (_EX2_PER_CLK_SM * 152 * mhz * 1e6) * 1e3
     nqt = 2 if Nqp >= 256 else 1
+    # The library's default (cta_mode 0) is 1-CTA tiles for every shape.
+    cta2 = args.cta_mode == 2
     kfmt = 1 if fmt == 3 else fmt   # the rotated MXFP4 format runs the MXFP4 kernel
     # Q smoothing runs the instance that adds dS to the logits (last template flag).
     ds_flag = ",1" if w.smooth_q else ""
-    kernel = f"sage_attn_kernel<{kfmt},{nqt},{(2 if nqt == 2 else 3) if kfmt == 0 else 4}{ds_flag}>"
+    stages = 4 if cta2 else ((2 if nqt == 2 else 3) if kfmt == 0 else 4)
+    kernel = f"sage_attn_kernel<{kfmt},{nqt},{stages}{ds_flag}{',0,1' if cta2 else ''}>"
     fmt_names = {0: ("int8+fp8e4m3", "int8_qk_fp8_v"), 1: ("mxfp4+fp8e4m3", "mxfp4_qk_fp8_v"),
                  4: ("mxfp4", "mxfp4_qk_mxfp4_pv"),
                  2: ("fp8e4m3", "fp8_qk_fp8_v"),
@@ -582,8 +587,9 @@ def main():
                    "l2": "flushed between steps (256 MiB read outside the timed events)",
                    "launch": ("two CUDA graphs per step: the quantize call (sage_quantize_qkv; with K "
                               "smoothing the three quantize calls) and the attention call"),
-                   "cta": ("1-CTA tiles (cta_group::1), "
-                           f"{nqt} query tile(s) of 128 rows per CTA, one MMA warp per tile"),
+                   "cta": (("2-CTA tiles (cta_group::2, clusters of two CTAs, M = 256 rows), "
+                            if cta2 else "1-CTA tiles (cta_group::1), ")
+                           + f"{nqt} query tile(s) of 128 rows per CTA, one MMA warp per tile"),
                    "parallelism": f"replicas x{world}"},
         "eager_ms_per_step": eager_ms,
         "attn_only_tflops": achieved,

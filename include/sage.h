@@ -272,7 +272,14 @@ sage_status_t sage_delta_s(sage_format_t fmt, const float* q_mean, const void* k
 
 typedef struct {
   int32_t num_splits;   /* KV splits: 0 = library choice, 1 = no split, >1 = forced */
-  int32_t cta_mode;     /* reserved: 0 = library choice */
+  int32_t cta_mode;     /* 0 = library choice (per shape, from measurement: 1-CTA),
+                           1 = 1-CTA tiles (one SM per 128-row query tile pair),
+                           2 = 2-CTA tiles ("[None][feat] Add VisualGen FA4 autotuning",
+                           first paragraph: 1-CTA vs 2-CTA): clusters of two CTAs on an
+                           SM pair run cta_group::2 MMAs of M = 256 rows, each CTA
+                           staging half of every K and V tile; INT8 and FP8 Q/K formats,
+                           Nq > 128, no delta_s (else SAGE_ERR_UNSUPPORTED). The results
+                           equal the 1-CTA ones up to FP32 summation order. */
   const float* k_mean;  /* nullable: the k_mean written by sage_quantize_k_smooth when K
                            was smoothed (SAGE_FMT_QK_INT8_V_FP8 only; 16-byte aligned);
                            LSE_i then adds softmax_scale * (s_q q8_i) . k_mean, the

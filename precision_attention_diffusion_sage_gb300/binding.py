@@ -317,11 +317,12 @@ def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int
                   lse: Optional[torch.Tensor] = None, num_splits: int = 0,
                   workspace: Optional[torch.Tensor] = None, k_mean: Optional[torch.Tensor] = None,
                   delta_s: Optional[torch.Tensor] = None, wait_cycles: int = 0,
-                  test_withhold_v: bool = False):
+                  test_withhold_v: bool = False, cta_mode: int = 0):
     """Attention forward on quantized operands. Returns (O ``[B, Nq, H, D]`` bf16, LSE or None).
     k_mean: the channel means from sage_quantize_k_smooth when K was smoothed.
     wait_cycles / test_withhold_v: sage_attn_options_t's wait bound and its
-    testing-only withheld V loads."""
+    testing-only withheld V loads. cta_mode: 0 library choice, 1 one-CTA tiles,
+    2 two-CTA tiles (cta_group::2 pairs)."""
     B, H = q_q.shape[0], q_q.shape[1]
     D = 128
     dev = q_q.device
@@ -333,7 +334,7 @@ def sage_attn_fwd(fmt: int, q_q, q_scale, k_q, k_scale, v_q, v_scale, *, Nq: int
     if need > 0 and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ln = _lens_tensor(k_lens, dev)
-    opts = AttnOptions(num_splits, 0, None if k_mean is None else k_mean.data_ptr(),
+    opts = AttnOptions(num_splits, int(cta_mode), None if k_mean is None else k_mean.data_ptr(),
                        None if delta_s is None else delta_s.data_ptr(), int(wait_cycles),
                        int(bool(test_withhold_v)), 0)
     sc = -1.0 if softmax_scale is None else float(softmax_scale)
@@ -352,7 +353,8 @@ def sage_last_device_status() -> int:
 
 def sage_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: int = FMT_INT8,
                    k_lens=None, softmax_scale: Optional[float] = None, num_splits: int = 0,
-                   return_lse: bool = True, smooth_k: bool = False, smooth_q: bool = False):
+                   return_lse: bool = True, smooth_k: bool = False, smooth_q: bool = False,
+                   cta_mode: int = 0):
     """Quantize Q/K/V (one sage_quantize_qkv call) and attend. smooth_q (INT8
     only) quantizes Q with sage_quantize_q_smooth and adds sage_delta_s's
     correction to the logits. smooth_k
@@ -377,7 +379,7 @@ def sage_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: in
         (qq, qs), (kq, ks), (vq, vs) = sage_quantize_qkv(q, k, v, fmt, k_lens=k_lens)
     return sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
                          softmax_scale=softmax_scale, num_splits=num_splits,
-                         return_lse=return_lse, k_mean=km, delta_s=ds)
+                         return_lse=return_lse, k_mean=km, delta_s=ds, cta_mode=cta_mode)
 
 
 def int8_codes(x_q: torch.Tensor) -> torch.Tensor:

@@ -95,15 +95,19 @@ struct QKFormat<4> : QKFormat<1> {};
 template <int FMT>
 __host__ __device__ constexpr bool is_mx() { return FMT == 1 || FMT == 4; }
 
-template <int FMT, int NQT, int STAGES>
+template <int FMT, int NQT, int STAGES, bool CTA2 = false>
 struct SmemLayout {
   using F = QKFormat<FMT>;
   static constexpr int kPSlots = 2 * (128 / F::kStep);  // P slots per query tile
   static constexpr int kQ = 0;                             // NQT Q tiles
   static constexpr int kK = kQ + NQT * F::kTileBytes;      // STAGES K tiles
   static constexpr int kVTile = FMT == 4 ? 8192 : 16384;  // V^T 128x128: E2M1 or E4M3
-  static constexpr int kV = kK + STAGES * F::kTileBytes;   // STAGES V tiles
-  static constexpr int kP = kV + STAGES * kVTile;          // NQT x 2 x 16 KB (P, double buffer;
+  // A CTA pair holds half of each K tile (64 keys) and of each V^T tile (64
+  // channels) in each CTA.
+  static constexpr int kKStage = CTA2 ? F::kTileBytes / 2 : F::kTileBytes;
+  static constexpr int kVStage = CTA2 ? kVTile / 2 : kVTile;
+  static constexpr int kV = kK + STAGES * kKStage;         // STAGES V tiles
+  static constexpr int kP = kV + STAGES * kVStage;         // NQT x 2 x 16 KB (P, double buffer;
                                                            // also the O staging of the epilogue)
   static constexpr int kSf = kP + NQT * 2 * 16384;         // (NQT + STAGES) scale blocks
   static constexpr int kSv = kSf + (NQT + STAGES) * F::kSfBytes;  // 128 V channel scales
@@ -221,9 +225,10 @@ __device__ __forceinline__ float exp2_neg_int(float k) {
   return ki < -126 ? 0.0f : __uint_as_float(static_cast<uint32_t>(ki + 127) << 23);
 }
 
+template <bool CL = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
                                               int* status, long long limit) {
-  if (mbar_wait(bar, parity, abort, limit)) return true;
+  if (mbar_wait<CL>(bar, parity, abort, limit)) return true;
   if (!*abort) {
     *abort = 1;
     atomicOr(status, kStatusTimeout);
@@ -234,18 +239,22 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // Warp-collective variant: every lane waits, the result is uniform. The
 // common case (phase already complete) costs one try_wait: the whole warp
 // executes it on the same barrier state, so its result is uniform already.
+// CL: cluster-scope acquire (barriers the peer CTA of a pair arrives on or
+// completes copies on).
+template <bool CL = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* status, long long limit) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const bool r = wait_or_abort(bar, parity, abort, status, limit);
+  if (CL ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const bool r = wait_or_abort<CL>(bar, parity, abort, status, limit);
   return __all_sync(0xffffffffu, r);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight work,
 // which always completes; so it keeps the default bound).
+template <bool CL = false>
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
   const int zero = 0;
-  if (!mbar_wait(bar, parity, &zero)) atomicOr(status, kStatusTimeout);
+  if (!mbar_wait<CL>(bar, parity, &zero)) atomicOr(status, kStatusTimeout);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -292,13 +301,22 @@ __host__ __device__ constexpr bool attn_split_regs() { return !is_mx<FMT>() && N
 
 // DS: Q smoothing's dS is added to the logits (INT8 only; a separate
 // instance, so the plain path keeps its register allocation).
-template <int FMT, int NQT, int STAGES, bool DS = false>
+// CTA2: 2-CTA tiles. The grid's CTAs form clusters of two (CTAs 2c and
+// 2c + 1, on an SM pair); the even CTA's MMA warps issue cta_group::2 MMAs of
+// M = 256 rows (its tile t and its peer's tile t) for both. Each CTA loads
+// its own Q tiles, keys 64r .. 64r + 63 of every K tile and channels 64r ..
+// 64r + 63 of every V^T tile (r = its rank in the pair), so each CTA stages
+// half of the K/V bytes of the 1-CTA kernel; the peer's copies complete on
+// the even CTA's barriers, and the peer's softmax warps arrive there too.
+// Everything else (softmax, epilogue) runs in each CTA on its own rows.
+template <int FMT, int NQT, int STAGES, bool DS = false, bool CTA2 = false>
 __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     sage_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmO, const AttnParams p) {
-  using L = SmemLayout<FMT, NQT, STAGES>;
+  static_assert(!CTA2 || ((FMT == 0 || FMT == 2) && NQT == 2 && !DS), "2-CTA tiles: INT8/FP8");
+  using L = SmemLayout<FMT, NQT, STAGES, CTA2>;
   using F = QKFormat<FMT>;
   using TM = TmemLayout<FMT, NQT>;
   constexpr int kStep = F::kStep;
@@ -342,6 +360,11 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
+  // Rank in the CTA pair (0 without pairs); the even CTA issues the MMAs.
+  const uint32_t rank = CTA2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  // Cluster address of a barrier in the even CTA of the pair.
+  auto lead_bar = [&](uint64_t* bar) { return cluster_map(smem_u32(bar), 0); };
   const int64_t h = blockIdx.y;
   const int64_t b = blockIdx.z / p.num_splits;
   const int split = static_cast<int>(blockIdx.z % p.num_splits);
@@ -349,8 +372,11 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   const int64_t Nq_pad = p.nbq * 128, Nk_pad = p.nbk * 128;
 
   // A CTA of an earlier launch already ran out of a bounded wait: do not
-  // pile further timeouts on top (the status word keeps the error).
-  if (*reinterpret_cast<volatile int*>(p.status) & kStatusTimeout) return;
+  // pile further timeouts on top (the status word keeps the error). (Not
+  // with pairs: the two CTAs of a pair must take the same path, and the word
+  // can change between their reads.)
+  if constexpr (!CTA2)
+    if (*reinterpret_cast<volatile int*>(p.status) & kStatusTimeout) return;
 
   // ---- per-batch key range (uniform over the CTA)
   // Token counts fit in 32 bits (the host caps N at 4,194,240).
@@ -397,8 +423,12 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   // V channel scales (MXFP4 V carries its scales inside the MMA: 1).
   if (threadIdx.x < 128)
     sSv[threadIdx.x] = FMT == 4 ? 1.0f : __ldg(&p.v_scale[bh * 128 + threadIdx.x]);
+  // With pairs, the even CTA's barriers that the peer also arrives on count
+  // its arrivals: q_full one relay arrive, s_free / p_full one per peer warp
+  // (per-warp arrivals in both CTAs: 4 + 4).
+  constexpr int kStepArrivals = CTA2 ? 8 : 128;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, CTA2 && leader ? 2 : 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], NQT);  // one commit per query tile's MMA warp
@@ -407,9 +437,9 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&s_free[t], 128);
+      mbar_init(&s_free[t], kStepArrivals);
       for (int q = 0; q < kPSlots; ++q) {
-        mbar_init(&p_full[t * kPSlots + q], 128);
+        mbar_init(&p_full[t * kPSlots + q], kStepArrivals);
         mbar_init(&o_done[t * kPSlots + q], 1);
       }
     }
@@ -418,11 +448,22 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, TM::kCols);
-    tmem_relinquish();
+    // One warp of each CTA of a pair allocates, collectively for the pair.
+    if constexpr (CTA2) {
+      tmem_alloc_pair(tmem_slot, TM::kCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TM::kCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  // Pairs: both CTAs' barriers are initialised and their TMEM allocated
+  // before either CTA signals the other.
+  if constexpr (CTA2)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   // INT8 with two query tiles: 384 threads launch with 168 registers each, a
@@ -489,13 +530,27 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         __syncwarp();
       }
       if (elect_one()) {
-        mbar_arrive_expect_tx(&k_full[s], F::kTileBytes);
         const int yk = static_cast<int>(bh * Nk_pad) + (j0 + it) * 128;
-        if constexpr (FMT == 0) {
-          tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
-          tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
+        if constexpr (CTA2) {
+          // This CTA's 64 keys of the tile (64-row boxes), completing on the
+          // even CTA's barrier, which expects both halves.
+          if (leader) mbar_arrive_expect_tx(&k_full[s], 2 * L::kKStage);
+          const uint32_t kb = lead_bar(&k_full[s]);
+          const int yh = yk + 64 * static_cast<int>(rank);
+          if constexpr (FMT == 0) {
+            tma_load_2d_pair(sK + s * L::kKStage, &tmK, kb, 0, yh);
+            tma_load_2d_pair(sK + s * L::kKStage + L::kKStage / 2, &tmK, kb, 64, yh);
+          } else {
+            tma_load_2d_pair(sK + s * L::kKStage, &tmK, kb, 0, yh);
+          }
         } else {
-          tma_load_2d(sK + s * F::kTileBytes, &tmK, &k_full[s], 0, yk);
+          mbar_arrive_expect_tx(&k_full[s], F::kTileBytes);
+          if constexpr (FMT == 0) {
+            tma_load_2d(sK + s * 32768, &tmK, &k_full[s], 0, yk);
+            tma_load_2d(sK + s * 32768 + 16384, &tmK, &k_full[s], 64, yk);
+          } else {
+            tma_load_2d(sK + s * F::kTileBytes, &tmK, &k_full[s], 0, yk);
+          }
         }
       }
       __syncwarp();
@@ -511,11 +566,15 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         rph ^= 1u;
       }
     }
-    // Drain: no TMA write may still be in flight when the CTA exits.
-    drain_wait(q_full, 0, p.status);
-    for (int st = 0; st < STAGES; ++st) {
-      const int fills = (filled - st + STAGES - 1) / STAGES;
-      if (fills > 0) drain_wait(&k_full[st], static_cast<uint32_t>(fills - 1) & 1u, p.status);
+    // Drain: no TMA write may still be in flight when the CTA exits. (With
+    // pairs the even CTA's barriers see both CTAs' K copies complete, and
+    // the peer exits only after the final cluster barrier.)
+    drain_wait<CTA2>(q_full, 0, p.status);
+    if (leader) {
+      for (int st = 0; st < STAGES; ++st) {
+        const int fills = (filled - st + STAGES - 1) / STAGES;
+        if (fills > 0) drain_wait<CTA2>(&k_full[st], static_cast<uint32_t>(fills - 1) & 1u, p.status);
+      }
     }
   } else if (warp == kTmaVWarp) {
     // ================================================================ TMA producer (V)
@@ -539,10 +598,18 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         __syncwarp();
       }
       if (elect_one()) {
-        mbar_arrive_expect_tx(&v_full[s], L::kVTile);
-        // E4M3 V^T rows of Nk_pad bytes, or E2M1 rows of Nk_pad / 2 bytes.
-        tma_load_2d(sV + s * L::kVTile, &tmV, &v_full[s], (j0 + it) * (FMT == 4 ? 64 : 128),
-                    static_cast<int>(bh * 128));
+        if constexpr (CTA2) {
+          // This CTA's 64 channels of the V^T tile, completing on the even
+          // CTA's barrier.
+          if (leader) mbar_arrive_expect_tx(&v_full[s], 2 * L::kVStage);
+          tma_load_2d_pair(sV + s * L::kVStage, &tmV, lead_bar(&v_full[s]), (j0 + it) * 128,
+                           static_cast<int>(bh * 128) + 64 * static_cast<int>(rank));
+        } else {
+          mbar_arrive_expect_tx(&v_full[s], L::kVTile);
+          // E4M3 V^T rows of Nk_pad bytes, or E2M1 rows of Nk_pad / 2 bytes.
+          tma_load_2d(sV + s * L::kVTile, &tmV, &v_full[s], (j0 + it) * (FMT == 4 ? 64 : 128),
+                      static_cast<int>(bh * 128));
+        }
       }
       __syncwarp();
       filled = it + 1;
@@ -551,18 +618,29 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         rph ^= 1u;
       }
     }
-    for (int st = 0; st < STAGES; ++st) {
-      const int fills = (filled - st + STAGES - 1) / STAGES;
-      if (fills > 0) drain_wait(&v_full[st], static_cast<uint32_t>(fills - 1) & 1u, p.status);
+    if (leader) {
+      for (int st = 0; st < STAGES; ++st) {
+        const int fills = (filled - st + STAGES - 1) / STAGES;
+        if (fills > 0) drain_wait<CTA2>(&v_full[st], static_cast<uint32_t>(fills - 1) & 1u, p.status);
+      }
     }
-  } else if (warp == kMmaWarp || (NQT == 2 && warp == kMmaWarp1)) {
+  } else if (CTA2 && !leader && warp == kMmaWarp) {
+    // ================================================================ pair peer
+    // The even CTA issues every MMA; this warp relays the completion of this
+    // CTA's Q copies to the even CTA's q_full.
+    if (warp_wait(q_full, 0, abort, p.status, p.wait_cycles) && elect_one())
+      mbar_arrive_remote(lead_bar(q_full));
+    __syncwarp();
+  } else if ((!CTA2 || leader) && (warp == kMmaWarp || (NQT == 2 && warp == kMmaWarp1))) {
     // ================================================================ MMA issuers
     // One warp per query tile issues that tile's MMAs, so neither tile's
     // tensor work waits in line behind the other tile's softmax. Both read
     // the same K/V stages; a stage is released once both have committed.
     const int t = warp == kMmaWarp ? 0 : 1;
-    constexpr uint32_t kIdescS = idesc_f32acc(128, 128);  // f16 x f16 -> f32 (INT8 codes)
-    constexpr uint32_t kIdescO = idesc_f32acc(128, 128);  // e4m3 x e4m3 -> f32
+    // M = 256 rows (this CTA's tile t and the peer's) with pairs.
+    constexpr int kM = CTA2 ? 256 : 128;
+    constexpr uint32_t kIdescS = idesc_f32acc(kM, 128);  // f16 x f16 -> f32 (INT8 codes)
+    constexpr uint32_t kIdescO = idesc_f32acc(kM, 128);  // e4m3 x e4m3 -> f32
     // Descriptor low words of this tile's operand buffers (k slices add a
     // constant). The 64- and 128-byte swizzled layouts share the encoding.
     const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ + t * F::kTileBytes));
@@ -577,22 +655,39 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     // K-scale TMEM slot `sf_slot`.
     auto issue_s = [&](int stage, int half, int sf_slot) {
       if constexpr (FMT == 0) {
-        const uint32_t ka = k_lo + stage * 2048;
+        const uint32_t ka = k_lo + stage * (L::kKStage >> 4);
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-            mma_f16_ss_lo(d_s, q_lo + off, ka + off, kIdescS, k > 0);
+            // K slice k: 64-channel box k / 4 (the Q box is 16 KB, a K box
+            // holds the stage's 128, or with pairs 64, keys), 32 bytes each.
+            const uint32_t offq = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+            const uint32_t offk = ((k >> 2) * (L::kKStage / 2) + (k & 3) * 32) >> 4;
+            if constexpr (CTA2)
+              mma_f16_ss_lo_pair(d_s, q_lo + offq, ka + offk, kIdescS, k > 0);
+            else
+              mma_f16_ss_lo(d_s, q_lo + offq, ka + offk, kIdescS, k > 0);
           }
-          mma_commit(&s_full[t]);
+          if constexpr (CTA2)
+            mma_commit_pair(&s_full[t]);
+          else
+            mma_commit(&s_full[t]);
         }
       } else if constexpr (FMT == 2) {
         // E4M3 x E4M3 over K = 128: four K = 32 slices of the 128-byte rows.
-        const uint32_t ka = k_lo + stage * 1024;
+        const uint32_t ka = k_lo + stage * (L::kKStage >> 4);
         if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_f8_ss_lo(d_s, q_lo + k * 2, ka + k * 2, kIdescO, k > 0);
-          mma_commit(&s_full[t]);
+          for (int k = 0; k < 4; ++k) {
+            if constexpr (CTA2)
+              mma_f8_ss_lo_pair(d_s, q_lo + k * 2, ka + k * 2, kIdescO, k > 0);
+            else
+              mma_f8_ss_lo(d_s, q_lo + k * 2, ka + k * 2, kIdescO, k > 0);
+          }
+          if constexpr (CTA2)
+            mma_commit_pair(&s_full[t]);
+          else
+            mma_commit(&s_full[t]);
         }
       } else {
         // Keys 64h .. 64h+63 of the stage: B rows at +4096 bytes, their
@@ -639,29 +734,43 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
           mma_commit(&o_done[t * kPSlots + slot]);
         }
       } else {
-        const uint32_t pa = p_lo + pbuf * 1024, va = v_lo + stage * 1024;
+        // V^T stage: 128 (with pairs 64) channel rows of 128 keys.
+        const uint32_t pa = p_lo + pbuf * 1024, va = v_lo + stage * (L::kVStage >> 4);
         constexpr int kK = kStep / 32;  // K = 32 slices per step
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < kK; ++k) {
             const int kk = half * kK + k;
-            mma_f8_ss_lo(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+            if constexpr (CTA2)
+              mma_f8_ss_lo_pair(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+            else
+              mma_f8_ss_lo(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
           }
-          mma_commit(&o_done[t * kPSlots + slot]);
+          if constexpr (CTA2)
+            mma_commit_pair(&o_done[t * kPSlots + slot]);
+          else
+            mma_commit(&o_done[t * kPSlots + slot]);
         }
       }
       __syncwarp();
     };
+    // Commits of the ring stages and of the final barrier reach both CTAs of
+    // a pair (each CTA's producers and softmax wait on their own barriers).
     auto commit = [&](uint64_t* bar) {
-      if (elect_one()) mma_commit(bar);
+      if (elect_one()) {
+        if constexpr (CTA2)
+          mma_commit_pair(bar);
+        else
+          mma_commit(bar);
+      }
       __syncwarp();
     };
     // K ring position of the S steps (stage, parity of its fill round) and
     // V ring position of the P V steps; both advance after a tile's last step.
     int ks = 0, vs = 0;
     uint32_t kph = 0, vph = 0;
-    bool ok = warp_wait(q_full, 0, abort, p.status, p.wait_cycles);
-    if (ok) ok = warp_wait(&k_full[0], 0, abort, p.status, p.wait_cycles);
+    bool ok = warp_wait<CTA2>(q_full, 0, abort, p.status, p.wait_cycles);
+    if (ok) ok = warp_wait<CTA2>(&k_full[0], 0, abort, p.status, p.wait_cycles);
     tc_fence_after();
     if (ok) {
       if constexpr (kMx) {
@@ -683,10 +792,12 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       if (v < nsteps) {
         const int hv = v & (kSteps - 1);
         if (hv == 0) {
-          if (!(ok = warp_wait(&k_full[ks], kph, abort, p.status, p.wait_cycles))) break;
+          if (!(ok = warp_wait<CTA2>(&k_full[ks], kph, abort, p.status, p.wait_cycles))) break;
           tc_fence_after();
         }
-        if (!(ok = warp_wait(&s_free[t], static_cast<uint32_t>(u) & 1u, abort, p.status, p.wait_cycles))) break;
+        if (!(ok = warp_wait<CTA2>(&s_free[t], static_cast<uint32_t>(u) & 1u, abort, p.status,
+                                   p.wait_cycles)))
+          break;
         tc_fence_after();
         const int sf_slot = (v / kSteps) & 1;
         if constexpr (kMx) {
@@ -701,11 +812,12 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       const int hu = u & (kSteps - 1);
       const int slot = u & (kPSlots - 1);
       if (hu == 0) {
-        if (!(ok = warp_wait(&v_full[vs], vph, abort, p.status, p.wait_cycles))) break;
+        if (!(ok = warp_wait<CTA2>(&v_full[vs], vph, abort, p.status, p.wait_cycles))) break;
         tc_fence_after();
       }
-      if (!(ok = warp_wait(&p_full[t * kPSlots + slot],
-                           static_cast<uint32_t>(u >> kPSlotShift) & 1u, abort, p.status, p.wait_cycles)))
+      if (!(ok = warp_wait<CTA2>(&p_full[t * kPSlots + slot],
+                                 static_cast<uint32_t>(u >> kPSlotShift) & 1u, abort, p.status,
+                                 p.wait_cycles)))
         break;
       tc_fence_after();
       issue_pv(slot, vs, hu, (u / kSteps) & 1, u > 0);
@@ -722,6 +834,22 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
       if constexpr (kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
     // ================================================================ softmax
     const int t = warp / 4;
+    // Step handshakes with the MMA warp: every thread arrives, or with pairs
+    // one lane per warp (after the warp's own accesses, ordered before it by
+    // __syncwarp) on the even CTA's barrier.
+    auto step_arrive = [&](uint64_t* bar) {
+      if constexpr (CTA2) {
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(bar);
+          else
+            mbar_arrive_remote(lead_bar(bar));
+        }
+      } else {
+        mbar_arrive(bar);
+      }
+    };
     const int r = static_cast<int>(threadIdx.x & 127);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + lane_base + TM::s(t);
@@ -774,7 +902,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         for (int i = 0; i < kStep; ++i) s[i] = __uint_as_float(v[i]);
       }
       tc_fence_before();
-      mbar_arrive(&s_free[t]);
+      step_arrive(&s_free[t]);
 
       // Kept strictly positive, so that a masked score (-inf) gives x = -inf
       // and p = 0 with no per-element test in the exponential loop. A zero
@@ -919,7 +1047,7 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&p_full[t * kPSlots + slot]);
+      step_arrive(&p_full[t * kPSlots + slot]);
     }
 
     // ---- epilogue
@@ -1018,10 +1146,19 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // Pairs: the even CTA's MMAs (which write this CTA's tensor memory and read
+  // its shared memory) are complete and neither CTA signals the other any
+  // more once both have reached this barrier.
+  if constexpr (CTA2)
+    cluster_sync();
+  else
+    __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tbase, TM::kCols);
+    if constexpr (CTA2)
+      tmem_dealloc_pair(tbase, TM::kCols);
+    else
+      tmem_dealloc(tbase, TM::kCols);
   } else if (warp == kTmaWarp && p.o_tma && !*abort) {
     // Store the staged O tiles (rows past Nq are clipped by the tensor map).
     if (elect_one()) {
@@ -1085,12 +1222,12 @@ bool make_map_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int es
   return encode_tiled(m, dt, 2, ptr, dims, strides, box, swizzle);
 }
 
-template <int FMT, int NQT, int STAGES, bool DS = false>
+template <int FMT, int NQT, int STAGES, bool DS = false, bool CTA2 = false>
 cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mo, const AttnParams& p, cudaStream_t stream) {
-  using L = SmemLayout<FMT, NQT, STAGES>;
+  using L = SmemLayout<FMT, NQT, STAGES, CTA2>;
   static_assert(L::kDynamic <= 232448, "shared memory budget");
-  constexpr auto kern = sage_attn_kernel<FMT, NQT, STAGES, DS>;
+  constexpr auto kern = sage_attn_kernel<FMT, NQT, STAGES, DS, CTA2>;
   cudaError_t e = once_per_device<kern>([]() {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
     if (r != cudaSuccess) return r;
@@ -1104,15 +1241,49 @@ cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const C
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((p.nbq + NQT - 1) / NQT), static_cast<unsigned>(p.H),
+  const unsigned ctas_x = static_cast<unsigned>((p.nbq + NQT - 1) / NQT);
+  dim3 grid(CTA2 ? (ctas_x + 1) / 2 * 2 : ctas_x, static_cast<unsigned>(p.H),
             static_cast<unsigned>(p.B * p.num_splits));
-  kern<<<grid, attn_threads<NQT>(), L::kDynamic, stream>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError();
+  if constexpr (CTA2) {
+    // Clusters of two CTAs along x (an even grid: a last CTA past the query
+    // tiles computes rows that are not stored).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(attn_threads<NQT>());
+    cfg.dynamicSmemBytes = L::kDynamic;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p);
+  } else {
+    kern<<<grid, attn_threads<NQT>(), L::kDynamic, stream>>>(mq, mk, mv, mo, p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
 int attn_q_tiles_per_cta(int64_t nbq) { return nbq >= 2 ? 2 : 1; }
+
+bool attn_cta2_supported(int fmt, int64_t Nq, bool delta_s) {
+  return (fmt == 0 || fmt == 2) && !delta_s && attn_q_tiles_per_cta(pad128(Nq) / 128) == 2;
+}
+
+// The library's choice between 1-CTA and 2-CTA tiles, from measurement on
+// GB300 (every configuration timed both ways): 1-CTA tiles everywhere.
+bool attn_prefer_cta2(int fmt, int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
+  (void)fmt;
+  (void)B;
+  (void)H;
+  (void)Nq;
+  (void)Nk;
+  return false;
+}
 
 int attn_auto_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
   const int64_t nbq = pad128(Nq) / 128, nkv = pad128(Nk) / 128;
@@ -1132,15 +1303,19 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   const uint64_t k_rows = static_cast<uint64_t>(a.p.B * a.p.H * Nk_pad);
   CUtensorMap mq, mk, mv;
   bool maps_ok;
+  // 2-CTA tiles: each CTA of a pair loads 64 keys of a K tile and 64
+  // channels of a V^T tile (64-row boxes).
+  const bool cta2 = a.cta2 != 0;
+  const uint32_t kv_rows = cta2 ? 64 : 128;
   if (a.fmt == 0)  // FP16-held INT8 codes: 128-byte boxes of 64 channels
     maps_ok = make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128, q_rows, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128, k_rows, 64, 128,
+              make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 128, k_rows, 64, kv_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   else if (a.fmt == 2)  // E4M3 codes: one 128-byte row per token
     maps_ok = make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, q_rows, 128, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, k_rows, 128, 128,
+              make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, k_rows, 128, kv_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   else  // packed E2M1: one 64-byte row per token
     maps_ok = make_map_2d(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, q_rows, 64, 128,
@@ -1155,7 +1330,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
                                  static_cast<uint64_t>(Nk_pad / 2), v_rows, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_64B)
                    : make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                                 static_cast<uint64_t>(Nk_pad), v_rows, 128, 128,
+                                 static_cast<uint64_t>(Nk_pad), v_rows, 128, kv_rows,
                                  CU_TENSOR_MAP_SWIZZLE_128B)))
     return cudaErrorInvalidValue;
   // O through a 4-D map over the caller's [B][Nq][H][D] strides (boxes of
@@ -1177,15 +1352,18 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   }
   if (!p.o_tma) mo = mv;  // unused by the kernel
   const bool two = attn_q_tiles_per_cta(p.nbq) == 2;
+  if (cta2 && (!two || p.delta_s || (a.fmt != 0 && a.fmt != 2))) return cudaErrorInvalidValue;
   cudaError_t e;
   if (a.fmt == 0)
     e = p.delta_s ? (two ? launch_variant<0, 2, 2, true>(mq, mk, mv, mo, p, stream)
                          : launch_variant<0, 1, 3, true>(mq, mk, mv, mo, p, stream))
-                  : (two ? launch_variant<0, 2, 2>(mq, mk, mv, mo, p, stream)
-                         : launch_variant<0, 1, 3>(mq, mk, mv, mo, p, stream));
+                  : (cta2  ? launch_variant<0, 2, 4, false, true>(mq, mk, mv, mo, p, stream)
+                     : two ? launch_variant<0, 2, 2>(mq, mk, mv, mo, p, stream)
+                           : launch_variant<0, 1, 3>(mq, mk, mv, mo, p, stream));
   else if (a.fmt == 2)
-    e = two ? launch_variant<2, 2, 4>(mq, mk, mv, mo, p, stream)
-            : launch_variant<2, 1, 4>(mq, mk, mv, mo, p, stream);
+    e = cta2  ? launch_variant<2, 2, 4, false, true>(mq, mk, mv, mo, p, stream)
+        : two ? launch_variant<2, 2, 4>(mq, mk, mv, mo, p, stream)
+              : launch_variant<2, 1, 4>(mq, mk, mv, mo, p, stream);
   else if (a.fmt == 4)
     e = two ? launch_variant<4, 2, 4>(mq, mk, mv, mo, p, stream)
             : launch_variant<4, 1, 4>(mq, mk, mv, mo, p, stream);

@@ -34,6 +34,8 @@ struct AttnParams {
 
 struct AttnLaunch {
   int fmt;        // 0: INT8 Q/K, 1: MXFP4 Q/K, 2: FP8 E4M3 Q/K, 4: MXFP4 Q/K, V and P
+  int cta2;       // 1: 2-CTA tiles (cta_group::2, clusters of two CTAs; INT8 / FP8, two
+                  // query tiles per CTA, no dS)
   const void* q;  // INT8: FP16-held codes [B][H][Nq_pad][128]; MXFP4: packed E2M1 [B][H][Nq_pad][64]
   const void* k;  // same layout with Nk_pad
   const void* v;  // FP8 [B][H][128][Nk_pad]
@@ -41,6 +43,9 @@ struct AttnLaunch {
 };
 
 int attn_q_tiles_per_cta(int64_t nbq);
+// 2-CTA tiles for this shape and format (measured choice; see attention.cu).
+bool attn_prefer_cta2(int fmt, int64_t B, int64_t H, int64_t Nq, int64_t Nk);
+bool attn_cta2_supported(int fmt, int64_t Nq, bool delta_s);
 int attn_auto_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk);
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);
 

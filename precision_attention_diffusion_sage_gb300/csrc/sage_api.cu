@@ -301,6 +301,14 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
     return SAGE_ERR_INVALID_ARG;
   const int req = opts ? opts->num_splits : 0;
   if (req < 0 || req > 64) return SAGE_ERR_INVALID_ARG;
+  const int cta_mode = opts ? opts->cta_mode : 0;
+  if (cta_mode < 0 || cta_mode > 2) return SAGE_ERR_INVALID_ARG;
+  const int kfmt = fmt == SAGE_FMT_QK_MXFP4_V_MXFP4 ? 4
+                   : mx_qk(fmt)                   ? 1
+                   : fmt == SAGE_FMT_QK_FP8_V_FP8 ? 2
+                                                  : 0;
+  if (cta_mode == 2 && !attn_cta2_supported(kfmt, Nq, delta_s != nullptr))
+    return SAGE_ERR_UNSUPPORTED;
   const int64_t wait_cycles = opts ? opts->wait_cycles : 0;
   const int withhold_v = opts ? opts->test_withhold_v : 0;
   if (wait_cycles < 0 || wait_cycles > (int64_t{1} << 31) || (opts && opts->reserved != 0) ||
@@ -317,7 +325,9 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
   const bool mx = mx_qk(fmt);
   const bool v4 = fmt == SAGE_FMT_QK_MXFP4_V_MXFP4;
   AttnLaunch a;
-  a.fmt = v4 ? 4 : (mx ? 1 : (fmt == SAGE_FMT_QK_FP8_V_FP8 ? 2 : 0));
+  a.fmt = kfmt;
+  a.cta2 = cta_mode == 2 || (cta_mode == 0 && attn_cta2_supported(kfmt, Nq, delta_s != nullptr) &&
+                             attn_prefer_cta2(kfmt, B, H, Nq, Nk));
   a.q = q_q;
   a.k = k_q;
   a.v = v_q;

@@ -263,6 +263,88 @@ def test_bounded_wait_runs_out_and_next_call_is_clean():
     assert_attention_close(o, lse, ro, rl)
 
 
+# ------------------------------------------------------------------ 2-CTA tiles
+# cta_mode 2: clusters of two CTAs run cta_group::2 MMAs of M = 256 rows, each
+# CTA staging half of every K and V tile. Compared with the oracle and with
+# the 1-CTA kernel (cta_mode 1) on the same quantized operands: odd numbers
+# of query-tile pairs (a padding CTA), ragged tails, per-batch key lengths
+# including 0, forced KV splits and K smoothing.
+@pytest.mark.parametrize("fmt", [0, 2])
+@pytest.mark.parametrize("B,Nq,Nk,lens,splits", [(1, 256, 256, None, 0), (1, 129, 128, None, 0),
+                                                 (1, 300, 333, None, 0),
+                                                 (2, 513, 1000, [1000, 77], 0),
+                                                 (2, 640, 1000, [0, 999], 3)])
+def test_attention_cta2_matches_oracle_and_1cta(fmt, B, Nq, Nk, lens, splits):
+    w, q, k, v = _small(B, 2, Nq, Nk, seed=200 + Nq + fmt, structure="k_offset_std2")
+    qq, qs = binding.sage_quantize_qk(q, fmt)
+    kq, ks = binding.sage_quantize_qk(k, fmt, lens=lens)
+    vq, vs = binding.sage_quantize_v(v, lens=lens)
+    outs = {}
+    for mode in (1, 2):
+        outs[mode] = binding.sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=lens,
+                                           num_splits=splits, cta_mode=mode)
+        torch.cuda.synchronize()
+        assert binding.sage_last_device_status() == 0
+    qz, kz, vz = oracle_quantize(fmt, q, k, v, k_lens=lens)
+    ro, rl = _oracle_attention(fmt, qz, kz, vz, Nq, Nk, k_lens=lens)
+    for mode in (1, 2):
+        assert_attention_close(*outs[mode], ro, rl)
+    (o1, l1), (o2, l2) = outs[1], outs[2]
+    assert float((o1.float() - o2.float()).abs().max()) <= 1e-2
+    fin = torch.isfinite(l1)
+    assert torch.equal(fin, torch.isfinite(l2))
+    assert float((l1[fin] - l2[fin]).abs().max()) <= 1e-4 if fin.any() else True
+
+
+def test_attention_cta2_k_smooth():
+    w = Workload("case", 1, 2, 384, 700, seed=210, structure="k_mean")
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    qq, qs = binding.sage_quantize_qk(q, 0)
+    kq, ks, km = binding.sage_quantize_k_smooth(k)
+    vq, vs = binding.sage_quantize_v(v)
+    o, lse = binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=384, Nk=700, k_mean=km,
+                                   cta_mode=2)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    qz = oracle.quantize_int8(bf16_bits(q))
+    rq, rs, rm = oracle.quantize_int8_smooth(bf16_bits(k))
+    vz = oracle.quantize_v_fp8(bf16_bits(v))
+    ro, rl, _ = oracle.attention(0, *qz, rq, rs, *vz, Nq=384, Nk=700, k_mean=rm)
+    assert_attention_close(o, lse, ro, rl)
+
+
+def test_attention_cta2_rejects_unsupported():
+    w, q, k, v = _small(1, 1, 128, 256, seed=211)
+    qq, qs = binding.sage_quantize_qk(q, 0)
+    kq, ks = binding.sage_quantize_qk(k, 0)
+    vq, vs = binding.sage_quantize_v(v)
+    with pytest.raises(binding.SageError):  # one query tile: no pair of tiles per CTA
+        binding.sage_attn_fwd(0, qq, qs, kq, ks, vq, vs, Nq=128, Nk=256, cta_mode=2)
+    w, q, k, v = _small(1, 1, 256, 256, seed=212)
+    mq, ms = binding.sage_quantize_qk(q, 1)
+    mk, mks = binding.sage_quantize_qk(k, 1)
+    vq, vs = binding.sage_quantize_v(v)
+    with pytest.raises(binding.SageError):  # MXFP4 Q/K
+        binding.sage_attn_fwd(1, mq, ms, mk, mks, vq, vs, Nq=256, Nk=256, cta_mode=2)
+
+
+@pytest.mark.parametrize("name,heads", [("video_dit", [0, 39]), ("long_video", [17]),
+                                        ("image_dit_fp8", [0, 23])])
+def test_full_size_workload_cta2(name, heads):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    (qq, qs), (kq, ks), (vq, vs) = binding.sage_quantize_qkv(q, k, v, w.fmt)
+    o, lse = binding.sage_attn_fwd(w.fmt, qq, qs, kq, ks, vq, vs, Nq=w.Nq, Nk=w.Nk, cta_mode=2)
+    torch.cuda.synchronize()
+    assert binding.sage_last_device_status() == 0
+    del qq, kq, vq
+    sub = lambda t: t[:, :, heads]  # noqa: E731  head slice of [B, N, H, D]
+    qz, kz, vz = oracle_quantize(w.fmt, sub(q), sub(k), sub(v))
+    rows = _tile_rows(w.Nq, salt=29)
+    ro, rl = _oracle_attention(w.fmt, qz, kz, vz, w.Nq, w.Nk, rows=rows)
+    assert_attention_close(o[:, :, heads], lse[:, heads], ro, rl, rows=rows)
+
+
 # ------------------------------------------------------------------ full-size workloads
 # Every full-size test compares the quantized tensors and scales of every
 # batch and head bit for bit, and attention on one query row of every 128-row

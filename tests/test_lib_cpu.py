@@ -125,6 +125,25 @@ def test_wait_bound_options_validated_before_launch():
     assert call(reserved=1) == -1
 
 
+def test_cta_mode_validated_before_launch():
+    """cta_mode: 0, 1 or 2; 2-CTA tiles only for INT8 / FP8 Q/K with more
+    than one query tile and no dS."""
+    lib = binding.library()
+    S = binding.Strides(0, 0, 0)
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(fmt, mode, Nq=256, ds=None):
+        opts = binding.AttnOptions(1, mode, None, ds)
+        return lib.sage_attn_fwd(fmt, fake, fake, fake, fake, fake, fake, None, 1, 1, Nq, 256, 128,
+                                 -1.0, 0, fake, S, None, None, 0, ctypes.byref(opts), None)
+
+    assert call(0, 3) == -1 and call(0, -1) == -1
+    assert call(1, 2) == -2                 # MXFP4 Q/K
+    assert call(4, 2) == -2                 # MXFP4 Q/K, V and P
+    assert call(0, 2, Nq=128) == -2         # one query tile
+    assert call(0, 2, ds=1 << 20) == -2     # Q smoothing's dS
+
+
 def test_status_strings():
     lib = binding.library()
     for code in range(-7, 1):
