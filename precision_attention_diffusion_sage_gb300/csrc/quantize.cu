@@ -150,6 +150,18 @@ __device__ __forceinline__ uint32_t e4m3x2_fast(float x0, float x1, float inv, b
   return clo;
 }
 
+// Four E4M3 codes in a word (byte i = element i): a.x, a.y, b.x, b.y.
+__device__ __forceinline__ uint32_t e4m3x4w(float2 a, float2 b) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      " mov.b32 %0, {lo, hi};\n}\n"
+      : "=r"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // E4M3 codes of eight BF16 values (one row chunk) at scale s > 0, inv = 1/s,
 // eight bytes (element i in byte i): the codes of the IEEE binary32 quotients
 // x / s, exact as in e4m3x2_fast (the rare bracketed pairs, or a subnormal
@@ -1163,9 +1175,11 @@ constexpr int kVStages = 2;
 // warps then store as 128-byte token-contiguous rows of V^T.
 __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
     const __grid_constant__ CUtensorMap tmV, QuantVArgs a) {
-  constexpr int kPitchWords = 33;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint32_t tileT[128 * kPitchWords];
+  // Transposed block: 128 channel rows of 32 words (128 tokens); the 4-word
+  // groups of row d are XOR-swizzled by (d / 8) % 8, so that the transposing
+  // word stores and the 16-byte row reads both spread over the banks.
+  __shared__ __align__(16) uint32_t tileT[128 * 32];
   __shared__ float sv[128], sinv[128];
   __shared__ int abort_flag;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -1194,10 +1208,12 @@ __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
     const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
     const uint8_t* tile = ring.stage(k);
     float s8[8], inv8[8];
+    bool inv_bad = false;  // a subnormal scale whose reciprocal overflows
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       s8[q] = sv[cg * 8 + q];
       inv8[q] = sinv[cg * 8 + q];
+      inv_bad |= s8[q] > 0.0f && !(inv8[q] < INFINITY);
     }
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
@@ -1209,33 +1225,46 @@ __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
         if (c.blk * 128 + t0 + u >= nv) raw = make_uint4(0, 0, 0, 0);
         unpack8(raw, f[u]);
       }
+      // Four tokens of each channel per word: the codes of r = x * (1/s) shrunk
+      // and grown by 2^-21 (packed products); when the two words differ, some
+      // quotient brackets a rounding boundary and the exact divisions decide
+      // (as in e4m3x2_fast). A zero scale (all-zero channel) gives zero codes.
+      const float2 dn = make_float2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
+      const float2 up = make_float2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
       uint32_t w[8];
-      uint32_t redo = 0;
+      bool redo = inv_bad;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        bool e0 = false, e1 = false;
-        const uint32_t lo = e4m3x2_fast(f[0][q], f[1][q], inv8[q], e0);
-        const uint32_t hi = e4m3x2_fast(f[2][q], f[3][q], inv8[q], e1);
-        w[q] = s8[q] > 0.0f ? (lo | (hi << 16)) : 0u;
-        redo |= static_cast<uint32_t>(s8[q] > 0.0f && (e0 || e1 || !(inv8[q] < INFINITY))) << q;
+        const float2 iv = make_float2(inv8[q], inv8[q]);
+        const float2 r01 = __fmul2_rn(make_float2(f[0][q], f[1][q]), iv);
+        const float2 r23 = __fmul2_rn(make_float2(f[2][q], f[3][q]), iv);
+        const uint32_t clo = e4m3x4w(__fmul2_rn(r01, dn), __fmul2_rn(r23, dn));
+        const uint32_t chi = e4m3x4w(__fmul2_rn(r01, up), __fmul2_rn(r23, up));
+        redo |= clo != chi;
+        w[q] = s8[q] > 0.0f ? clo : 0u;
       }
-      if (redo) {  // rare: pairs near an E4M3 rounding boundary
+      if (redo) {  // rare: quotients near an E4M3 rounding boundary
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          if ((redo >> q) & 1)
+          if (s8[q] > 0.0f)
             w[q] = e4m3x2(__fdiv_rn(f[0][q], s8[q]), __fdiv_rn(f[1][q], s8[q])) |
                    (e4m3x2(__fdiv_rn(f[2][q], s8[q]), __fdiv_rn(f[3][q], s8[q])) << 16);
       }
+      const int tw = t0 / 4;  // word (4 tokens) of the channel rows
 #pragma unroll
-      for (int q = 0; q < 8; ++q) tileT[(cg * 8 + q) * kPitchWords + t0 / 4] = w[q];
+      for (int q = 0; q < 8; ++q) {
+        const int d = cg * 8 + q;
+        tileT[d * 32 + ((((tw >> 2) ^ (d >> 3)) & 7) << 2) + (tw & 3)] = w[q];
+      }
     }
     __syncthreads();
+    // 16-byte pieces of the V^T rows: 8 per channel row, 128 bytes per row.
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int wi = threadIdx.x + 256 * j;
-      const int d = wi >> 5, tw = wi & 31;
-      reinterpret_cast<uint32_t*>(a.out + (bh * 128 + d) * Np + c.blk * 128)[tw] =
-          tileT[d * kPitchWords + tw];
+    for (int j = 0; j < 4; ++j) {
+      const int ci = static_cast<int>(threadIdx.x) + 256 * j;
+      const int d = ci >> 3, g = ci & 7;
+      const uint4 v4 = *reinterpret_cast<const uint4*>(&tileT[d * 32 + ((g ^ (d >> 3)) & 7) * 4]);
+      *reinterpret_cast<uint4*>(a.out + (bh * 128 + d) * Np + c.blk * 128 + g * 16) = v4;
     }
     __syncthreads();  // stage, tileT and sv free again
   }
