@@ -358,7 +358,7 @@ def main():
         vq = torch.empty((B, H, D, Nkp // 2), dtype=torch.uint8, device=dev)
         vs = torch.empty((B, H, Nkp // 128, D, 4), dtype=torch.uint8, device=dev)
     else:
-        vq = torch.empty((B, H, D, Nkp), dtype=torch.uint8, device=dev)
+        vq = torch.empty((B, H, Nkp, D), dtype=torch.uint8, device=dev)
         vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
     vws = torch.empty(max(16, binding.sage_workspace_bytes(1, fmt, B, H, Nk, Nk)), dtype=torch.uint8,
                       device=dev)

@@ -103,7 +103,9 @@ typedef struct {
  *   data  : [B][H][Npad][D] FP8 E4M3 codes (one byte each).
  *   scale : [B][H][Npad/128] float, absmax/448 of each 128-token block.
  * V (formats 0-3):
- *   data  : [B][H][D][Npad] FP8 E4M3 codes, token-contiguous (V transposed).
+ *   data  : [B][H][Npad][D] FP8 E4M3 codes, channel-contiguous (the layout of
+ *           V itself; the attention kernel reads each 128-token tile as an
+ *           MN-major operand of its P V MMA).
  *   scale : [B][H][D] float, absmax/448 of each channel over valid tokens.
  * V (SAGE_FMT_QK_MXFP4_V_MXFP4, from sage_quantize_v_mxfp4):
  *   data  : [B][H][D][Npad/2] bytes of packed E2M1 codes, token-contiguous,
@@ -158,7 +160,7 @@ sage_status_t sage_quantize_v_mxfp4(const void* v, sage_strides_t vs, int64_t B,
 /* Quantize V to FP8 E4M3 ("new MHA v4 entrypoint": sage_quant_v_amax_partial,
  * sage_quant_v_amax_finalize and sage_quant_v kernels; reading: one FP32
  * scale absmax/448 per (b,h,channel) over valid tokens, codes E4M3 with round
- * to nearest even and saturation, written token-contiguous).
+ * to nearest even and saturation, written [B][H][Npad][D]).
  * A clear of the workspace, then two launches: channel maxima of every
  * 128-token block folded into `workspace`, then finalize + quantize.
  *   workspace : device scratch of at least sage_workspace_bytes(1, ...) bytes,

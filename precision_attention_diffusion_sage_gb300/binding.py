@@ -176,11 +176,11 @@ def sage_quantize_qk(x: torch.Tensor, fmt: int = FMT_INT8, lens=None,
 def sage_quantize_v(v: torch.Tensor, lens=None, out: Optional[torch.Tensor] = None,
                     scale: Optional[torch.Tensor] = None,
                     workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Quantize BF16 V ``[B, N, H, D]`` to FP8 E4M3 ``[B, H, D, Npad]`` (uint8) + scales."""
+    """Quantize BF16 V ``[B, N, H, D]`` to FP8 E4M3 ``[B, H, Npad, D]`` (uint8) + scales."""
     B, N, H, D = v.shape
     Np = pad128(N)
     if out is None:
-        out = torch.empty((B, H, D, Np), dtype=torch.uint8, device=v.device)
+        out = torch.empty((B, H, Np, D), dtype=torch.uint8, device=v.device)
     if scale is None:
         scale = torch.empty((B, H, D), dtype=torch.float32, device=v.device)
     need = sage_workspace_bytes(1, FMT_INT8, B, H, N, N, D)
@@ -235,7 +235,7 @@ def sage_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: in
             vq = torch.empty((B, H, D, pad128(Nk) // 2), dtype=torch.uint8, device=dev)
             vs = torch.empty((B, H, pad128(Nk) // 128, D, 4), dtype=torch.uint8, device=dev)
         else:
-            vq = torch.empty((B, H, D, pad128(Nk)), dtype=torch.uint8, device=dev)
+            vq = torch.empty((B, H, pad128(Nk), D), dtype=torch.uint8, device=dev)
             vs = torch.empty((B, H, D), dtype=torch.float32, device=dev)
     else:
         (qq, qs), (kq, ks), (vq, vs) = outs

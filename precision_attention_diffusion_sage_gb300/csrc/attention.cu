@@ -31,7 +31,8 @@
 // kHeadroom; O and l are then rescaled by the exact power of two
 // 2^(m_old - m_new). P8 = E4M3(2^(t - m + 8 - kHeadroom)) goes to a
 // double-buffered 128-byte-swizzled K-major tile in shared memory and
-// O += P8 * V8^T runs as kind::f8f6f4. Epilogue: O * s_v / l -> BF16,
+// O += P8 * V8 runs as kind::f8f6f4 with the V tile token-major (an
+// MN-major B operand: channels contiguous). Epilogue: O * s_v / l -> BF16,
 // LSE = (m + log2 l - 8 + kHeadroom) ln 2 (l is kept in P8 units).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -101,8 +102,8 @@ struct SmemLayout {
   static constexpr int kPSlots = 2 * (128 / F::kStep);  // P slots per query tile
   static constexpr int kQ = 0;                             // NQT Q tiles
   static constexpr int kK = kQ + NQT * F::kTileBytes;      // STAGES K tiles
-  static constexpr int kVTile = FMT == 4 ? 8192 : 16384;  // V^T 128x128: E2M1 or E4M3
-  // A CTA pair holds half of each K tile (64 keys) and of each V^T tile (64
+  static constexpr int kVTile = FMT == 4 ? 8192 : 16384;  // V 128x128: E2M1 V^T or E4M3 V
+  // A CTA pair holds half of each K tile (64 keys) and of each V tile (64
   // channels) in each CTA.
   static constexpr int kKStage = CTA2 ? F::kTileBytes / 2 : F::kTileBytes;
   static constexpr int kVStage = CTA2 ? kVTile / 2 : kVTile;
@@ -305,7 +306,7 @@ __host__ __device__ constexpr bool attn_split_regs() { return !is_mx<FMT>() && N
 // 2c + 1, on an SM pair); the even CTA's MMA warps issue cta_group::2 MMAs of
 // M = 256 rows (its tile t and its peer's tile t) for both. Each CTA loads
 // its own Q tiles, keys 64r .. 64r + 63 of every K tile and channels 64r ..
-// 64r + 63 of every V^T tile (r = its rank in the pair), so each CTA stages
+// 64r + 63 of every V tile (r = its rank in the pair), so each CTA stages
 // half of the K/V bytes of the 1-CTA kernel; the peer's copies complete on
 // the even CTA's barriers, and the peer's softmax warps arrive there too.
 // Everything else (softmax, epilogue) runs in each CTA on its own rows.
@@ -598,17 +599,21 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
         __syncwarp();
       }
       if (elect_one()) {
+        // E4M3 V: 128 token rows of 128 channel bytes (token-major; with pairs
+        // this CTA's 64 channels, completing on the even CTA's barrier).
+        // Format 4: E2M1 V^T rows of Nk_pad / 2 bytes.
+        const int yv = static_cast<int>(bh * Nk_pad) + (j0 + it) * 128;
         if constexpr (CTA2) {
-          // This CTA's 64 channels of the V^T tile, completing on the even
-          // CTA's barrier.
           if (leader) mbar_arrive_expect_tx(&v_full[s], 2 * L::kVStage);
-          tma_load_2d_pair(sV + s * L::kVStage, &tmV, lead_bar(&v_full[s]), (j0 + it) * 128,
-                           static_cast<int>(bh * 128) + 64 * static_cast<int>(rank));
+          tma_load_2d_pair(sV + s * L::kVStage, &tmV, lead_bar(&v_full[s]),
+                           64 * static_cast<int>(rank), yv);
+        } else if constexpr (FMT == 4) {
+          mbar_arrive_expect_tx(&v_full[s], L::kVTile);
+          tma_load_2d(sV + s * L::kVTile, &tmV, &v_full[s], (j0 + it) * 64,
+                      static_cast<int>(bh * 128));
         } else {
           mbar_arrive_expect_tx(&v_full[s], L::kVTile);
-          // E4M3 V^T rows of Nk_pad bytes, or E2M1 rows of Nk_pad / 2 bytes.
-          tma_load_2d(sV + s * L::kVTile, &tmV, &v_full[s], (j0 + it) * (FMT == 4 ? 64 : 128),
-                      static_cast<int>(bh * 128));
+          tma_load_2d(sV + s * L::kVTile, &tmV, &v_full[s], 0, yv);
         }
       }
       __syncwarp();
@@ -641,6 +646,9 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
     constexpr int kM = CTA2 ? 256 : 128;
     constexpr uint32_t kIdescS = idesc_f32acc(kM, 128);  // f16 x f16 -> f32 (INT8 codes)
     constexpr uint32_t kIdescO = idesc_f32acc(kM, 128);  // e4m3 x e4m3 -> f32
+    // P V: B = the V tile, token-major in shared memory (channels contiguous):
+    // an MN-major operand.
+    constexpr uint32_t kIdescPV = idesc_f32acc(kM, 128, true);
     // Descriptor low words of this tile's operand buffers (k slices add a
     // constant). The 64- and 128-byte swizzled layouts share the encoding.
     const uint32_t q_lo = sw128_desc_lo(smem_u32(sQ + t * F::kTileBytes));
@@ -734,17 +742,22 @@ __global__ void __launch_bounds__(attn_threads<NQT>(), 1)
           mma_commit(&o_done[t * kPSlots + slot]);
         }
       } else {
-        // V^T stage: 128 (with pairs 64) channel rows of 128 keys.
+        // V stage: 128 token rows of 128 channel bytes in the 128-byte
+        // swizzled layout (with pairs 64 channel bytes, 64-byte swizzle); the
+        // K = 32 slice kk of P's keys is V's rows 32 kk .. 32 kk + 31.
         const uint32_t pa = p_lo + pbuf * 1024, va = v_lo + stage * (L::kVStage >> 4);
+        constexpr uint32_t kVSliceStep = (32 * (CTA2 ? 64 : 128)) >> 4;
         constexpr int kK = kStep / 32;  // K = 32 slices per step
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < kK; ++k) {
             const int kk = half * kK + k;
             if constexpr (CTA2)
-              mma_f8_ss_lo_pair(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+              mma_f8_ss_lo_pair<kSw64DescHi>(d_o, pa + kk * 2, va + kk * kVSliceStep, kIdescPV,
+                                             (acc || k > 0) ? 1u : 0u);
             else
-              mma_f8_ss_lo(d_o, pa + kk * 2, va + kk * 2, kIdescO, (acc || k > 0) ? 1u : 0u);
+              mma_f8_ss_lo(d_o, pa + kk * 2, va + kk * kVSliceStep, kIdescPV,
+                           (acc || k > 0) ? 1u : 0u);
           }
           if constexpr (CTA2)
             mma_commit_pair(&o_done[t * kPSlots + slot]);
@@ -1304,7 +1317,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   bool maps_ok;
   // 2-CTA tiles: each CTA of a pair loads 64 keys of a K tile and 64
-  // channels of a V^T tile (64-row boxes).
+  // channels of a V tile (64-row K boxes, 64-byte V boxes).
   const bool cta2 = a.cta2 != 0;
   const uint32_t kv_rows = cta2 ? 64 : 128;
   if (a.fmt == 0)  // FP16-held INT8 codes: 128-byte boxes of 64 channels
@@ -1322,16 +1335,18 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
                           CU_TENSOR_MAP_SWIZZLE_64B) &&
               make_map_2d(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, k_rows, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_64B);
-  // V^T: E4M3 rows of Nk_pad bytes (128-byte boxes), or for format 4 packed
-  // E2M1 rows of Nk_pad / 2 bytes (64-byte boxes, the layout of a K tile).
-  const uint64_t v_rows = static_cast<uint64_t>(a.p.B * a.p.H * 128);
+  // E4M3 V: token rows of 128 channel bytes, like an FP8 K tile (128-byte
+  // boxes; with pairs 64-byte boxes of one CTA's channels, 64-byte swizzle).
+  // Format 4: packed E2M1 V^T rows of Nk_pad / 2 bytes (64-byte boxes, the
+  // layout of a K tile).
   if (!maps_ok ||
       !(a.fmt == 4 ? make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                                 static_cast<uint64_t>(Nk_pad / 2), v_rows, 64, 128,
+                                 static_cast<uint64_t>(Nk_pad / 2),
+                                 static_cast<uint64_t>(a.p.B * a.p.H * 128), 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_64B)
-                   : make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                                 static_cast<uint64_t>(Nk_pad), v_rows, 128, kv_rows,
-                                 CU_TENSOR_MAP_SWIZZLE_128B)))
+                   : make_map_2d(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, k_rows,
+                                 cta2 ? 64 : 128, 128,
+                                 cta2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)))
     return cudaErrorInvalidValue;
   // O through a 4-D map over the caller's [B][Nq][H][D] strides (boxes of
   // 128 rows x 64 channels); the kernel falls back to direct stores when the

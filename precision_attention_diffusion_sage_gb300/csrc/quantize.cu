@@ -4,11 +4,11 @@
 // combined with an integer atomic maximum, then finalize + quantize).
 //
 // The codes are the IEEE binary32 quotient x / s rounded (to an integer, or
-// to E4M3) exactly as the definition states. The kernels compute the
-// quotient as x * (1/s) (within 1.5 ulp of it) and take the exact division
-// only for the rare values that lie within a few ulps of a rounding boundary,
-// so the result is bit-identical while the common path avoids a division per
-// element.
+// to E4M3) exactly as the definition states, without a division per element:
+// INT8 codes compute the quotient as x * (1/s) (within 1.5 ulp of it) and
+// take the exact division only for the rare values within a few ulps of a
+// half-integer; E4M3 codes correct x * (1/s) by the exact residual of the
+// nearest E4M3 value or midpoint (two FMAs, no branch; see e4m3_q2).
 //
 // Restates the preprocessing named on "new MHA v4 entrypoint ..." (the
 // sage_quant_kernel, sage_quant_mxfp4, sage_quant_v_amax_partial /
@@ -126,28 +126,42 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-// Two E4M3 codes of x / s (IEEE binary32 quotient) for s > 0, inv = 1/s.
-// r = x * inv is within 1.5 ulp of the quotient; when the codes of r shrunk
-// and grown by 2^-21 agree, every value in between (the quotient included)
-// has that code; otherwise the exact divisions decide.
-__device__ __forceinline__ uint32_t e4m3x2_div(float x0, float x1, float s, float inv) {
-  const float r0 = __fmul_rn(x0, inv), r1 = __fmul_rn(x1, inv);
-  const uint32_t lo = e4m3x2(__fmul_rn(r0, 1.0f - 0x1p-21f), __fmul_rn(r1, 1.0f - 0x1p-21f));
-  const uint32_t hi = e4m3x2(__fmul_rn(r0, 1.0f + 0x1p-21f), __fmul_rn(r1, 1.0f + 0x1p-21f));
-  if (lo == hi && inv < INFINITY) return lo;  // (1/s overflows only for a subnormal s)
-  return e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+// Division-free exact E4M3 codes of IEEE binary32 quotients x / s (x BF16,
+// s > 0 in [2^-100, FLT_MAX]), with ninv = -(1/s) rounded to nearest (toward
+// zero when s has at most four significant bits):
+//  1. r = x / s within a few ulps (a product with the reciprocal); m = r
+//     rounded to five significant bits. The E4M3 values and the midpoints
+//     between them all lie on that grid, so m is the grid point nearest x / s.
+//  2. e = m s - x by one FMA, exactly: m s and x are multiples of
+//     2^(E(m) + E(s) - 27) and |e| < 2^(E(m) + E(s) - 3), 24 bits.
+//  3. q = m - e / s by one FMA with the reciprocal. If the binary32 quotient
+//     rounds to m (|e| <= s ulp(m) / 2), q = m: |e| is a multiple of the grid
+//     step above and s ulp(m) / 2 is S 2^-20 steps (S the 24-bit significand
+//     of s), so a strict inequality leaves a margin of 1/S that the
+//     reciprocal's error (under S 2^-48 relative) cannot close, and equality
+//     needs S divisible by 2^20, where the reciprocal rounded toward zero
+//     keeps q = m. Otherwise q lies strictly on the quotient's side of m. As
+//     no other grid point is nearer, q and x / s round to the same E4M3 code.
+// Working from -x keeps the sign of a zero input (q = -0 for x = -0).
+__device__ __forceinline__ float grid5(float v) {
+  return __uint_as_float((__float_as_uint(v) + 0x40000u) & 0xFFF80000u);
+}
+__device__ __forceinline__ float2 e4m3_q2(float nx0, float nx1, float2 s, float2 ninv) {
+  const float2 nx = make_float2(nx0, nx1);
+  const float2 r = __fmul2_rn(nx, ninv);
+  const float2 m = make_float2(grid5(r.x), grid5(r.y));
+  const float2 e = __ffma2_rn(m, s, nx);
+  return __ffma2_rn(e, ninv, m);
 }
 
-// Branch-free form: codes of r = x * inv shrunk and grown by 2^-21 (the
-// three products two lanes at a time); when they differ (`exact` set) the
-// caller redoes the pair with the division.
-__device__ __forceinline__ uint32_t e4m3x2_fast(float x0, float x1, float inv, bool& exact) {
-  const float2 r = __fmul2_rn(make_float2(x0, x1), make_float2(inv, inv));
-  const float2 lo = __fmul2_rn(r, make_float2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f));
-  const float2 hi = __fmul2_rn(r, make_float2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f));
-  const uint32_t clo = e4m3x2(lo.x, lo.y), chi = e4m3x2(hi.x, hi.y);
-  exact |= (clo != chi);
-  return clo;
+// -(1/s) for the encode above, or 0 for s = 0.
+__device__ __forceinline__ float e4m3_ninv(float s) {
+  if (!(s > 0.0f)) return 0.0f;
+  return (__float_as_uint(s) & 0xFFFFFu) == 0 ? -__frcp_rz(s) : -__frcp_rn(s);
+}
+// Scales the division-free encode covers (0 included: zero codes).
+__device__ __forceinline__ bool e4m3_scale_ok(float s) {
+  return s == 0.0f || (s >= 0x1p-100f && s <= 3.4028234663852886e38f);
 }
 
 // Four E4M3 codes in a word (byte i = element i): a.x, a.y, b.x, b.y.
@@ -162,22 +176,74 @@ __device__ __forceinline__ uint32_t e4m3x4w(float2 a, float2 b) {
   return r;
 }
 
-// E4M3 codes of eight BF16 values (one row chunk) at scale s > 0, inv = 1/s,
-// eight bytes (element i in byte i): the codes of the IEEE binary32 quotients
-// x / s, exact as in e4m3x2_fast (the rare bracketed pairs, or a subnormal
-// s whose reciprocal overflows, take the divisions).
-__device__ __forceinline__ uint2 fp8_codes8(const uint4& raw, float s, float inv) {
-  float f[8];
-  unpack8(raw, f);
-  bool exact = !(inv < INFINITY);
-  uint32_t c[4];
+// Eight BF16 values negated (sign bits flipped) and widened.
+__device__ __forceinline__ void unpack8_neg(const uint4& u, float (&f)[8]) {
+  unpack8(make_uint4(u.x ^ 0x80008000u, u.y ^ 0x80008000u, u.z ^ 0x80008000u,
+                     u.w ^ 0x80008000u), f);
+}
+
+// E4M3 codes of eight BF16 values (one row chunk) at one scale s (FP8 Q/K
+// blocks), eight bytes, element i in byte i: the division-free encode for
+// e4m3_scale_ok(s), the divisions otherwise (uniform over the block).
+__device__ __forceinline__ uint2 fp8_codes8(const uint4& raw, float s, float ninv) {
+  uint32_t c[2];
+  if (e4m3_scale_ok(s)) {
+    float f[8];
+    unpack8_neg(raw, f);
+    const float2 s2 = make_float2(s, s), n2 = make_float2(ninv, ninv);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) c[q] = e4m3x2_fast(f[2 * q], f[2 * q + 1], inv, exact);
-  if (exact) {
+    for (int h = 0; h < 2; ++h)
+      c[h] = e4m3x4w(e4m3_q2(f[4 * h], f[4 * h + 1], s2, n2),
+                     e4m3_q2(f[4 * h + 2], f[4 * h + 3], s2, n2));
+  } else {
+    float f[8];
+    unpack8(raw, f);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) c[q] = e4m3x2(__fdiv_rn(f[2 * q], s), __fdiv_rn(f[2 * q + 1], s));
+    for (int h = 0; h < 2; ++h)
+      c[h] = e4m3x2(__fdiv_rn(f[4 * h], s), __fdiv_rn(f[4 * h + 1], s)) |
+             (e4m3x2(__fdiv_rn(f[4 * h + 2], s), __fdiv_rn(f[4 * h + 3], s)) << 16);
   }
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  return make_uint2(c[0], c[1]);
+}
+
+// E4M3 codes of eight BF16 values of one token (channels c .. c + 7) with the
+// channels' own scales s[i] and negated reciprocals ninv[i] (V): eight bytes,
+// element i in byte i. `bad` (some s[i] outside e4m3_scale_ok) takes the
+// divisions; `keep` has byte i set when s[i] > 0 (a zero scale gives a zero
+// code).
+__device__ __forceinline__ uint2 fp8_codes8_channels(const uint4& raw, const float (&s)[8],
+                                                     const float (&ninv)[8], bool bad,
+                                                     const uint2& keep) {
+  uint32_t c[2];
+  if (!bad) {
+    float f[8];
+    unpack8_neg(raw, f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      c[h] = e4m3x4w(e4m3_q2(f[4 * h], f[4 * h + 1], make_float2(s[4 * h], s[4 * h + 1]),
+                             make_float2(ninv[4 * h], ninv[4 * h + 1])),
+                     e4m3_q2(f[4 * h + 2], f[4 * h + 3], make_float2(s[4 * h + 2], s[4 * h + 3]),
+                             make_float2(ninv[4 * h + 2], ninv[4 * h + 3])));
+  } else {  // rare: a subnormal or infinite channel scale
+    float f[8];
+    unpack8(raw, f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      c[h] = e4m3x2(s[4 * h] > 0.0f ? __fdiv_rn(f[4 * h], s[4 * h]) : 0.0f,
+                    s[4 * h + 1] > 0.0f ? __fdiv_rn(f[4 * h + 1], s[4 * h + 1]) : 0.0f) |
+             (e4m3x2(s[4 * h + 2] > 0.0f ? __fdiv_rn(f[4 * h + 2], s[4 * h + 2]) : 0.0f,
+                     s[4 * h + 3] > 0.0f ? __fdiv_rn(f[4 * h + 3], s[4 * h + 3]) : 0.0f)
+              << 16);
+  }
+  return make_uint2(c[0] & keep.x, c[1] & keep.y);
+}
+
+// The byte mask of fp8_codes8_channels for scales s.
+__device__ __forceinline__ uint2 fp8_keep_mask(const float (&s)[8]) {
+  uint32_t k[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) k[i / 4] |= (s[i] > 0.0f ? 0xFFu : 0u) << (8 * (i % 4));
+  return make_uint2(k[0], k[1]);
 }
 
 // CODE 0: INT8 codes held as FP16 (absmax/127); CODE 1: FP8 E4M3 codes
@@ -230,7 +296,7 @@ __global__ void __launch_bounds__(256) quantize_qk_block_kernel(QuantQKArgs a) {
       __half* out = static_cast<__half*>(a.out);
       *reinterpret_cast<uint4*>(out + (bh * Np + n) * 128 + col) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
-      const uint2 c = (n < nv && s > 0.0f) ? fp8_codes8(raw[i], s, inv) : make_uint2(0, 0);
+      const uint2 c = (n < nv && s > 0.0f) ? fp8_codes8(raw[i], s, e4m3_ninv(s)) : make_uint2(0, 0);
       uint8_t* out = static_cast<uint8_t*>(a.out);
       *reinterpret_cast<uint2*>(out + (bh * Np + n) * 128 + col) = c;
     }
@@ -440,56 +506,39 @@ __global__ void __launch_bounds__(256) v_amax_kernel(QuantVArgs a) {
   }
 }
 
-// V pass 2: finalize the channel scales, quantize one 128-token tile and
-// write it transposed ([D][Npad], token-contiguous) through shared memory.
+// V pass 2 (direct loads, any strides): finalize the channel scales and
+// encode one 128-token block into the token-major layout [B][H][Npad][128].
 __global__ void __launch_bounds__(256) v_quantize_kernel(QuantVArgs a) {
-  constexpr int kPitchWords = 33;  // 128 tokens = 32 words, +1 to spread banks
-  __shared__ uint32_t tileT[128 * kPitchWords];
-  __shared__ float sv[128], sinv[128];
+  __shared__ float sv[128], sninv[128];
   const int64_t h = blockIdx.x, tile = blockIdx.y, b = blockIdx.z;
   const int64_t nv = valid_tokens(a.lens, b, a.N, a.status);
   const int64_t bh = b * a.H + h;
   const int64_t Np = pad128(a.N);
   if (threadIdx.x < 128) {
     const float m = __int_as_float(a.amax[bh * 128 + threadIdx.x]);
-    const float s = __fdiv_rn(m, 448.0f);
-    sv[threadIdx.x] = s;
-    sinv[threadIdx.x] = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    if (tile == 0) a.scale[bh * 128 + threadIdx.x] = s;
+    const float sc = __fdiv_rn(m, 448.0f);
+    sv[threadIdx.x] = sc;
+    sninv[threadIdx.x] = e4m3_ninv(sc);
+    if (tile == 0) a.scale[bh * 128 + threadIdx.x] = sc;
   }
   __syncthreads();
-  const int cg = threadIdx.x & 15;  // channels 8cg .. 8cg+7
-  const int tg = threadIdx.x >> 4;  // token quad within a 64-token half
-#pragma unroll 1
-  for (int half = 0; half < 2; ++half) {
-    const int t0 = half * 64 + tg * 4;
-    float f[4][8];
+  const int col = (threadIdx.x & 15) * 8;
+  const int r0 = threadIdx.x >> 4;
+  float s8[8], ninv8[8];
+  bool bad = false;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t n = tile * 128 + t0 + u;
-      if (n < nv) {
-        unpack8(ldg_v4(a.v + b * a.sb + n * a.sn + h * a.sh + cg * 8), f[u]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[u][k] = 0.0f;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int d = cg * 8 + k;
-      const float s = sv[d], inv = sinv[d];
-      uint32_t w = 0;
-      if (s > 0.0f) w = e4m3x2_div(f[0][k], f[1][k], s, inv) | (e4m3x2_div(f[2][k], f[3][k], s, inv) << 16);
-      tileT[d * kPitchWords + t0 / 4] = w;
-    }
+  for (int q = 0; q < 8; ++q) {
+    s8[q] = sv[col + q];
+    ninv8[q] = sninv[col + q];
+    bad |= !e4m3_scale_ok(s8[q]);
   }
-  __syncthreads();
+  const uint2 keep = fp8_keep_mask(s8);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int wi = threadIdx.x + 256 * i;
-    const int d = wi >> 5, tw = wi & 31;
-    reinterpret_cast<uint32_t*>(a.out + (bh * 128 + d) * Np + tile * 128)[tw] =
-        tileT[d * kPitchWords + tw];
+  for (int j = 0; j < 8; ++j) {
+    const int64_t n = tile * 128 + r0 + 16 * j;
+    const uint4 raw = n < nv ? ldg_v4(a.v + b * a.sb + n * a.sn + h * a.sh + col) : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint2*>(a.out + (bh * Np + n) * 128 + col) =
+        fp8_codes8_channels(raw, s8, ninv8, bad, keep);
   }
 }
 
@@ -892,11 +941,17 @@ constexpr int kBlockBytes = 128 * 128 * 2;
 struct BlockCoord {
   int64_t b, h, blk;
 };
+// Block indices stay below 2^31 (the host caps B * H * Npad), so the
+// decomposition uses 32-bit divisions: 64-bit ones are long software
+// sequences, and every block pays them.
 __device__ __forceinline__ BlockCoord block_coord(int64_t i, int64_t H, int64_t nb) {
+  const uint32_t ii = static_cast<uint32_t>(i), hh = static_cast<uint32_t>(H);
+  const uint32_t nn = static_cast<uint32_t>(nb);
+  const uint32_t q = ii / hh, b = q / nn;
   BlockCoord c;
-  c.h = i % H;
-  c.blk = (i / H) % nb;
-  c.b = i / (H * nb);
+  c.h = ii - q * hh;
+  c.blk = q - b * nn;
+  c.b = b;
   return c;
 }
 
@@ -1009,10 +1064,11 @@ __device__ __forceinline__ void qk_block_from_tile(const uint8_t* tile, const Bl
       *reinterpret_cast<uint4*>(orow0 + j * 16 * 128) = cw;
     }
   } else {
+    const float ninv = e4m3_ninv(s);
     uint8_t* orow0 = static_cast<uint8_t*>(a.out) + (bh * Np + c.blk * 128 + r0) * 128 + col;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint2 cw = s > 0.0f ? fp8_codes8(raw[j], s, inv) : make_uint2(0, 0);
+      const uint2 cw = s > 0.0f ? fp8_codes8(raw[j], s, ninv) : make_uint2(0, 0);
       *reinterpret_cast<uint2*>(orow0 + j * 16 * 128) = cw;
     }
   }
@@ -1132,7 +1188,8 @@ __global__ void __launch_bounds__(256, 2) quantize_qkv_tma_kernel(
       c = block_coord(i, a.q.H, nbq);
     } else {
       map = i < nQ + nK ? &tmK : &tmV;
-      c = block_coord((i - nQ) % nK, a.k.H, nbk);
+      const int64_t ik = i - nQ;
+      c = block_coord(ik < nK ? ik : ik - nK, a.k.H, nbk);
     }
     const int st = static_cast<int>(k % kQStages);
     mbar_arrive_expect_tx(&ring.full[st], kBlockBytes);
@@ -1165,108 +1222,60 @@ __global__ void __launch_bounds__(256, 2) quantize_qkv_tma_kernel(
   ring.drain(k, a.q.status);
 }
 
-constexpr int kVStages = 2;
-
-// V encode, TMA-fed: thread t owns channels 8 (t % 16) .. + 7 and, in each
-// 64-token half of the staged block, tokens 4 (t / 16) .. + 3. It packs the
-// four tokens' codes of each channel (E4M3 of the binary32 quotient v / s_d,
-// exact as in e4m3x2_fast) into one word of a transposed block in shared
-// memory (128 channel rows, 33-word pitch against bank conflicts), which the
-// warps then store as 128-byte token-contiguous rows of V^T.
+// V encode, TMA-fed: the V^T-free token-major layout [B][H][Npad][128], so
+// each 128-token block is encoded like a Q/K block (thread = 8 channels x 8
+// rows, 8-byte stores, 128-byte rows) with the channels' own scales
+// absmax/448 (finalized from the channel maxima at the head's first block,
+// where they are also written out).
 __global__ void __launch_bounds__(256, 2) v_quantize_tma_kernel(
     const __grid_constant__ CUtensorMap tmV, QuantVArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  // Transposed block: 128 channel rows of 32 words (128 tokens); the 4-word
-  // groups of row d are XOR-swizzled by (d / 8) % 8, so that the transposing
-  // word stores and the 16-byte row reads both spread over the banks.
-  __shared__ __align__(16) uint32_t tileT[128 * 32];
-  __shared__ float sv[128], sinv[128];
+  __shared__ float sv[128], sninv[128];
   __shared__ int abort_flag;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~static_cast<uintptr_t>(127));
-  BlockRing<kVStages> ring;
+  BlockRing<kQStages> ring;
   ring.init(base, &abort_flag);
   const int64_t Np = pad128(a.N), nb = Np / 128, total = a.B * a.H * nb;
-  const int cg = threadIdx.x & 15;
-  const int tg = threadIdx.x >> 4;
-  for (int k = 0; k < kVStages - 1; ++k) ring.load(&tmV, k, total, a.H, nb);
+  const int col = (threadIdx.x & 15) * 8;
+  const int r0 = threadIdx.x >> 4;
+  for (int k = 0; k < kQStages - 1; ++k) ring.load(&tmV, k, total, a.H, nb);
   int64_t k = 0;
   for (;; ++k) {
     const int64_t i = blockIdx.x + k * gridDim.x;
     if (i >= total) break;
-    ring.load(&tmV, k + kVStages - 1, total, a.H, nb);
+    ring.load(&tmV, k + kQStages - 1, total, a.H, nb);
     const BlockCoord c = block_coord(i, a.H, nb);
     const int64_t bh = c.b * a.H + c.h;
     if (threadIdx.x < 128) {
       const float mx = __int_as_float(a.amax[bh * 128 + threadIdx.x]);
-      const float s = __fdiv_rn(mx, 448.0f);
-      sv[threadIdx.x] = s;
-      sinv[threadIdx.x] = s > 0.0f ? __frcp_rn(s) : 0.0f;
-      if (c.blk == 0) a.scale[bh * 128 + threadIdx.x] = s;
+      const float sc = __fdiv_rn(mx, 448.0f);
+      sv[threadIdx.x] = sc;
+      sninv[threadIdx.x] = e4m3_ninv(sc);
+      if (c.blk == 0) a.scale[bh * 128 + threadIdx.x] = sc;
     }
-    if (!ring.wait(k, &abort_flag, a.status)) break;  // (also orders sv/sinv)
+    if (!ring.wait(k, &abort_flag, a.status)) break;  // (also orders sv/sninv)
     const int64_t nv = valid_tokens(a.lens, c.b, a.N, a.status);
     const uint8_t* tile = ring.stage(k);
-    float s8[8], inv8[8];
-    bool inv_bad = false;  // a subnormal scale whose reciprocal overflows
+    float s8[8], ninv8[8];
+    bool bad = false;  // a subnormal or infinite scale: divisions
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      s8[q] = sv[cg * 8 + q];
-      inv8[q] = sinv[cg * 8 + q];
-      inv_bad |= s8[q] > 0.0f && !(inv8[q] < INFINITY);
+      s8[q] = sv[col + q];
+      ninv8[q] = sninv[col + q];
+      bad |= !e4m3_scale_ok(s8[q]);
     }
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      const int t0 = half * 64 + tg * 4;
-      float f[4][8];
+    const uint2 keep = fp8_keep_mask(s8);
+    uint8_t* orow0 = a.out + (bh * Np + c.blk * 128 + r0) * 128 + col;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint4 raw = *reinterpret_cast<const uint4*>(tile + (t0 + u) * 256 + cg * 16);
-        if (c.blk * 128 + t0 + u >= nv) raw = make_uint4(0, 0, 0, 0);
-        unpack8(raw, f[u]);
-      }
-      // Four tokens of each channel per word: the codes of r = x * (1/s) shrunk
-      // and grown by 2^-21 (packed products); when the two words differ, some
-      // quotient brackets a rounding boundary and the exact divisions decide
-      // (as in e4m3x2_fast). A zero scale (all-zero channel) gives zero codes.
-      const float2 dn = make_float2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
-      const float2 up = make_float2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
-      uint32_t w[8];
-      bool redo = inv_bad;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float2 iv = make_float2(inv8[q], inv8[q]);
-        const float2 r01 = __fmul2_rn(make_float2(f[0][q], f[1][q]), iv);
-        const float2 r23 = __fmul2_rn(make_float2(f[2][q], f[3][q]), iv);
-        const uint32_t clo = e4m3x4w(__fmul2_rn(r01, dn), __fmul2_rn(r23, dn));
-        const uint32_t chi = e4m3x4w(__fmul2_rn(r01, up), __fmul2_rn(r23, up));
-        redo |= clo != chi;
-        w[q] = s8[q] > 0.0f ? clo : 0u;
-      }
-      if (redo) {  // rare: quotients near an E4M3 rounding boundary
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (s8[q] > 0.0f)
-            w[q] = e4m3x2(__fdiv_rn(f[0][q], s8[q]), __fdiv_rn(f[1][q], s8[q])) |
-                   (e4m3x2(__fdiv_rn(f[2][q], s8[q]), __fdiv_rn(f[3][q], s8[q])) << 16);
-      }
-      const int tw = t0 / 4;  // word (4 tokens) of the channel rows
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int d = cg * 8 + q;
-        tileT[d * 32 + ((((tw >> 2) ^ (d >> 3)) & 7) << 2) + (tw & 3)] = w[q];
-      }
+    for (int j = 0; j < 8; ++j) {
+      const int rr = r0 + 16 * j;
+      uint4 raw = *reinterpret_cast<const uint4*>(tile + rr * 256 + col * 2);
+      if (c.blk * 128 + rr >= nv) raw = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint2*>(orow0 + j * 16 * 128) =
+          fp8_codes8_channels(raw, s8, ninv8, bad, keep);
     }
-    __syncthreads();
-    // 16-byte pieces of the V^T rows: 8 per channel row, 128 bytes per row.
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int ci = static_cast<int>(threadIdx.x) + 256 * j;
-      const int d = ci >> 3, g = ci & 7;
-      const uint4 v4 = *reinterpret_cast<const uint4*>(&tileT[d * 32 + ((g ^ (d >> 3)) & 7) * 4]);
-      *reinterpret_cast<uint4*>(a.out + (bh * 128 + d) * Np + c.blk * 128 + g * 16) = v4;
-    }
-    __syncthreads();  // stage, tileT and sv free again
+    __syncthreads();  // stage k % kQStages and sv free again
   }
   ring.drain(k, a.status);
 }
@@ -1490,7 +1499,7 @@ cudaError_t launch_quantize_qkv_code(const QuantQKArgs& q, const QuantQKArgs& k,
   cudaError_t e = cudaMemsetAsync(v.amax, 0, static_cast<size_t>(v_workspace_bytes(v.B, v.H)), s);
   if (e != cudaSuccess) return e;
   const int smem1 = kQStages * kBlockBytes + kQStages * 8 + 128;
-  const int smem2 = kVStages * kBlockBytes + kVStages * 8 + 128;
+  const int smem2 = smem1;
   if ((e = set_smem<quantize_qkv_tma_kernel<CODE>>(smem1)) != cudaSuccess) return e;
   if ((e = set_smem<v_quantize_tma_kernel>(smem2)) != cudaSuccess) return e;
   const int64_t nQ = q.B * q.H * (pad128(q.N) / 128), nV = v.B * v.H * (pad128(v.N) / 128);
@@ -1551,7 +1560,7 @@ cudaError_t launch_quantize_v(const QuantVArgs& a, cudaStream_t s) {
   if (bnhd_map(&m, a.v, a.sb, a.sn, a.sh, a.B, a.N, a.H)) {
     const int64_t blocks = a.B * a.H * (pad128(a.N) / 128);
     const int smem1 = kQStages * kBlockBytes + kQStages * 8 + 128;
-    const int smem2 = kVStages * kBlockBytes + kVStages * 8 + 128;
+    const int smem2 = smem1;
     if ((e = set_smem<v_amax_tma_kernel>(smem1)) != cudaSuccess) return e;
     if ((e = set_smem<v_quantize_tma_kernel>(smem2)) != cudaSuccess) return e;
     v_amax_tma_kernel<<<persistent_grid(blocks), 256, smem1, s>>>(m, a);

@@ -26,7 +26,7 @@ struct QuantVArgs {
   int64_t sb, sn, sh;
   int64_t B, N, H;
   const int32_t* lens;
-  uint8_t* out;   // [B][H][D][Npad]
+  uint8_t* out;   // E4M3 [B][H][Npad][128] (token-major); MXFP4 [B][H][128][Npad/2]
   float* scale;   // [B][H][D]
   int* amax;      // [B][H][D] channel maxima as binary32 bit patterns (workspace)
   int* status;

@@ -96,7 +96,7 @@ size_t sage_quantized_bytes(sage_format_t fmt, int which, int64_t B, int64_t N, 
                                     : B * H * Np * D * (fmt == SAGE_FMT_QK_INT8_V_FP8 ? 2 : 1));
     case 1:
       return static_cast<size_t>(mx ? B * H * Np * (D / 32) : B * H * (Np / 128) * 4);
-    case 2:  // V: E4M3 [B][H][D][Npad], or E2M1 [B][H][D][Npad/2]
+    case 2:  // V: E4M3 [B][H][Npad][D], or E2M1 [B][H][D][Npad/2]
       return static_cast<size_t>(v4 ? B * H * D * Np / 2 : B * H * D * Np);
     case 3:  // V scales: float [B][H][D], or E8M0 [B][H][Npad/128][D][4]
       return static_cast<size_t>(v4 ? B * H * Np * D / 32 : B * H * D * 4);

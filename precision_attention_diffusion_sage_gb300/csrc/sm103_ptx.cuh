@@ -248,12 +248,27 @@ __device__ __forceinline__ void mma_f8_ss_lo(uint32_t d_tmem, uint32_t a_lo, uin
       : "memory");
 }
 
-// Instruction descriptor, dense MMA with FP32 accumulator and both operands
-// K-major. Format code 0 is F16 for kind::f16 and E4M3 for kind::f8f6f4.
-__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, uint32_t a_fmt = 0,
-                                                    uint32_t b_fmt = 0) {
-  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor, dense MMA with FP32 accumulator, A K-major and B
+// K-major (or, with b_mn, MN-major: B's N dimension contiguous in memory).
+// Format code 0 is F16 for kind::f16 and E4M3 for kind::f8f6f4.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn = false,
+                                                    uint32_t a_fmt = 0, uint32_t b_fmt = 0) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (b_mn ? 1u << 16 : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same MMAs with separate high descriptor words for A and B (operands in
+// different swizzle layouts, e.g. a 128-byte swizzled A and a 64-byte
+// swizzled MN-major B).
+template <uint32_t AHI, uint32_t BHI>
+__device__ __forceinline__ void mma_f8_ss_lo_ab(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %4, 0;\n"
+      " mov.b64 a, {%1, %5};\n mov.b64 b, {%2, %6};\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AHI), "n"(BHI)
+      : "memory");
 }
 
 // ---------------------------------------------------------------- block-scaled MXFP4 MMA
@@ -441,13 +456,14 @@ __device__ __forceinline__ void mma_f16_ss_lo_pair(uint32_t d_tmem, uint32_t a_l
       "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSw128DescHi)
       : "memory");
 }
+template <uint32_t BHI = kSw128DescHi>
 __device__ __forceinline__ void mma_f8_ss_lo_pair(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                                   uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %4, 0;\n"
-      " mov.b64 a, {%1, %5};\n mov.b64 b, {%2, %5};\n"
+      " mov.b64 a, {%1, %5};\n mov.b64 b, {%2, %6};\n"
       " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSw128DescHi)
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSw128DescHi), "n"(BHI)
       : "memory");
 }
 // Arrives once on the mbarrier at shared address `bar` in both CTAs of the

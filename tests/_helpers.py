@@ -63,12 +63,14 @@ def assert_qk_equal(fmt, gpu_q, gpu_s, ref_q, ref_s):
 
 def assert_v_equal(gpu_v, gpu_s, ref_v, ref_s):
     """V codes and scales bit for bit: FP32 channel scales (E4M3 V) or E8M0
-    bytes (MXFP4 V)."""
-    np.testing.assert_array_equal(gpu_v.cpu().numpy(), ref_v)
+    bytes (MXFP4 V). The library's E4M3 V is token-major [B, H, Npad, D]; the
+    oracle writes [B, H, D, Npad], so the comparison transposes the GPU's."""
     gs = gpu_s.cpu().numpy()
     if ref_s.dtype == np.uint8:
+        np.testing.assert_array_equal(gpu_v.cpu().numpy(), ref_v)
         np.testing.assert_array_equal(gs, ref_s)
     else:
+        np.testing.assert_array_equal(gpu_v.transpose(-1, -2).cpu().numpy(), ref_v)
         np.testing.assert_array_equal(gs.view(np.uint32), ref_s.view(np.uint32))
 
 

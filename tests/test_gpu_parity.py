@@ -117,6 +117,78 @@ def test_quantize_rounding_ties_bitexact():
     assert_v_equal(vq, vs, rv, rvs)
 
 
+def _e4m3_midpoints():
+    e4 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double()
+    vals = torch.unique(e4[torch.isfinite(e4) & (e4 > 0)])
+    return torch.cat([vals[:1] / 2, (vals[:-1] + vals[1:]) / 2])  # incl. the one below 2^-9
+
+
+def _tie_channel(g, amax, n):
+    """BF16 values of one channel whose channel scale is amax / 448 (binary32)
+    and whose quotients x / s are, where BF16 allows, exact E4M3 midpoints,
+    or one BF16 step beside one; amax itself at row 0."""
+    s = float(np.float32(np.float32(amax) / np.float32(448.0)))
+    mids = _e4m3_midpoints()
+    m = mids[torch.randint(0, len(mids), (n,), generator=g)]
+    sign = torch.where(torch.rand(n, generator=g, dtype=torch.float64) < 0.5, -1.0, 1.0)
+    x = (m * s * sign).to(torch.bfloat16)
+    step = torch.randint(-1, 2, (n,), generator=g)                 # a BF16 step off, or on
+    xb = x.view(torch.int16) + step.to(torch.int16) * (x != 0).to(torch.int16)
+    x = xb.view(torch.bfloat16).double().clamp(-amax, amax)
+    x[0] = amax
+    return x
+
+
+def test_quantize_fp8_exact_encode_edges():
+    """E4M3 codes (V channel scales and FP8 Q/K block scales) at the edges of
+    the division-free encode: scales with at most four significant bits
+    (amax = 448 j 2^k / 8), scales from BF16 maxima whose quotients hit E4M3
+    midpoints exactly or one BF16 step away, signed zeros, subnormal BF16
+    inputs, an all-zero channel, a scale below 2^-100 and an infinite one
+    (the division path), and a scale near the top of the range."""
+    g = torch.Generator().manual_seed(71)
+    N, H = 256, 2
+    x = torch.zeros((1, N, H, 128), dtype=torch.float64)
+    for h in range(H):
+        for c in range(128):
+            kind = (c + 5 * h) % 8
+            if kind in (0, 1, 2):    # short scales
+                j = int(torch.randint(8, 16, (1,), generator=g))
+                k = int(torch.randint(-20, 6, (1,), generator=g))
+                amax = 448.0 * j / 8 * 2.0 ** k
+            elif kind in (3, 4, 5):  # BF16 maxima of randn-like channels
+                amax = float(torch.tensor(abs(float(torch.randn(1, generator=g))) * 3 + 1.5)
+                             .to(torch.bfloat16)) * 2.0 ** int(torch.randint(-30, 30, (1,), generator=g))
+            elif kind == 6:
+                amax = float(torch.tensor(3.0e38).to(torch.bfloat16))
+            else:
+                amax = 0.0
+            if amax > 0:
+                x[0, :, h, c] = _tie_channel(g, amax, N)
+    x[0, 7:40, 0, 7] = -0.0                                     # signed zeros in an all-zero channel
+    x[0, 3:20, 0, 10] = torch.tensor([0.0, -0.0]).repeat(9)[:17]
+    x[0, 30:40, 1, 11] = 2.0 ** -133 * torch.arange(-5, 5)      # BF16 subnormals
+    x[0, :, 1, 12] = 1e-29 * torch.randn(N, generator=g, dtype=torch.float64)  # s < 2^-100
+    x[0, :, 1, 13] = torch.randn(N, generator=g, dtype=torch.float64)
+    x[0, 9, 1, 13] = float("inf")                                 # s = inf: x / s = 0 or NaN
+    x[0, 10, 1, 13] = -float("inf")
+    xb = x.to(torch.bfloat16)
+    xc = xb.cuda()
+    vq, vs = binding.sage_quantize_v(xc)
+    rv, rvs = oracle.quantize_v_fp8(bf16_bits(xb))
+    assert_v_equal(vq, vs, rv, rvs)
+    # FP8 Q/K: one block scale per 128 tokens; rows of short-scale channels
+    # make blocks whose maximum is the channel's, with its ties
+    y = torch.zeros((1, N, 1, 128), dtype=torch.float64)
+    y[0, :128, 0, :] = _tie_channel(g, 448.0 * 13 / 8 * 2.0 ** -4, 128 * 128).view(128, 128)
+    y[0, 128:, 0, :] = _tie_channel(g, 5.5 * 2.0 ** 7, 128 * 128).view(128, 128)
+    yb = y.to(torch.bfloat16)
+    gq, gs = binding.sage_quantize_qk(yb.cuda(), 2)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_fp8_qk(bf16_bits(yb))
+    assert_qk_equal(2, gq, gs, rq, rs)
+
+
 def test_quantize_strided_packed_qkv():
     """A packed [B, N, 3, H, D] QKV buffer quantizes like contiguous tensors."""
     w, q, k, v = _small(1, 2, 300, 300, seed=5)

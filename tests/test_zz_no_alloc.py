@@ -28,7 +28,7 @@ def lib():
 def _noalloc(binding, v, lens):
     B, N, H, D = v.shape
     Np = binding.pad128(N)
-    out = torch.full((B, H, D, Np), 0xAB, dtype=torch.uint8, device=v.device)
+    out = torch.full((B, H, Np, D), 0xAB, dtype=torch.uint8, device=v.device)
     scale = torch.full((B, H, D), -1.0, dtype=torch.float32, device=v.device)
     ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=v.device)
     f = binding.library().sage_quantize_v_noalloc
