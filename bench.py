@@ -8,7 +8,10 @@ smoothing the separate quantize calls it needs) and one attention call (BF16 O
 + FP32 LSE), each replayed from a CUDA graph. Effective TFLOPS =
 4*B*H*Nq*Nk*D / (summed step time). Between steps, outside the timed events,
 L2 is flushed by reading a 256 MiB buffer. The default workload is the
-65520-token long-video self-attention. Prints one JSON line on rank 0.
+65520-token long-video self-attention. `e2e` times the same work through
+sage_attention_host: Q/K/V in page-locked host memory, O/LSE written back to
+host memory, the library's pipelined copies inside the timed region. Prints
+one JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -500,17 +503,17 @@ def main():
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        qd, kd, vd = (torch.empty_like(t) for t in (q, k, v))
+        host_kw = dict(fmt=fmt, k_lens=w.k_lens, num_splits=args.splits, smooth_k=w.smooth_k,
+                       smooth_q=w.smooth_q, cta_mode=args.cta_mode)
+        ws_host = torch.empty(binding.sage_attention_host_workspace_bytes(
+            w.B, w.Nq, w.Nk, w.H, fmt=fmt, smooth_k=w.smooth_k, smooth_q=w.smooth_q,
+            num_splits=args.splits, cta_mode=args.cta_mode, k_lens=w.k_lens is not None),
+            dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            oo, ll = binding.sage_attention(qd, kd, vd, fmt=fmt, k_lens=k_lens,
-                                            num_splits=args.splits, smooth_k=w.smooth_k,
-                                            smooth_q=w.smooth_q, cta_mode=args.cta_mode)
-            oh.copy_(oo, non_blocking=True)
-            lh.copy_(ll, non_blocking=True)
+            # host Q/K/V in, host O/LSE out: head groups are copied in,
+            # quantized, attended and copied out by the library, pipelined
+            binding.sage_attention_host(qh, kh, vh, out=oh, lse=lh, workspace=ws_host, **host_kw)
 
         for _ in range(args.warmup):
             e2e_step()
@@ -526,7 +529,7 @@ def main():
         barrier()
         e_ms = sum(a.elapsed_time(b) for a, b in ee)
         e_ms = max_over_ranks(e_ms, world, dev)
-        h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+        h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
         e2e = {"value": replica_throughput(flops, args.steps, e_ms, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

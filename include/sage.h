@@ -345,6 +345,55 @@ sage_status_t sage_attn_fwd(sage_format_t fmt, const void* q_q, const void* q_sc
                             size_t ws_bytes, const sage_attn_options_t* opts,
                             sage_stream_t stream);
 
+/* The pages this library restates have no counterpart to this entry point.
+ * Attention with Q, K, V and the results in HOST memory: the heads are taken
+ * in groups; while one group is quantized and attended on the GPU, the next
+ * group's Q/K/V slices are copied in and the previous group's O and LSE are
+ * copied out, so the copy engines and the SMs overlap. Per group the call
+ * runs the library's own steps: sage_quantize_qkv (or, with smoothing,
+ * sage_quantize_q_smooth / sage_quantize_k_smooth / sage_quantize_qk,
+ * sage_quantize_v or sage_quantize_v_mxfp4, and sage_delta_s) and
+ * sage_attn_fwd. Every scale, code and output row depends on its own head
+ * only, and the split count and tile mode are resolved once for the whole
+ * shape, so O and LSE equal those of the same calls on the whole device
+ * tensors, bit for bit.
+ * Stream order: the work starts after the work already queued on `stream`,
+ * and `stream` is made to wait for all of it (copies included) before any
+ * work queued on it later; the host buffers must stay valid and unchanged
+ * until then. The call creates, and releases on return, its own CUDA streams
+ * and events (so it cannot be captured into a CUDA graph). Page-locked host
+ * buffers let copies overlap kernels; pageable ones work, without overlap. */
+typedef struct {
+  sage_format_t fmt;
+  int64_t B, Nq, Nk, H, D;  /* D must be 128 */
+  const void* q;            /* host BF16 [B][Nq][H][D], contiguous */
+  const void* k;            /* host BF16 [B][Nk][H][D], contiguous */
+  const void* v;            /* host BF16 [B][Nk][H][D], contiguous */
+  void* o;                  /* host BF16 [B][Nq][H][D], contiguous (output) */
+  float* lse;               /* nullable host float [B][H][Nq] (output) */
+  const int32_t* k_lens;    /* nullable host int32 [B], as sage_attn_fwd */
+  float softmax_scale;      /* <= 0 selects 1/sqrt(D) */
+  int32_t smooth_k;         /* 0 or 1: K smoothing (SAGE_FMT_QK_INT8_V_FP8 only) */
+  int32_t smooth_q;         /* 0 or 1: Q smoothing with dS (SAGE_FMT_QK_INT8_V_FP8 only) */
+  int32_t heads_per_group;  /* 0 = library choice (about 20 groups when each head's
+                               attention outlasts its copies several times over, as
+                               at 65520 tokens, else about 5), else 1..H */
+  int32_t num_splits;       /* as sage_attn_options_t, resolved for the whole shape */
+  int32_t cta_mode;         /* as sage_attn_options_t, resolved for the whole shape */
+} sage_host_attention_t;
+
+/* Device workspace bytes of sage_attention_host for `a` (two groups' buffers
+ * and the key lengths); 0 when `a` is invalid. No CUDA call. */
+size_t sage_attention_host_workspace_bytes(const sage_host_attention_t* a);
+
+/*   workspace : device scratch of at least sage_attention_host_workspace_bytes(a)
+ *               bytes, 256-byte aligned; contents on entry are ignored.
+ * Returns a validation error before any CUDA call, SAGE_ERR_CUDA when a CUDA
+ * call fails (work queued until then still runs), else the first error of a
+ * per-group call. Device-side errors go to the device status word. */
+sage_status_t sage_attention_host(const sage_host_attention_t* a, void* workspace,
+                                  size_t ws_bytes, sage_stream_t stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char* sage_status_string(sage_status_t st);
 

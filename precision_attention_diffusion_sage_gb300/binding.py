@@ -43,6 +43,16 @@ class AttnOptions(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class HostAttention(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int), ("B", ctypes.c_int64), ("Nq", ctypes.c_int64),
+                ("Nk", ctypes.c_int64), ("H", ctypes.c_int64), ("D", ctypes.c_int64),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("k_lens", ctypes.c_void_p),
+                ("softmax_scale", ctypes.c_float), ("smooth_k", ctypes.c_int32),
+                ("smooth_q", ctypes.c_int32), ("heads_per_group", ctypes.c_int32),
+                ("num_splits", ctypes.c_int32), ("cta_mode", ctypes.c_int32)]
+
+
 _P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 _lib.sage_quantized_bytes.restype = ctypes.c_size_t
 _lib.sage_quantized_bytes.argtypes = [_I32, _I32, _I64, _I64, _I64, _I64]
@@ -70,6 +80,10 @@ _lib.sage_attn_fwd.restype = _I32
 _lib.sage_attn_fwd.argtypes = [_I32, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
                                ctypes.c_float, _I32, _P, Strides, _P, _P, ctypes.c_size_t,
                                ctypes.POINTER(AttnOptions), _P]
+_lib.sage_attention_host_workspace_bytes.restype = ctypes.c_size_t
+_lib.sage_attention_host_workspace_bytes.argtypes = [ctypes.POINTER(HostAttention)]
+_lib.sage_attention_host.restype = _I32
+_lib.sage_attention_host.argtypes = [ctypes.POINTER(HostAttention), _P, ctypes.c_size_t, _P]
 _lib.sage_status_string.restype = ctypes.c_char_p
 _lib.sage_status_string.argtypes = [_I32]
 _lib.sage_last_device_status.restype = _I32
@@ -380,6 +394,67 @@ def sage_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: in
     return sage_attn_fwd(fmt, qq, qs, kq, ks, vq, vs, Nq=Nq, Nk=Nk, k_lens=k_lens,
                          softmax_scale=softmax_scale, num_splits=num_splits,
                          return_lse=return_lse, k_mean=km, delta_s=ds, cta_mode=cta_mode)
+
+
+def _host_desc(q, k, v, o, lse, lens, fmt, softmax_scale, smooth_k, smooth_q, heads_per_group,
+               num_splits, cta_mode) -> HostAttention:
+    B, Nq, H, D = q.shape
+    addr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    return HostAttention(fmt, B, Nq, k.shape[1], H, D, addr(q), addr(k), addr(v), addr(o),
+                         addr(lse), addr(lens),
+                         float(softmax_scale) if softmax_scale else 0.0, int(smooth_k),
+                         int(smooth_q), int(heads_per_group), int(num_splits), int(cta_mode))
+
+
+def sage_attention_host_workspace_bytes(B: int, Nq: int, Nk: int, H: int, *, fmt: int = FMT_INT8,
+                                        D: int = 128, smooth_k: bool = False,
+                                        smooth_q: bool = False, heads_per_group: int = 0,
+                                        num_splits: int = 0, cta_mode: int = 0,
+                                        k_lens: bool = False, lse: bool = True) -> int:
+    """Device workspace of sage_attention_host for these sizes (0 if invalid)."""
+    one = 1  # non-null placeholders: only sizes are read
+    d = HostAttention(fmt, B, Nq, Nk, H, D, one, one, one, one, one if lse else None,
+                      one if k_lens else None, 0.0, int(smooth_k), int(smooth_q),
+                      int(heads_per_group), int(num_splits), int(cta_mode))
+    return int(_lib.sage_attention_host_workspace_bytes(ctypes.byref(d)))
+
+
+def sage_attention_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, fmt: int = FMT_INT8,
+                        k_lens=None, softmax_scale: Optional[float] = None, num_splits: int = 0,
+                        smooth_k: bool = False, smooth_q: bool = False, cta_mode: int = 0,
+                        heads_per_group: int = 0, out: Optional[torch.Tensor] = None,
+                        lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+                        workspace: Optional[torch.Tensor] = None):
+    """sage_attention on HOST tensors (contiguous BF16 [B, N, H, D] on the CPU,
+    page-locked for copy/compute overlap): the library copies head groups in,
+    quantizes and attends them, and copies O (and LSE) out, pipelined. Stream
+    ordered on the current CUDA stream: synchronise it before reading the
+    outputs. Returns host (o, lse)."""
+    for t in (q, k, v):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous BF16 host tensors")
+    B, Nq, H, D = q.shape
+    Nk = k.shape[1]
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, Nq, H, D), dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=pin)
+    lens = None
+    if k_lens is not None:
+        lens = torch.as_tensor(k_lens, dtype=torch.int32).contiguous()
+        if lens.is_cuda:
+            raise ValueError("k_lens must be a host tensor or a sequence")
+    d = _host_desc(q, k, v, out, lse, lens, fmt, softmax_scale, smooth_k, smooth_q,
+                   heads_per_group, num_splits, cta_mode)
+    need = int(_lib.sage_attention_host_workspace_bytes(ctypes.byref(d)))
+    if need == 0:
+        raise SageError(-1, "sage_attention_host_workspace_bytes")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    _check(_lib.sage_attention_host(ctypes.byref(d), _ptr(workspace), need, _stream()),
+           "sage_attention_host")
+    return out, lse
 
 
 def int8_codes(x_q: torch.Tensor) -> torch.Tensor:

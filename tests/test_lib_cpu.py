@@ -189,3 +189,52 @@ def test_format4_byte_counts():
     assert binding.sage_quantized_bytes(4, 2, B, N, H, D) == B * H * D * Np // 2  # E2M1 V^T
     assert binding.sage_quantized_bytes(4, 3, B, N, H, D) == B * H * Np * D // 32  # E8M0 V
     assert binding.sage_workspace_bytes(1, 4, B, H, N, N) == 0                     # no V maxima
+
+
+def _host_desc(**kw):
+    d = dict(fmt=0, B=1, Nq=300, Nk=500, H=5, D=128, q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20,
+             lse=1 << 20, k_lens=None, softmax_scale=0.0, smooth_k=0, smooth_q=0,
+             heads_per_group=0, num_splits=0, cta_mode=0)
+    d.update(kw)
+    return binding.HostAttention(**d)
+
+
+def test_host_attention_workspace_and_validation():
+    """sage_attention_host: its workspace is two slots of one head group's
+    buffers plus the key lengths (no CUDA call), and invalid calls are
+    rejected before any CUDA call."""
+    lib = binding.library()
+    size = lambda **kw: lib.sage_attention_host_workspace_bytes(ctypes.byref(_host_desc(**kw)))  # noqa: E731
+    B, Nq, Nk, D = 1, 300, 500, 128
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # one head per group, INT8: BF16 Q/K/V, codes, scales, V scales, O, LSE
+    slot = (r(B * Nq * D * 2) + 2 * r(B * Nk * D * 2) + r(384 * D * 2) + r(3 * 4) + r(512 * D * 2)
+            + r(4 * 4) + r(512 * D) + r(D * 4) + r(B * Nq * D * 2) + r(Nq * 4) + r(D * 4))
+    assert size(heads_per_group=1, num_splits=1) == 2 * slot + 256
+    # the split count is resolved for the whole shape; each group holds its partials
+    splits = 3
+    assert size(heads_per_group=1, num_splits=splits) == 2 * (slot + r(splits * Nq * (D + 1) * 4)) + 256
+    # grows with the group; by default about 5 groups, or about 20 when each
+    # head's attention outlasts its copies several times over (long sequences)
+    assert size(heads_per_group=2) > size(heads_per_group=1)
+    assert size(heads_per_group=0) == size(heads_per_group=1)  # H = 5 -> 5 groups of 1
+    assert size(H=40) == size(H=40, heads_per_group=8)
+    assert size(H=40, Nq=65520, Nk=65520) == size(H=40, Nq=65520, Nk=65520, heads_per_group=2)
+    # smoothing adds its buffers; invalid descriptions size to 0
+    assert size(smooth_k=1, smooth_q=1) > size()
+    for bad in (dict(D=64), dict(fmt=9), dict(smooth_k=1, fmt=1), dict(heads_per_group=6),
+                dict(heads_per_group=-1), dict(q=None), dict(o=None), dict(num_splits=65),
+                dict(cta_mode=3), dict(Nq=0), dict(smooth_q=2)):
+        assert size(**bad) == 0, bad
+    assert lib.sage_attention_host_workspace_bytes(None) == 0
+    # the call itself: the same checks, then the workspace, before any CUDA call
+    call = lambda ws, n, **kw: lib.sage_attention_host(ctypes.byref(_host_desc(**kw)), ws, n, None)  # noqa: E731
+    ws = ctypes.c_void_p(1 << 24)
+    assert lib.sage_attention_host(None, ws, 1 << 30, None) == -1
+    assert call(ws, 1 << 30, D=64) == -2
+    assert call(ws, 1 << 30, smooth_q=1, fmt=2) == -2
+    assert call(ws, 1 << 30, heads_per_group=9) == -1
+    assert call(ws, 1 << 30, softmax_scale=float("inf")) == -1
+    assert call(None, 1 << 30) == -3
+    assert call(ws, size() - 1) == -3
+    assert call(ctypes.c_void_p((1 << 24) + 16), 1 << 30) == -3  # 256-byte alignment
