@@ -51,10 +51,14 @@ constexpr float kLn2 = 0.693147180559945309f;
 // raised (and O, l rescaled by 2^(m_old - m_new)) only when a tile's ceil(max t)
 // exceeds m + kHeadroom; otherwise p8 = 2^(t - m + 8 - kHeadroom) <= 2^8 still
 // fits E4M3. Every p8 differs from the final-maximum encoding by an exact power
-// of two, so the two agree wherever both are normal E4M3 numbers (the band of
-// differing subnormals widens by at most kHeadroom binades, below 2^-12 of the
-// row maximum).
-constexpr float kHeadroom = 2.0f;
+// of two, so the two agree wherever both are normal E4M3 numbers (codes can
+// differ only below 2^(kHeadroom - 13) of the row maximum, where this encoding
+// is subnormal). A rescale waits for the tile's previous P V, and the tile's
+// next step waits for its slowest warp: with a headroom of 2 binades about one
+// 128-row tile step in five had a rescaling warp on Gaussian logits (row
+// maxima of later tiles often exceed the first tile's by more than 2), with 4
+// about one in five hundred.
+constexpr float kHeadroom = 4.0f;
 
 // Operand format of Q and K (V is FP8 E4M3 in both).
 template <int FMT>
