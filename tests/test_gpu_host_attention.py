@@ -44,6 +44,8 @@ CASES = [
     (0, 2, 3, 200, 160, [0, 160], 0, 0, False, True, 0),
     (0, 1, 4, 512, 512, None, 3, 0, False, False, 2),
     (0, 1, 9, 640, 1000, None, 0, 0, True, False, 0),
+    (0, 1, 1, 1, 1, None, 0, 0, False, False, 0),
+    (2, 3, 2, 129, 2, [2, 0, 1], 1, 0, False, False, 0),
 ]
 
 
